@@ -1,0 +1,161 @@
+/*
+ * axonn_fc.h -- C ABI of the GB300 FC-layer GEMM library (libaxonn_fc.so).
+ *
+ * What it computes.  The three matrix products of a fully-connected layer's
+ * training step, either on the whole layer or on one local block of
+ * Agarwal's 3D parallel matrix multiplication ("Parallelization of a matrix
+ * multiply in an FC layer with Agarwal's 3D parallel matrix multiplication
+ * algorithm ... G_x, G_y and G_z ... the three dimensions of the virtual grid
+ * topology" -- Figure 1 caption, "Democratizing AI: Open-source Scalable LLM
+ * Training on GPU-based Supercomputers"; the 4D grid G_data x G_x x G_y x G_z
+ * with collectives is described under "What carries the argument" in the
+ * pith.science review of arXiv 2502.08145):
+ *
+ *   forward          Y[T x N]  = X[T x K] . W[K x N]
+ *   data gradient    dX[T x K] = dY[T x N] . W^T
+ *   weight gradient  dW[K x N] = X^T . dY
+ *
+ * Inputs and outputs are bf16; products accumulate in fp32 on the tensor
+ * cores and are rounded once, to nearest even, when written as bf16.
+ *
+ * 3D grid.  T is split by G_z, K by G_x and N by G_y.  Block (x, y, z) owns
+ * X[Tz, Kx], W[Kx, Ny] and dY[Tz, Ny] and computes
+ *   fwd    Y^(x)_{z,y}  = X[Tz,Kx] . W[Kx,Ny]      (partials summed over x)
+ *   dgrad  dX^(y)_{z,x} = dY[Tz,Ny] . W[Kx,Ny]^T   (summed over y)
+ *   wgrad  dW^(z)_{x,y} = X[Tz,Kx]^T . dY[Tz,Ny]   (summed over z)
+ * A dimension D is cut into units of 8 elements: with U = ceil(D/8), block b
+ * of G gets floor(U/G) units plus one if b < U mod G, blocks are contiguous
+ * in order, and the last block is clipped at D (see axonn_block_range).
+ *
+ * Virtual grid (AXONN_VGRID).  All G_x*G_y*G_z block products run in one
+ * launch on this GPU; the partials of the reduced axis are written in fp32
+ * to the caller's workspace and summed in fixed order 0..G-1 by a second
+ * kernel, which stands in for the all-reduce / reduce-scatter of the grid.
+ *
+ * Conventions for every entry point below.
+ *  - Pointers are DEVICE pointers; the caller owns every buffer and the
+ *    stream.  The library never allocates device memory on a call; scratch
+ *    comes from the caller's workspace (axonn_fc_workspace_size).
+ *  - Layout: matrices are row-major with a leading dimension (row stride) in
+ *    elements.  Flag AXONN_A_T says the op's first operand (X for fwd and
+ *    wgrad, dY for dgrad) is stored transposed, i.e. as [K x T] / [N x T];
+ *    AXONN_B_T says the second operand (W for fwd and dgrad, dY for wgrad) is
+ *    stored transposed ([N x K] for W -- PyTorch's Linear layout -- or
+ *    [N x T] for dY).  Outputs are always row-major in their logical shape.
+ *  - Alignment: every base pointer 16-byte aligned; bf16 leading dimensions
+ *    multiples of 8, fp32 ones multiples of 4.  Otherwise AXONN_ERR_ALIGNMENT.
+ *  - Calls are asynchronous on `stream`.  A device-side timeout (a bounded
+ *    wait inside a kernel that expired) is reported by axonn_sync_status.
+ *  - Errors are status codes; axonn_last_error() gives a thread-local message.
+ *    No C++ exception crosses this boundary.
+ *  - Empty outputs (an extent of 0) return AXONN_OK and touch nothing; an
+ *    empty reduction range writes zeros (leaves C unchanged with
+ *    AXONN_ACCUM_F32).
+ */
+#ifndef AXONN_FC_H_
+#define AXONN_FC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  AXONN_OK = 0,
+  AXONN_ERR_INVALID_ARG = 1,  /* bad size, grid, coordinate, flag or pointer */
+  AXONN_ERR_ALIGNMENT = 2,    /* pointer or leading dimension misaligned */
+  AXONN_ERR_UNSUPPORTED = 3,  /* valid request this build cannot run */
+  AXONN_ERR_WORKSPACE = 4,    /* workspace missing or too small */
+  AXONN_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
+  AXONN_ERR_TIMEOUT = 6       /* a bounded device-side wait expired */
+} axonn_status_t;
+
+typedef enum { AXONN_OP_FWD = 0, AXONN_OP_DGRAD = 1, AXONN_OP_WGRAD = 2 } axonn_op_t;
+
+/* Layer sizes, grid and block coordinate.  A full-layer product is the grid
+ * 1x1x1 at (0,0,0).  gx, gy, gz >= 1; 0 <= x < gx etc. */
+typedef struct {
+  int64_t T, K, N;
+  int32_t gx, gy, gz;
+  int32_t x, y, z;
+} axonn_fc_shape_t;
+
+/* Flags (bitwise or). */
+#define AXONN_A_T 0x1u            /* first operand stored transposed */
+#define AXONN_B_T 0x2u            /* second operand stored transposed */
+#define AXONN_ACCUM_F32 0x4u      /* output is fp32 and the result is added */
+#define AXONN_VGRID 0x8u          /* all blocks + on-device partial sum */
+#define AXONN_FULL_OPERANDS 0x10u /* block mode: pointers are full matrices */
+#define AXONN_OUT_F32 0x20u       /* output is fp32, overwritten */
+
+/*
+ * Forward product Y = X . W of the layer, of block (x,y,z), or of the whole
+ * virtual grid.
+ *   X   first operand, [T x K] (or [K x T] with AXONN_A_T), leading dim ldx
+ *   W   second operand, [K x N] (or [N x K] with AXONN_B_T), leading dim ldw
+ *   Y   output [T x N], leading dim ldy; bf16 unless AXONN_ACCUM_F32 /
+ *       AXONN_OUT_F32 make it fp32
+ *   Block mode (no AXONN_VGRID, grid larger than 1): without
+ *   AXONN_FULL_OPERANDS the pointers address the block's own shards
+ *   (X_blk [Tz x Kx], W_blk [Kx x Ny], Y_blk [Tz x Ny], each with its ld);
+ *   with it they address the full matrices and the block is located by its
+ *   offsets, its partial written at Y[Tz, Ny].
+ *   ws / ws_bytes: device workspace, needed only with AXONN_VGRID when
+ *   G_x > 1 (size from axonn_fc_workspace_size); may be NULL / 0 otherwise.
+ */
+axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw,
+                            int64_t ldy, const axonn_fc_shape_t* shape, uint32_t flags,
+                            void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Data gradient dX = dY . W^T.  dY [T x N] (AXONN_A_T: [N x T]), W [K x N]
+ * (AXONN_B_T: [N x K]), dX [T x K].  Block (x,y,z) yields dX^(y)_{z,x};
+ * the virtual grid sums over y.  Other arguments as for axonn_fc_fwd. */
+axonn_status_t axonn_fc_dgrad(const void* dY, const void* W, void* dX, int64_t lddy,
+                              int64_t ldw, int64_t lddx, const axonn_fc_shape_t* shape,
+                              uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Weight gradient dW = X^T . dY.  X [T x K] (AXONN_A_T: [K x T]), dY
+ * [T x N] (AXONN_B_T: [N x T]), dW [K x N].  Block (x,y,z) yields
+ * dW^(z)_{x,y}; the virtual grid sums over z.  AXONN_ACCUM_F32 gives the
+ * fp32 main-gradient update dW += X^T . dY. */
+axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t ldx,
+                              int64_t lddy, int64_t lddw, const axonn_fc_shape_t* shape,
+                              uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Workspace bytes an op needs with these flags (0 when none).  `op` is an
+ * axonn_op_t.  Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
+axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
+                                       size_t* bytes);
+
+/* Rows [*start, *stop) of block b when a dimension D is cut into G blocks by
+ * the 8-element-unit rule above.  Host-only, no GPU needed. */
+axonn_status_t axonn_block_range(int64_t D, int32_t G, int32_t b, int64_t* start, int64_t* stop);
+
+/* Waits for `stream`, then reports (and clears) a device-side timeout
+ * recorded by any kernel of this library on the current device since the
+ * last call: AXONN_ERR_TIMEOUT, AXONN_ERR_CUDA if the stream failed, else
+ * AXONN_OK.  *detail (may be NULL) receives the raw error word. */
+axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail);
+
+/* Upper bound, in nanoseconds, on any single wait inside the kernels
+ * (default 4e9).  Process-wide; applies to launches made afterwards. */
+void axonn_set_wait_timeout_ns(uint64_t ns);
+
+/* Test hook: 1 makes the next launches' producer withhold all operand
+ * loads, so the bounded waits expire and AXONN_ERR_TIMEOUT is reported;
+ * 0 restores normal operation.  Never needed in production. */
+void axonn_debug_set_inject(int mode);
+
+/* Thread-local description of the last error returned on this thread. */
+const char* axonn_last_error(void);
+
+/* Library version string. */
+const char* axonn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AXONN_FC_H_ */

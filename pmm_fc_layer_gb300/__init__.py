@@ -1,0 +1,204 @@
+"""Python binding of libaxonn_fc.so -- argument marshalling only.
+
+Every function named ``axonn_*`` here calls the C entry point of the same
+name (declared in include/axonn_fc.h); all arithmetic runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  There
+is no fallback: if the library is missing or cannot load, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+OP_FWD, OP_DGRAD, OP_WGRAD = 0, 1, 2
+OPS = {"fwd": OP_FWD, "dgrad": OP_DGRAD, "wgrad": OP_WGRAD}
+
+A_T = 0x1
+B_T = 0x2
+ACCUM_F32 = 0x4
+VGRID = 0x8
+FULL_OPERANDS = 0x10
+OUT_F32 = 0x20
+
+OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
+STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]
+
+EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_workspace_size",
+           "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
+           "axonn_debug_set_inject", "axonn_last_error", "axonn_version")
+
+
+class AxonnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        self.status = status
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"AXONN_ERR_{name}: {message}")
+
+
+class Shape(ctypes.Structure):
+    """axonn_fc_shape_t: layer sizes, 3D grid and block coordinate."""
+    _fields_ = [("T", ctypes.c_int64), ("K", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("gx", ctypes.c_int32), ("gy", ctypes.c_int32), ("gz", ctypes.c_int32),
+                ("x", ctypes.c_int32), ("y", ctypes.c_int32), ("z", ctypes.c_int32)]
+
+    def __init__(self, T, K, N, grid=(1, 1, 1), coords=(0, 0, 0)):
+        super().__init__(T, K, N, *grid, *coords)
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Load the built library (raises if it is absent)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libaxonn_fc.so not built at {p}; run pmm_fc_layer_gb300.build.build()")
+        lib = ctypes.CDLL(p)
+        vp, i64, u32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint32, ctypes.c_int32
+        sz = ctypes.c_size_t
+        sig = [vp, vp, vp, i64, i64, i64, ctypes.POINTER(Shape), u32, vp, sz, vp]
+        for name in ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad"):
+            f = getattr(lib, name)
+            f.argtypes = sig
+            f.restype = ctypes.c_int
+        lib.axonn_fc_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(Shape), u32,
+                                                ctypes.POINTER(sz)]
+        lib.axonn_fc_workspace_size.restype = ctypes.c_int
+        lib.axonn_block_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.axonn_block_range.restype = ctypes.c_int
+        lib.axonn_sync_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
+        lib.axonn_sync_status.restype = ctypes.c_int
+        lib.axonn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
+        lib.axonn_set_wait_timeout_ns.restype = None
+        lib.axonn_debug_set_inject.argtypes = [ctypes.c_int]
+        lib.axonn_debug_set_inject.restype = None
+        lib.axonn_last_error.restype = ctypes.c_char_p
+        lib.axonn_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != OK:
+        raise AxonnError(status, load().axonn_last_error().decode())
+
+
+def _ptr(t) -> int:
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _ld(t, ld):
+    if ld is not None:
+        return int(ld)
+    if t is None or isinstance(t, int):
+        return 0
+    if t.dim() != 2 or (t.stride(1) != 1 and t.size(1) > 1):
+        raise ValueError("operands must be 2-D with unit column stride")
+    return t.stride(0)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _call(name, P, Q, C, shape, flags, ws, ldp, ldq, ldc, stream):
+    lib = load()
+    ws_bytes = 0
+    if ws is not None and not isinstance(ws, int):
+        ws_bytes = ws.numel() * ws.element_size()
+    elif isinstance(ws, int):
+        raise ValueError("pass the workspace as a tensor")
+    st = getattr(lib, name)(_ptr(P), _ptr(Q), _ptr(C), _ld(P, ldp), _ld(Q, ldq), _ld(C, ldc),
+                            ctypes.byref(shape), flags, _ptr(ws), ws_bytes, _stream(stream))
+    _check(st)
+
+
+def axonn_fc_fwd(X, W, Y, shape: Shape, flags: int = 0, ws=None, ldx=None, ldw=None, ldy=None,
+                 stream=None):
+    """Y = X . W (layer, block or virtual grid); see include/axonn_fc.h."""
+    _call("axonn_fc_fwd", X, W, Y, shape, flags, ws, ldx, ldw, ldy, stream)
+
+
+def axonn_fc_dgrad(dY, W, dX, shape: Shape, flags: int = 0, ws=None, lddy=None, ldw=None,
+                   lddx=None, stream=None):
+    """dX = dY . W^T (layer, block or virtual grid)."""
+    _call("axonn_fc_dgrad", dY, W, dX, shape, flags, ws, lddy, ldw, lddx, stream)
+
+
+def axonn_fc_wgrad(X, dY, dW, shape: Shape, flags: int = 0, ws=None, ldx=None, lddy=None,
+                   lddw=None, stream=None):
+    """dW = X^T . dY (layer, block or virtual grid)."""
+    _call("axonn_fc_wgrad", X, dY, dW, shape, flags, ws, ldx, lddy, lddw, stream)
+
+
+def axonn_fc_workspace_size(op, shape: Shape, flags: int = 0) -> int:
+    op = OPS.get(op, op)
+    n = ctypes.c_size_t(0)
+    _check(load().axonn_fc_workspace_size(int(op), ctypes.byref(shape), flags, ctypes.byref(n)))
+    return n.value
+
+
+def axonn_block_range(D: int, G: int, b: int):
+    s, e = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(load().axonn_block_range(D, G, b, ctypes.byref(s), ctypes.byref(e)))
+    return s.value, e.value
+
+
+def axonn_sync_status(stream=None, raise_on_error: bool = True):
+    """Waits for the stream and returns (status, detail word)."""
+    detail = ctypes.c_uint64(0)
+    st = load().axonn_sync_status(_stream(stream), ctypes.byref(detail))
+    if raise_on_error:
+        _check(st)
+    return st, detail.value
+
+
+def axonn_set_wait_timeout_ns(ns: int):
+    load().axonn_set_wait_timeout_ns(int(ns))
+
+
+def axonn_debug_set_inject(mode: int):
+    load().axonn_debug_set_inject(int(mode))
+
+
+def axonn_last_error() -> str:
+    return load().axonn_last_error().decode()
+
+
+def axonn_version() -> str:
+    return load().axonn_version().decode()
+
+
+# ---------------------------------------------------------------- helpers
+def out_shape(op, T, K, N):
+    """Logical output shape of an op on the full layer."""
+    op = OPS.get(op, op)
+    return {OP_FWD: (T, N), OP_DGRAD: (T, K), OP_WGRAD: (K, N)}[op]
+
+
+def call(op, P, Q, C, shape: Shape, flags: int = 0, ws=None, stream=None):
+    """Dispatch by op name ('fwd' | 'dgrad' | 'wgrad') to the entry point."""
+    op = OPS.get(op, op)
+    fn = {OP_FWD: axonn_fc_fwd, OP_DGRAD: axonn_fc_dgrad, OP_WGRAD: axonn_fc_wgrad}[op]
+    fn(P, Q, C, shape, flags, ws, stream=stream)

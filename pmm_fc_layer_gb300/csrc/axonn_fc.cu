@@ -1,0 +1,523 @@
+// C ABI of the FC-layer GEMM library: argument checks, 3D-grid block
+// resolution, TMA tensor-map encoding and kernel launches.  Declarations and
+// the contract of every entry point are in include/axonn_fc.h.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "axonn_fc.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using axonn::GemmParams;
+using axonn::ProblemDesc;
+
+constexpr int kMaxProblems = 64;  // largest virtual grid Gx*Gy*Gz
+
+thread_local std::string t_last_error;
+std::atomic<uint64_t> g_timeout_ns{4000000000ULL};
+std::atomic<int> g_inject{0};
+
+axonn_status_t fail(axonn_status_t s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return s;
+}
+
+axonn_status_t ok() {
+  t_last_error.clear();
+  return AXONN_OK;
+}
+
+// ------------------------------------------------------------------ driver
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Per-device facts and one-time kernel attributes.
+struct DeviceState {
+  int sms = 0;
+  bool attrs_set = false;
+};
+std::mutex g_dev_mu;
+std::vector<DeviceState> g_devs;
+
+template <int BN, int STAGES, int MAXP>
+void* kernel_ptr() {
+  return reinterpret_cast<void*>(&axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>);
+}
+
+template <int BN, int STAGES, int MAXP>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              axonn::SmemLayout<BN, STAGES>::kBytes);
+}
+
+axonn_status_t device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (static_cast<int>(g_devs.size()) <= dev) g_devs.resize(dev + 1);
+  DeviceState& d = g_devs[dev];
+  if (!d.attrs_set) {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (major != 10 || minor != 3)
+      return fail(AXONN_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
+                  dev, major, minor);
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    cudaError_t es[] = {set_smem_attr<256, 4, 1>(), set_smem_attr<256, 4, kMaxProblems>(),
+                        set_smem_attr<128, 6, 1>(), set_smem_attr<128, 6, kMaxProblems>()};
+    for (cudaError_t x : es)
+      if (x != cudaSuccess)
+        return fail(AXONN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(x));
+    d.attrs_set = true;
+  }
+  *out = &d;
+  return AXONN_OK;
+}
+
+// ------------------------------------------------------------------ grid
+void split_range(int64_t D, int64_t G, int64_t b, int64_t* s, int64_t* e) {
+  const int64_t units = (D + 7) / 8;
+  const int64_t base = units / G, rem = units % G;
+  const int64_t start = 8 * (b * base + (b < rem ? b : rem));
+  const int64_t n = base + (b < rem ? 1 : 0);
+  *s = start < D ? start : D;
+  const int64_t stop = start + 8 * n;
+  *e = stop < D ? stop : D;
+}
+
+struct Range {
+  int64_t s = 0, e = 0;
+  int64_t len() const { return e - s; }
+};
+
+// The op as C[M x N] = A[M x R] . B[R x N] over full logical matrices.
+struct OpView {
+  const char* A;
+  int64_t lda;
+  bool a_mn;  // A(i, r) at A + (r*lda + i) (M-contiguous) else A + (i*lda + r)
+  const char* B;
+  int64_t ldb;
+  bool b_mn;  // B(r, j) at B + (r*ldb + j) (N-contiguous) else B + (j*ldb + r)
+  char* C;
+  int64_t ldc;
+  int64_t M, N, R;
+};
+
+// Logical ranges of block (x,y,z): output rows, reduced range, output cols.
+void block_ranges(int op, const axonn_fc_shape_t& s, int x, int y, int z, Range* rows, Range* red,
+                  Range* cols) {
+  Range Tz, Kx, Ny;
+  split_range(s.T, s.gz, z, &Tz.s, &Tz.e);
+  split_range(s.K, s.gx, x, &Kx.s, &Kx.e);
+  split_range(s.N, s.gy, y, &Ny.s, &Ny.e);
+  if (op == AXONN_OP_FWD) {  // Y[Tz,Ny] += X[Tz,Kx] W[Kx,Ny]
+    *rows = Tz; *red = Kx; *cols = Ny;
+  } else if (op == AXONN_OP_DGRAD) {  // dX[Tz,Kx] += dY[Tz,Ny] W[Kx,Ny]^T
+    *rows = Tz; *red = Ny; *cols = Kx;
+  } else {  // dW[Kx,Ny] += X[Tz,Kx]^T dY[Tz,Ny]
+    *rows = Kx; *red = Tz; *cols = Ny;
+  }
+}
+
+int reduce_extent(int op, const axonn_fc_shape_t& s) {
+  return op == AXONN_OP_FWD ? s.gx : (op == AXONN_OP_DGRAD ? s.gy : s.gz);
+}
+
+int reduce_coord(int op, int x, int y, int z) {
+  return op == AXONN_OP_FWD ? x : (op == AXONN_OP_DGRAD ? y : z);
+}
+
+void full_dims(int op, const axonn_fc_shape_t& s, int64_t* M, int64_t* N, int64_t* R) {
+  if (op == AXONN_OP_FWD) { *M = s.T; *N = s.N; *R = s.K; }
+  else if (op == AXONN_OP_DGRAD) { *M = s.T; *N = s.K; *R = s.N; }
+  else { *M = s.K; *N = s.N; *R = s.T; }
+}
+
+constexpr uint32_t kKnownFlags = AXONN_A_T | AXONN_B_T | AXONN_ACCUM_F32 | AXONN_VGRID |
+                                 AXONN_FULL_OPERANDS | AXONN_OUT_F32;
+
+axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
+  if (op < AXONN_OP_FWD || op > AXONN_OP_WGRAD) return fail(AXONN_ERR_INVALID_ARG, "bad op %d", op);
+  if (!s) return fail(AXONN_ERR_INVALID_ARG, "shape is NULL");
+  if (flags & ~kKnownFlags) return fail(AXONN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnownFlags);
+  if ((flags & AXONN_ACCUM_F32) && (flags & AXONN_OUT_F32))
+    return fail(AXONN_ERR_INVALID_ARG, "AXONN_ACCUM_F32 and AXONN_OUT_F32 are exclusive");
+  if (s->T < 0 || s->K < 0 || s->N < 0) return fail(AXONN_ERR_INVALID_ARG, "negative extent");
+  const int64_t lim = (int64_t{1} << 31) - 256;
+  if (s->T > lim || s->K > lim || s->N > lim) return fail(AXONN_ERR_UNSUPPORTED, "extent above 2^31");
+  if (s->gx < 1 || s->gy < 1 || s->gz < 1) return fail(AXONN_ERR_INVALID_ARG, "grid extents must be >= 1");
+  if (static_cast<int64_t>(s->gx) * s->gy * s->gz > kMaxProblems)
+    return fail(AXONN_ERR_UNSUPPORTED, "grid %dx%dx%d has more than %d blocks", s->gx, s->gy, s->gz,
+                kMaxProblems);
+  if (!(flags & AXONN_VGRID)) {
+    if (s->x < 0 || s->x >= s->gx || s->y < 0 || s->y >= s->gy || s->z < 0 || s->z >= s->gz)
+      return fail(AXONN_ERR_INVALID_ARG, "block (%d,%d,%d) outside grid %dx%dx%d", s->x, s->y, s->z,
+                  s->gx, s->gy, s->gz);
+  }
+  return AXONN_OK;
+}
+
+size_t vgrid_ws_bytes(int op, const axonn_fc_shape_t& s, uint32_t flags) {
+  if (!(flags & AXONN_VGRID)) return 0;
+  const int G = reduce_extent(op, s);
+  if (G <= 1) return 0;
+  int64_t M, N, R;
+  full_dims(op, s, &M, &N, &R);
+  const int64_t ldp = (N + 7) / 8 * 8;
+  return static_cast<size_t>(G) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * 4u;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks one stored operand: pointer, leading dimension, alignment.
+axonn_status_t check_operand(const char* name, const void* p, int64_t ld, int64_t rows,
+                             int64_t cols) {
+  if (rows == 0 || cols == 0) return AXONN_OK;
+  if (!p) return fail(AXONN_ERR_INVALID_ARG, "%s is NULL", name);
+  if (ld < cols) return fail(AXONN_ERR_INVALID_ARG, "%s: leading dimension %lld < row length %lld", name,
+                             (long long)ld, (long long)cols);
+  if (!aligned16(p)) return fail(AXONN_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+  if (ld % 8 != 0) return fail(AXONN_ERR_ALIGNMENT, "%s: leading dimension %lld is not a multiple of 8", name,
+                               (long long)ld);
+  if (ld * 2 >= (int64_t{1} << 40)) return fail(AXONN_ERR_UNSUPPORTED, "%s: stride too large", name);
+  return AXONN_OK;
+}
+
+axonn_status_t encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                         int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2u};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return AXONN_OK;
+}
+
+// tcgen05 instruction descriptor, kind::f16: bf16 A and B, fp32 D.
+uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// One block product to run: operand bases and extents, output and mode.
+struct Block {
+  const char* A;
+  const char* B;
+  char* C;
+  int64_t ldc;
+  int64_t M, N, R;
+  int out_mode;
+};
+
+struct LaunchPlan {
+  int BN = 256;
+  std::vector<Block> blocks;
+};
+
+template <int BN, int STAGES, int MAXP>
+axonn_status_t launch_gemm(const OpView& v, const std::vector<Block>& blocks, int sms,
+                           cudaStream_t stream) {
+  static_assert(sizeof(GemmParams<MAXP>) < 32000, "kernel parameter space");
+  GemmParams<MAXP> P;
+  memset(&P, 0, sizeof(P));
+  int tiles = 0, np = 0;
+  for (const Block& b : blocks) {
+    if (b.M == 0 || b.N == 0) continue;
+    if (np >= MAXP) return fail(AXONN_ERR_UNSUPPORTED, "too many block products");
+    ProblemDesc& d = P.prob[np];
+    d.C = b.C;
+    d.ldc = b.ldc;
+    d.M = static_cast<int32_t>(b.M);
+    d.N = static_cast<int32_t>(b.N);
+    d.R = static_cast<int32_t>(b.R);
+    d.tiles_m = static_cast<int32_t>((b.M + axonn::kBM - 1) / axonn::kBM);
+    d.tiles_n = static_cast<int32_t>((b.N + BN - 1) / BN);
+    d.tile_start = tiles;
+    d.num_k = static_cast<int32_t>((b.R + axonn::kBK - 1) / axonn::kBK);
+    d.a_mn = v.a_mn;
+    d.b_mn = v.b_mn;
+    d.idesc = make_idesc(axonn::kBM, BN, v.a_mn, v.b_mn);
+    d.out_mode = b.out_mode;
+    if (b.R > 0) {
+      axonn_status_t s;
+      if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, 64);
+      else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, 64, axonn::kBM);
+      if (s != AXONN_OK) return s;
+      if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, 64);
+      else s = encode_2d(&P.tmb[np], b.B, b.R, b.N, v.ldb, 64, BN);
+      if (s != AXONN_OK) return s;
+    }
+    tiles += d.tiles_m * d.tiles_n;
+    ++np;
+  }
+  if (np == 0) return AXONN_OK;
+  P.num_problems = np;
+  P.total_tiles = tiles;
+  P.group_m = 16;
+  P.inject = g_inject.load();
+  P.timeout_ns = g_timeout_ns.load();
+  const int grid = tiles < sms ? tiles : sms;
+  axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>
+      <<<grid, axonn::kThreads, axonn::SmemLayout<BN, STAGES>::kBytes, stream>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  return AXONN_OK;
+}
+
+axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, int sms, cudaStream_t stream) {
+  const bool many = plan.blocks.size() > 1;
+  if (plan.BN == 256)
+    return many ? launch_gemm<256, 4, kMaxProblems>(v, plan.blocks, sms, stream)
+                : launch_gemm<256, 4, 1>(v, plan.blocks, sms, stream);
+  return many ? launch_gemm<128, 6, kMaxProblems>(v, plan.blocks, sms, stream)
+              : launch_gemm<128, 6, 1>(v, plan.blocks, sms, stream);
+}
+
+int choose_bn(const std::vector<Block>& blocks, int sms) {
+  int64_t tiles256 = 0, maxN = 0;
+  for (const Block& b : blocks) {
+    tiles256 += ((b.M + 127) / 128) * ((b.N + 255) / 256);
+    if (b.N > maxN) maxN = b.N;
+  }
+  if (maxN <= 128 || tiles256 < sms / 2) return 128;
+  return 256;
+}
+
+// Shared body of the three entry points.  P and Q are the op's first and
+// second stored operands, C its output.
+axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp, int64_t ldq,
+                     int64_t ldc, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                     size_t ws_bytes, cudaStream_t stream) {
+  axonn_status_t st = check_shape(op, shape, flags);
+  if (st != AXONN_OK) return st;
+  const axonn_fc_shape_t& s = *shape;
+  const bool vgrid = (flags & AXONN_VGRID) != 0;
+  const bool single = s.gx * s.gy * s.gz == 1;
+  const bool full_ops = vgrid || single || (flags & AXONN_FULL_OPERANDS);
+  const bool a_t = (flags & AXONN_A_T) != 0, b_t = (flags & AXONN_B_T) != 0;
+  const bool out_f32 = (flags & (AXONN_ACCUM_F32 | AXONN_OUT_F32)) != 0;
+  const int user_mode = (flags & AXONN_ACCUM_F32) ? axonn::kOutF32Accum
+                        : (flags & AXONN_OUT_F32) ? axonn::kOutF32
+                                                  : axonn::kOutBF16;
+
+  // Logical extents the caller's buffers hold.
+  int64_t M, N, R;
+  full_dims(op, s, &M, &N, &R);
+  Range rows{0, M}, red{0, R}, cols{0, N};
+  if (!vgrid && !single) block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
+  const int64_t hM = full_ops ? M : rows.len();
+  const int64_t hR = full_ops ? R : red.len();
+  const int64_t hN = full_ops ? N : cols.len();
+
+  // Map the op onto C = A . B with operand major-ness (see OpView).
+  OpView v;
+  v.A = static_cast<const char*>(P);
+  v.lda = ldp;
+  v.B = static_cast<const char*>(Q);
+  v.ldb = ldq;
+  v.C = static_cast<char*>(C);
+  v.ldc = ldc;
+  v.M = hM; v.N = hN; v.R = hR;
+  if (op == AXONN_OP_FWD) {         // A = X, B = W
+    v.a_mn = a_t;                   // X stored [K x T]
+    v.b_mn = !b_t;                  // W stored [K x N] is N-contiguous
+  } else if (op == AXONN_OP_DGRAD) {  // A = dY, B = W^T
+    v.a_mn = a_t;                   // dY stored [N x T]
+    v.b_mn = b_t;                   // W^T(n, k): W stored [N x K] is K(=cols)-contiguous
+  } else {                          // A = X^T, B = dY
+    v.a_mn = !a_t;                  // X stored [T x K] is K(=rows)-contiguous
+    v.b_mn = !b_t;                  // dY stored [T x N] is N-contiguous
+  }
+
+  // Validate the stored operands as the caller laid them out.
+  const char* pn = op == AXONN_OP_DGRAD ? "dY" : "X";
+  const char* qn = op == AXONN_OP_WGRAD ? "dY" : "W";
+  st = v.a_mn ? check_operand(pn, P, ldp, hR, hM) : check_operand(pn, P, ldp, hM, hR);
+  if (st != AXONN_OK) return st;
+  st = v.b_mn ? check_operand(qn, Q, ldq, hR, hN) : check_operand(qn, Q, ldq, hN, hR);
+  if (st != AXONN_OK) return st;
+  if (hM > 0 && hN > 0) {
+    if (!C) return fail(AXONN_ERR_INVALID_ARG, "output is NULL");
+    if (ldc < hN) return fail(AXONN_ERR_INVALID_ARG, "output leading dimension %lld < %lld", (long long)ldc,
+                              (long long)hN);
+    if (!aligned16(C)) return fail(AXONN_ERR_ALIGNMENT, "output is not 16-byte aligned");
+    if (ldc % (out_f32 ? 4 : 8) != 0)
+      return fail(AXONN_ERR_ALIGNMENT, "output leading dimension %lld misaligned", (long long)ldc);
+  }
+  if (hM == 0 || hN == 0) return ok();
+
+  const int G = reduce_extent(op, s);
+  const bool partials = vgrid && G > 1;
+  int64_t ldpart = 0;
+  if (partials) {
+    const size_t need = vgrid_ws_bytes(op, s, flags);
+    if (!ws || ws_bytes < need)
+      return fail(AXONN_ERR_WORKSPACE, "virtual grid needs %zu workspace bytes, got %zu", need, ws_bytes);
+    if (!aligned16(ws)) return fail(AXONN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
+    ldpart = (N + 7) / 8 * 8;
+  }
+
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+
+  auto a_at = [&](int64_t i, int64_t r) {
+    return v.A + 2 * (v.a_mn ? r * v.lda + i : i * v.lda + r);
+  };
+  auto b_at = [&](int64_t r, int64_t j) {
+    return v.B + 2 * (v.b_mn ? r * v.ldb + j : j * v.ldb + r);
+  };
+  const size_t celt = out_f32 ? 4 : 2;
+
+  LaunchPlan plan;
+  if (vgrid) {
+    for (int x = 0; x < s.gx; ++x)
+      for (int y = 0; y < s.gy; ++y)
+        for (int z = 0; z < s.gz; ++z) {
+          Range br, bred, bc;
+          block_ranges(op, s, x, y, z, &br, &bred, &bc);
+          Block b;
+          b.A = a_at(br.s, bred.s);
+          b.B = b_at(bred.s, bc.s);
+          b.M = br.len(); b.N = bc.len(); b.R = bred.len();
+          if (partials) {
+            const int g = reduce_coord(op, x, y, z);
+            b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(g) * M * ldpart + br.s * ldpart + bc.s);
+            b.ldc = ldpart;
+            b.out_mode = axonn::kOutF32;
+          } else {
+            b.C = v.C + celt * (br.s * ldc + bc.s);
+            b.ldc = ldc;
+            b.out_mode = user_mode;
+          }
+          plan.blocks.push_back(b);
+        }
+  } else {
+    Block b;
+    const bool offs = full_ops && !single;
+    b.A = offs ? a_at(rows.s, red.s) : v.A;
+    b.B = offs ? b_at(red.s, cols.s) : v.B;
+    b.C = offs ? v.C + celt * (rows.s * ldc + cols.s) : v.C;
+    b.ldc = ldc;
+    b.M = rows.len(); b.N = cols.len(); b.R = red.len();
+    b.out_mode = user_mode;
+    plan.blocks.push_back(b);
+  }
+  plan.BN = choose_bn(plan.blocks, dev->sms);
+  st = run_blocks(v, plan, dev->sms, stream);
+  if (st != AXONN_OK) return st;
+
+  if (partials) {
+    const int64_t groups = M * ((N + 7) / 8);
+    int64_t nblk = (groups + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(dev->sms) * 8;
+    if (nblk > cap) nblk = cap;
+    axonn::vgrid_reduce_kernel<<<static_cast<int>(nblk), 256, 0, stream>>>(
+        static_cast<const float*>(ws), G, M * ldpart, ldpart, static_cast<int>(M), static_cast<int>(N), C,
+        ldc, user_mode);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "reduction launch: %s", cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw, int64_t ldy,
+                            const axonn_fc_shape_t* shape, uint32_t flags, void* ws, size_t ws_bytes,
+                            cudaStream_t stream) {
+  return fc_op(AXONN_OP_FWD, X, W, Y, ldx, ldw, ldy, shape, flags, ws, ws_bytes, stream);
+}
+
+axonn_status_t axonn_fc_dgrad(const void* dY, const void* W, void* dX, int64_t lddy, int64_t ldw,
+                              int64_t lddx, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  return fc_op(AXONN_OP_DGRAD, dY, W, dX, lddy, ldw, lddx, shape, flags, ws, ws_bytes, stream);
+}
+
+axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t ldx, int64_t lddy,
+                              int64_t lddw, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                              size_t ws_bytes, cudaStream_t stream) {
+  return fc_op(AXONN_OP_WGRAD, X, dY, dW, ldx, lddy, lddw, shape, flags, ws, ws_bytes, stream);
+}
+
+axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
+                                       size_t* bytes) {
+  if (!bytes) return fail(AXONN_ERR_INVALID_ARG, "bytes is NULL");
+  axonn_status_t st = check_shape(op, shape, flags);
+  if (st != AXONN_OK) return st;
+  *bytes = vgrid_ws_bytes(op, *shape, flags);
+  return ok();
+}
+
+axonn_status_t axonn_block_range(int64_t D, int32_t G, int32_t b, int64_t* start, int64_t* stop) {
+  if (!start || !stop) return fail(AXONN_ERR_INVALID_ARG, "NULL output");
+  if (D < 0 || G < 1 || b < 0 || b >= G) return fail(AXONN_ERR_INVALID_ARG, "bad D/G/b");
+  split_range(D, G, b, start, stop);
+  return ok();
+}
+
+axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail) {
+  if (detail) *detail = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
+  unsigned long long word = 0;
+  e = cudaMemcpyFromSymbolAsync(&word, axonn::g_status_word, sizeof(word), 0, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (word == 0) return ok();
+  const unsigned long long zero = 0;
+  e = cudaMemcpyToSymbolAsync(axonn::g_status_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (detail) *detail = word;
+  return fail(AXONN_ERR_TIMEOUT, "device wait expired: CTA %llu, site %llu", (word >> 8) & 0xFFFFFFull,
+              word & 0xFFull);
+}
+
+void axonn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
+
+void axonn_debug_set_inject(int mode) { g_inject.store(mode); }
+
+const char* axonn_last_error(void) { return t_last_error.c_str(); }
+
+const char* axonn_version(void) { return "axonn_fc 0.1 (sm_103a tcgen05)"; }
+
+}  // extern "C"

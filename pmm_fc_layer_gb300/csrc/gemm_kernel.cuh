@@ -1,0 +1,461 @@
+// Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores, plus the
+// fixed-order reduction of 3D-grid partial products.
+//
+//   C[M x N] (op)= A[M x R] . B[R x N]      bf16 in, fp32 accumulate in TMEM
+//
+// One launch processes a list of independent "problems" (one per block
+// product of the 3D grid, or a single full-layer GEMM).  Every problem has
+// its own pair of TMA tensor maps whose extents are the block's own extents,
+// so tile boxes that run past a block edge read zeros exactly as a GPU that
+// held only that shard would.
+//
+// CTA = 6 warps, one CTA per SM, persistent over a static tile schedule:
+//   warp 0      TMA producer (one thread): smem ring of STAGES x (A | B) tiles
+//   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma 128 x BN x 16
+//   warps 2..5  epilogue: tcgen05.ld -> fp32 -> bf16 RNE (or fp32) -> global
+// The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
+// of tile i overlaps the mainloop of tile i+1.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
+// records an error word in device memory, all roles leave their loops, the
+// producer's outstanding copies and the issued MMAs are drained (each drain
+// bounded too) and TMEM is released before the CTA exits.
+#pragma once
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace axonn {
+
+constexpr int kBM = 128;       // rows per tile (UMMA M, one CTA)
+constexpr int kBK = 64;        // reduction depth per stage: 64 bf16 = 128 B
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kEpiWarps = 4;
+
+// Output modes of the epilogue.
+enum OutMode : int32_t { kOutBF16 = 0, kOutF32 = 1, kOutF32Accum = 2 };
+
+struct ProblemDesc {
+  void* C;            // output base (element (0,0) of this problem)
+  int64_t ldc;        // output row stride, elements
+  int32_t M, N, R;    // problem extents
+  int32_t tiles_m, tiles_n;
+  int32_t tile_start;  // first global tile index of this problem
+  int32_t num_k;       // ceil(R / kBK)
+  uint32_t idesc;      // tcgen05 instruction descriptor
+  int32_t a_mn;        // A stored M-contiguous (else R-contiguous)
+  int32_t b_mn;        // B stored N-contiguous (else R-contiguous)
+  int32_t out_mode;
+  int32_t pad_;
+};
+
+template <int MAXP>
+struct GemmParams {
+  CUtensorMap tma[MAXP];  // A operand of each problem
+  CUtensorMap tmb[MAXP];  // B operand of each problem
+  ProblemDesc prob[MAXP];
+  int32_t num_problems;
+  int32_t total_tiles;
+  int32_t group_m;     // tile rows per rasterisation group
+  int32_t inject;      // test-only: 1 = the producer withholds every load
+  uint64_t timeout_ns; // bound on any single mbarrier wait
+};
+
+// Device-side error word: 0 = no error.  Layout of a timeout record:
+// bits 32..39 = 0x7E, bits 8..31 = CTA index, bits 0..7 = wait site.
+__device__ unsigned long long g_status_word;
+
+enum WaitSite : uint32_t {
+  kSiteProducerEmpty = 1,
+  kSiteMmaTmemEmpty = 2,
+  kSiteMmaFull = 3,
+  kSiteEpiTmemFull = 4,
+  kSiteDrainLoads = 5,
+  kSiteDrainMma = 6,
+};
+
+__device__ __forceinline__ void record_timeout(uint32_t site) {
+  const unsigned long long code =
+      (0x7EULL << 32) | (static_cast<unsigned long long>(blockIdx.x & 0xFFFFFFu) << 8) | site;
+  atomicCAS(&g_status_word, 0ULL, code);
+}
+
+// Bounded wait on the phase of `bar` with the given parity.  Returns false
+// if the limit passed (error recorded, CTA abort flag raised) or, when
+// `honor_abort` is set, another role of this CTA aborted first.  Drains of
+// in-flight copies and MMAs pass honor_abort = false: they must wait for the
+// hardware even after an abort, still within the limit.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                             volatile int* abort_flag, uint32_t site,
+                                             bool honor_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (honor_abort && *abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      record_timeout(site);
+      return false;
+    }
+  }
+}
+
+struct TileCoord {
+  int p, m_blk, n_blk;
+};
+
+template <int MAXP>
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams<MAXP>& P, int t) {
+  int p = 0;
+#pragma unroll 1
+  while (p + 1 < P.num_problems && t >= P.prob[p + 1].tile_start) ++p;
+  const ProblemDesc& d = P.prob[p];
+  const int lt = t - d.tile_start;
+  // Grouped rasterisation: walk group_m tile rows down one tile column before
+  // moving right, so concurrently running CTAs share A and B panels in L2.
+  const int per_group = P.group_m * d.tiles_n;
+  const int group = lt / per_group;
+  const int first_m = group * P.group_m;
+  const int gsize = min(P.group_m, d.tiles_m - first_m);
+  const int in_group = lt - group * per_group;
+  TileCoord c;
+  c.p = p;
+  c.m_blk = first_m + in_group % gsize;
+  c.n_blk = in_group / gsize;
+  return c;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bits) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Writes 32 accumulator columns [col0, col0+32) of one output row.
+__device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int col0,
+                                            const uint32_t (&r)[32]) {
+  const int ncols = min(32, d.N - col0);
+  if (d.out_mode == kOutBF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + col0;
+    uint32_t pk[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
+    if (ncols == 32) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        reinterpret_cast<uint4*>(out)[v] =
+            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    } else {
+      unsigned short* o16 = reinterpret_cast<unsigned short*>(out);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) o16[j] = static_cast<unsigned short>((pk[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+    }
+  } else {
+    float* out = reinterpret_cast<float*>(d.C) + row * d.ldc + col0;
+    const bool acc = d.out_mode == kOutF32Accum;
+    if (ncols == 32) {
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        float4 x = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+        if (acc) {
+          const float4 o = reinterpret_cast<const float4*>(out)[v];
+          x.x += o.x;
+          x.y += o.y;
+          x.z += o.z;
+          x.w += o.w;
+        }
+        reinterpret_cast<float4*>(out)[v] = x;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) out[j] = __uint_as_float(r[j]) + (acc ? out[j] : 0.0f);
+    }
+  }
+}
+
+// Row of zeros for a problem with an empty reduction range.
+__device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, int n0, int BN) {
+  if (d.out_mode == kOutF32Accum) return;
+  const int n1 = min(d.N, n0 + BN);
+  if (d.out_mode == kOutBF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc;
+    for (int c = n0; c < n1; ++c) out[c] = __float2bfloat16_rn(0.0f);
+  } else {
+    float* out = reinterpret_cast<float*>(d.C) + row * d.ldc;
+    for (int c = n0; c < n1; ++c) out[c] = 0.0f;
+  }
+}
+
+template <int BN, int STAGES>
+struct SmemLayout {
+  static constexpr int kABytes = kBM * kBK * 2;
+  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  // 1024 B of slack for aligning the tile ring, the ring, barriers, TMEM slot
+  // and the abort flag.
+  static constexpr int kBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
+};
+
+template <int BN, int STAGES, int MAXP>
+__global__ void __launch_bounds__(kThreads, 1)
+    fc_gemm_tcgen05_kernel(const __grid_constant__ GemmParams<MAXP> P) {
+  using L = SmemLayout<BN, STAGES>;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  static_assert(BN == 128 || BN == 256, "UMMA N");
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t ring = (raw + 1023u) & ~1023u;
+  uint8_t* ring_ptr = smem_raw + (ring - raw);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * L::kStageBytes);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // barrier indices
+  auto full_bar = [&](int s) { return smem_addr(bars + s); };
+  auto empty_bar = [&](int s) { return smem_addr(bars + STAGES + s); };
+  auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * STAGES + b); };
+  auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * STAGES + 2 + b); };
+  const uint32_t mma_done_bar = smem_addr(bars + 2 * STAGES + 4);
+  auto a_tile = [&](int s) { return ring + s * L::kStageBytes; };
+  auto b_tile = [&](int s) { return ring + s * L::kStageBytes + L::kABytes; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    mbar_init(mma_done_bar, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    for (int p = 0; p < P.num_problems; ++p) {
+      prefetch_tmap(&P.tma[p]);
+      prefetch_tmap(&P.tmb[p]);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint64_t tmo = P.timeout_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && P.inject != 1) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t loads = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile(P, t);
+        const ProblemDesc& d = P.prob[tc.p];
+        const CUtensorMap* ma = &P.tma[tc.p];
+        const CUtensorMap* mb = &P.tmb[tc.p];
+        const int m0 = tc.m_blk * kBM;
+        const int n0 = tc.n_blk * BN;
+        for (int k = 0; k < d.num_k; ++k) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, L::kStageBytes);
+          const int r0 = k * kBK;
+          if (d.a_mn) {
+#pragma unroll
+            for (int h = 0; h < kBM / 64; ++h) tma_load_2d(a_tile(stage) + h * 8192, ma, fb, m0 + 64 * h, r0);
+          } else {
+            tma_load_2d(a_tile(stage), ma, fb, r0, m0);
+          }
+          if (d.b_mn) {
+#pragma unroll
+            for (int h = 0; h < BN / 64; ++h) tma_load_2d(b_tile(stage) + h * 8192, mb, fb, n0 + 64 * h, r0);
+          } else {
+            tma_load_2d(b_tile(stage), mb, fb, r0, n0);
+          }
+          ++loads;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Drain: the last load issued on each stage must have landed before
+      // the CTA may exit.
+      for (int s = 0; s < STAGES; ++s) {
+        if (loads > static_cast<uint32_t>(s)) {
+          const uint32_t n_s = (loads - s + STAGES - 1) / STAGES;
+          wait_bounded(full_bar(s), (n_s - 1) & 1u, tmo, abort_flag, kSiteDrainLoads, false);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
+        const TileCoord tc = decode_tile(P, t);
+        const ProblemDesc& d = P.prob[tc.p];
+        if (d.num_k == 0) continue;
+        const uint32_t b = acc & 1u;
+        const uint32_t acc_phase = (acc >> 1) & 1u;
+        if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + b * BN;
+        for (int k = 0; k < d.num_k; ++k) {
+          if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = a_tile(stage);
+          const uint32_t sb = b_tile(stage);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t ad = d.a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(sa + kk * 32, 16, 1024);
+            const uint64_t bd = d.b_mn ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
+                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(b));
+        ++acc;
+      }
+      // Drain every MMA issued by this thread before TMEM is released.
+      umma_commit(mma_done_bar);
+      wait_bounded(mma_done_bar, 0, tmo, abort_flag, kSiteDrainMma, false);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0;
+    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
+      const TileCoord tc = decode_tile(P, t);
+      const ProblemDesc& d = P.prob[tc.p];
+      const int row = tc.m_blk * kBM + q * 32 + lane;
+      const int n0 = tc.n_blk * BN;
+      if (d.num_k == 0) {
+        if (row < d.M) store_zero_row(d, row, n0, BN);
+        continue;
+      }
+      const uint32_t b = acc & 1u;
+      const uint32_t acc_phase = (acc >> 1) & 1u;
+      int ok = 1;
+      if (lane == 0) ok = wait_bounded(tfull_bar(b), acc_phase, tmo, abort_flag, kSiteEpiTmemFull);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= d.N) break;
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(t_row + c * 32, r);
+        tmem_ld_wait();
+        if (row < d.M) store_chunk(d, row, col0, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(b));
+      ++acc;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// -------------------------------------------------------------------------
+// Partial-sum reduction of the virtual grid: out = sum_{g=0..G-1} P[g] in
+// fp32, fixed order, then one bf16 RNE (or fp32 add into out).  Each thread
+// owns 8 consecutive columns of one row; grid-stride over all such groups.
+// -------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) vgrid_reduce_kernel(const float* __restrict__ part,
+                                                           int G, int64_t part_stride,
+                                                           int64_t ldp, int M, int N,
+                                                           void* out, int64_t ldo,
+                                                           int out_mode) {
+  const int groups_per_row = (N + 7) / 8;
+  const int64_t total = static_cast<int64_t>(M) * groups_per_row;
+  for (int64_t gidx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gidx < total;
+       gidx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(gidx / groups_per_row);
+    const int col0 = static_cast<int>(gidx % groups_per_row) * 8;
+    const int ncols = min(8, N - col0);
+    float s[8];
+    const float* src = part + row * ldp + col0;
+    if (ncols == 8) {
+      float4 a = reinterpret_cast<const float4*>(src)[0];
+      float4 b = reinterpret_cast<const float4*>(src)[1];
+      s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+      s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+      for (int g = 1; g < G; ++g) {
+        const float* pg = src + g * part_stride;
+        a = reinterpret_cast<const float4*>(pg)[0];
+        b = reinterpret_cast<const float4*>(pg)[1];
+        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s[j] = j < ncols ? src[j] : 0.0f;
+      for (int g = 1; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < ncols) s[j] += src[g * part_stride + j];
+    }
+    if (out_mode == kOutBF16) {
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row * ldo + col0;
+      if (ncols == 8) {
+        uint4 v;
+        v.x = pack_bf16x2(__float_as_uint(s[0]), __float_as_uint(s[1]));
+        v.y = pack_bf16x2(__float_as_uint(s[2]), __float_as_uint(s[3]));
+        v.z = pack_bf16x2(__float_as_uint(s[4]), __float_as_uint(s[5]));
+        v.w = pack_bf16x2(__float_as_uint(s[6]), __float_as_uint(s[7]));
+        *reinterpret_cast<uint4*>(o) = v;
+      } else {
+        for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(s[j]);
+      }
+    } else {
+      float* o = reinterpret_cast<float*>(out) + row * ldo + col0;
+      const bool acc = out_mode == kOutF32Accum;
+      for (int j = 0; j < ncols; ++j) o[j] = s[j] + (acc ? o[j] : 0.0f);
+    }
+  }
+}
+
+}  // namespace axonn

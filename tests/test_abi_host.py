@@ -1,0 +1,125 @@
+"""Host-side checks of the C ABI that need no GPU: the library builds and
+loads, exports every entry point the header declares, resolves 3D-grid
+blocks like the oracle's split rule, sizes workspaces, and rejects bad
+arguments before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "axonn_fc.h")
+
+
+@pytest.fixture(scope="module")
+def fc():
+    from pmm_fc_layer_gb300 import build
+    build.build()
+    import pmm_fc_layer_gb300 as m
+    m.load()
+    return m
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(axonn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(fc):
+    syms = declared_symbols()
+    assert len(syms) >= 10
+    lib = ctypes.CDLL(fc.library_path())
+    for s in syms:
+        assert hasattr(lib, s), f"{s} declared in the header but not exported"
+    assert set(syms) == set(fc.EXPORTS)
+
+
+def test_version(fc):
+    assert "sm_103a" in fc.axonn_version()
+
+
+@pytest.mark.parametrize("D", [0, 1, 7, 8, 300, 1000, 5000, 6144, 24576, 53248])
+@pytest.mark.parametrize("G", [1, 2, 3, 4, 8])
+def test_block_range_matches_oracle_rule(fc, D, G):
+    for b in range(G):
+        assert fc.axonn_block_range(D, G, b) == oracle.split_range(D, G, b)
+
+
+def test_block_range_errors(fc):
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_block_range(10, 0, 0)
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_block_range(10, 2, 2)
+
+
+def test_workspace_size(fc):
+    s = fc.Shape(8192, 6144, 24576, (2, 2, 2))
+    assert fc.axonn_fc_workspace_size("fwd", s, 0) == 0
+    assert fc.axonn_fc_workspace_size("fwd", s, fc.VGRID) == 2 * 8192 * 24576 * 4
+    assert fc.axonn_fc_workspace_size("dgrad", s, fc.VGRID) == 2 * 8192 * 6144 * 4
+    assert fc.axonn_fc_workspace_size("wgrad", s, fc.VGRID) == 2 * 6144 * 24576 * 4
+    s4 = fc.Shape(4096, 16384, 18432, (1, 4, 4))
+    assert fc.axonn_fc_workspace_size("fwd", s4, fc.VGRID) == 0      # G_x = 1
+    assert fc.axonn_fc_workspace_size("dgrad", s4, fc.VGRID) == 4 * 4096 * 16384 * 4
+    odd = fc.Shape(100, 60, 1001, (1, 1, 3))
+    assert fc.axonn_fc_workspace_size("wgrad", odd, fc.VGRID) == 3 * 60 * 1008 * 4
+
+
+def _status(fc, fn, *args):
+    return fn(*args)
+
+
+def _raw(fc, name, P, Q, C, ldp, ldq, ldc, shape, flags, ws=0, ws_bytes=0):
+    lib = fc.load()
+    return getattr(lib, name)(P, Q, C, ldp, ldq, ldc, ctypes.byref(shape), flags, ws, ws_bytes, 0)
+
+
+FAKE = 0x10000000  # never dereferenced: every case below fails validation
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(shape=(64, 64, 64), grid=(0, 1, 1)), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), coords=(2, 0, 0)), 1),
+    (dict(shape=(-1, 64, 64)), 1),
+    (dict(shape=(64, 64, 64), flags=0x400), 1),
+    (dict(shape=(64, 64, 64), flags=0x4 | 0x20), 1),
+    (dict(shape=(64, 64, 64), grid=(8, 4, 4), flags=0x8), 3),
+    (dict(shape=(64, 64, 64), P=FAKE + 8), 2),
+    (dict(shape=(64, 64, 64), ldp=68), 2),
+    (dict(shape=(64, 64, 64), ldp=32), 1),
+    (dict(shape=(64, 64, 64), C=FAKE + 4), 2),
+    (dict(shape=(64, 64, 64), P=0), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x8), 4),
+])
+def test_validation_errors(fc, case, expect):
+    T, K, N = case["shape"]
+    shape = fc.Shape(T, K, N, case.get("grid", (1, 1, 1)), case.get("coords", (0, 0, 0)))
+    st = _raw(fc, "axonn_fc_fwd", case.get("P", FAKE), case.get("Q", FAKE), case.get("C", FAKE),
+              case.get("ldp", 64), case.get("ldq", 64), case.get("ldc", 64), shape,
+              case.get("flags", 0))
+    assert st == expect, fc.axonn_last_error()
+    assert fc.axonn_last_error()
+
+
+def test_no_device_is_an_error_not_a_fallback(fc):
+    """Valid arguments on a machine without a GPU must fail loudly."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, fc.Shape(64, 64, 64), 0)
+    assert st in (fc.ERR_CUDA, fc.ERR_UNSUPPORTED)
+
+
+def test_binding_refuses_missing_library(tmp_path):
+    import pmm_fc_layer_gb300 as m
+    saved = m._lib
+    m._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            m.load(str(tmp_path / "absent.so"))
+    finally:
+        m._lib = saved
