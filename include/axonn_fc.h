@@ -125,6 +125,30 @@ axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t l
                               int64_t lddy, int64_t lddw, const axonn_fc_shape_t* shape,
                               uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/*
+ * Virtual-grid product (as the entry points above with AXONN_VGRID) that
+ * allocates nothing and needs no workspace argument.  The pages have no
+ * counterpart: this exists for callers that cannot call cudaMalloc, such as
+ * code that runs inside a host framework that owns all device memory, or
+ * code that must not allocate once it is running.
+ *   op        axonn_op_t; P, Q, C and ld* as for that op's entry point
+ *   flags     as for the entry points; AXONN_VGRID is implied
+ * The fp32 partials live in a fixed 64 MiB scratch array inside the
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A product whose partials need more (G * M * ceil8(N) * 4 bytes,
+ * G the reduced grid extent) returns AXONN_ERR_WORKSPACE with a message;
+ * products whose reduced axis has one block need no scratch.  The first call
+ * on each device looks up the scratch's device address (once, with that
+ * device current); make that first call before any stream capture.  Every
+ * call uses the same scratch and the kernels overwrite every partial they
+ * later read, so no clearing is needed -- but calls that overlap on the GPU
+ * (on different streams, or from different threads) race on it and must be
+ * serialised by the caller.
+ */
+axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void* C, int64_t ldp,
+                                     int64_t ldq, int64_t ldc, const axonn_fc_shape_t* shape,
+                                     uint32_t flags, cudaStream_t stream);
+
 /* Workspace bytes an op needs with these flags (0 when none).  `op` is an
  * axonn_op_t.  Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,

@@ -26,7 +26,8 @@ OUT_F32 = 0x20
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]
 
-EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_workspace_size",
+EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_static",
+           "axonn_fc_workspace_size",
            "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_last_error", "axonn_version")
 
@@ -73,6 +74,9 @@ def load(path: str | None = None):
             f = getattr(lib, name)
             f.argtypes = sig
             f.restype = ctypes.c_int
+        lib.axonn_fc_vgrid_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64,
+                                              ctypes.POINTER(Shape), u32, vp]
+        lib.axonn_fc_vgrid_static.restype = ctypes.c_int
         lib.axonn_fc_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(Shape), u32,
                                                 ctypes.POINTER(sz)]
         lib.axonn_fc_workspace_size.restype = ctypes.c_int
@@ -150,6 +154,17 @@ def axonn_fc_wgrad(X, dY, dW, shape: Shape, flags: int = 0, ws=None, ldx=None, l
                    lddw=None, stream=None):
     """dW = X^T . dY (layer, block or virtual grid)."""
     _call("axonn_fc_wgrad", X, dY, dW, shape, flags, ws, ldx, lddy, lddw, stream)
+
+
+def axonn_fc_vgrid_static(op, P, Q, C, shape: Shape, flags: int = 0, ldp=None, ldq=None,
+                          ldc=None, stream=None):
+    """Virtual-grid product with the library's fixed scratch: nothing is
+    allocated and no workspace is passed (for callers that cannot allocate
+    device memory).  ``op`` is 'fwd', 'dgrad' or 'wgrad'."""
+    op = OPS.get(op, op)
+    st = load().axonn_fc_vgrid_static(int(op), _ptr(P), _ptr(Q), _ptr(C), _ld(P, ldp), _ld(Q, ldq),
+                                      _ld(C, ldc), ctypes.byref(shape), flags, _stream(stream))
+    _check(st)
 
 
 def axonn_fc_workspace_size(op, shape: Shape, flags: int = 0) -> int:

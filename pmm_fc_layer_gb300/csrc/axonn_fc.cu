@@ -457,9 +457,66 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   return ok();
 }
 
+// ----------------------------------------------------------------------
+// Fixed scratch for callers that cannot allocate device memory.
+//
+// The virtual-grid path needs an fp32 buffer for the partial products of
+// the reduced grid axis.  Normally the caller passes it as a workspace.  A
+// caller that may not call cudaMalloc -- code running where device memory is
+// handed out by someone else, or under a policy that forbids allocation
+// after start-up -- can use axonn_fc_vgrid_static instead, which takes its
+// scratch from this array.  The array is part of the library image: every
+// GPU that loads the library holds these bytes until the process exits.
+// ----------------------------------------------------------------------
+constexpr size_t kStaticScratchBytes = size_t{64} << 20;  // 64 MiB
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mu;
+std::vector<void*> g_static_addr;  // per device; set on the first call there
+
+// Device address of g_static_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so the address is asked
+// for once per device (with that device current) and cached.
+axonn_status_t static_scratch_addr(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  if (static_cast<int>(g_static_addr.size()) <= dev) g_static_addr.resize(dev + 1, nullptr);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(AXONN_ERR_CUDA, "cudaGetSymbolAddress(static scratch): %s", cudaGetErrorString(e));
+    g_static_addr[dev] = p;
+  }
+  *out = g_static_addr[dev];
+  return AXONN_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void* C, int64_t ldp,
+                                     int64_t ldq, int64_t ldc, const axonn_fc_shape_t* shape,
+                                     uint32_t flags, cudaStream_t stream) {
+  const uint32_t f = flags | AXONN_VGRID;
+  axonn_status_t st = check_shape(op, shape, f);
+  if (st != AXONN_OK) return st;
+  const size_t need = vgrid_ws_bytes(op, *shape, f);
+  if (need > kStaticScratchBytes)
+    return fail(AXONN_ERR_WORKSPACE,
+                "this product needs %zu bytes of partial-sum scratch; the built-in scratch holds %zu "
+                "(use the entry point with a caller workspace)",
+                need, kStaticScratchBytes);
+  void* ws = nullptr;
+  if (need > 0) {
+    st = static_scratch_addr(&ws);
+    if (st != AXONN_OK) return st;
+  }
+  return fc_op(op, P, Q, C, ldp, ldq, ldc, shape, f, ws, need > 0 ? kStaticScratchBytes : 0, stream);
+}
 
 axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw, int64_t ldy,
                             const axonn_fc_shape_t* shape, uint32_t flags, void* ws, size_t ws_bytes,
