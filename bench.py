@@ -222,6 +222,8 @@ def run_ours(args):
     from pmm_fc_layer_gb300 import build as _b
     _b.build()
     fc.load()
+    fc.axonn_set_kernel_config(args.config)
+    sms, max_pairs = fc.axonn_device_info()
 
     only = tuple(args.only.split(":")) if args.only else None
     layers = [l for l in LAYERS if only is None or l[0] == only[0]]
@@ -250,7 +252,9 @@ def run_ours(args):
             fc.call(op, P, Q, C, shape, 0, None, stream=stream)
             if events is not None:
                 events[gi][1].record(stream)
+                used[gi] = fc.axonn_last_kernel_config()
 
+    used = [None] * len(plan)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -289,7 +293,8 @@ def run_ours(args):
         gemm_ms_total += sum(ms)
         med = statistics.median(ms)
         per.append({"layer": name, "op": op, "M": m, "N": n, "R": r, "layout": {"fwd": "NN", "dgrad": "NT", "wgrad": "TN"}[op],
-                    "ms": round(med, 4), "tflops": round(fl / med / 1e9, 1)})
+                    "ms": round(med, 4), "tflops": round(fl / med / 1e9, 1),
+                    "config": fc.axonn_kernel_config_name(used[gi])})
     peaks = read_peaks()
     for p in per:
         p["frac_of_sustained"] = round(p["tflops"] / peaks["sustained"], 4)
@@ -362,6 +367,8 @@ def run_ours(args):
                      "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps}
                     if e2e_steps else None),
             "gpu_launches": launches,
+            "device": {"sms": sms, "resident_cta_pairs": max_pairs,
+                       "kernel_configs": sorted({p["config"] for p in per})},
             "clocks": clocks.summary(),
         }
         if only is not None:
@@ -384,6 +391,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--config", type=int, default=-1,
+                    help="force one kernel configuration (-1: the library's choice)")
     ap.add_argument("--only", default=None, metavar="LAYER:OP",
                     help="time one GEMM (e.g. out:fwd) for profiling; not a bench line")
     args = ap.parse_args()

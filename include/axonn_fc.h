@@ -173,6 +173,25 @@ void axonn_set_wait_timeout_ns(uint64_t ns);
  * 0 restores normal operation.  Never needed in production. */
 void axonn_debug_set_inject(int mode);
 
+/* Kernel configurations.  The library chooses one per call from the
+ * problem's tile counts (the pages' "automated BLAS kernel tuning": review of
+ * arXiv 2502.08145, "The reading"); these calls expose the choice.
+ *   0  1cta_128x128      one CTA per 128x128 output tile, 64-deep stages
+ *   1  1cta_128x256      one CTA per 128x256 output tile, 64-deep stages
+ *   2  pair_256x256      a CTA pair (cluster of 2, cta_group::2 MMA) per
+ *                        256x256 output tile, 64-deep stages
+ * axonn_set_kernel_config(c) forces configuration c for all later calls in
+ * the process (-1 restores automatic choice); AXONN_ERR_INVALID_ARG if c is
+ * out of range.  axonn_last_kernel_config() is the configuration the last
+ * GEMM launch on this thread used (-1 before any). */
+axonn_status_t axonn_set_kernel_config(int config);
+/* SM count of the current device and how many CTA pairs (clusters of 2
+ * running configuration 2) it keeps resident at once. */
+axonn_status_t axonn_device_info(int* sms, int* max_pairs);
+int axonn_num_kernel_configs(void);
+const char* axonn_kernel_config_name(int config);
+int axonn_last_kernel_config(void);
+
 /* Thread-local description of the last error returned on this thread. */
 const char* axonn_last_error(void);
 

@@ -29,7 +29,9 @@ STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "C
 EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_static",
            "axonn_fc_workspace_size",
            "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
-           "axonn_debug_set_inject", "axonn_last_error", "axonn_version")
+           "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs", "axonn_device_info",
+           "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
+           "axonn_version")
 
 
 class AxonnError(RuntimeError):
@@ -88,6 +90,14 @@ def load(path: str | None = None):
         lib.axonn_set_wait_timeout_ns.restype = None
         lib.axonn_debug_set_inject.argtypes = [ctypes.c_int]
         lib.axonn_debug_set_inject.restype = None
+        lib.axonn_set_kernel_config.argtypes = [ctypes.c_int]
+        lib.axonn_set_kernel_config.restype = ctypes.c_int
+        lib.axonn_num_kernel_configs.restype = ctypes.c_int
+        lib.axonn_device_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
+        lib.axonn_device_info.restype = ctypes.c_int
+        lib.axonn_kernel_config_name.argtypes = [ctypes.c_int]
+        lib.axonn_kernel_config_name.restype = ctypes.c_char_p
+        lib.axonn_last_kernel_config.restype = ctypes.c_int
         lib.axonn_last_error.restype = ctypes.c_char_p
         lib.axonn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -195,6 +205,30 @@ def axonn_set_wait_timeout_ns(ns: int):
 
 def axonn_debug_set_inject(mode: int):
     load().axonn_debug_set_inject(int(mode))
+
+
+def axonn_set_kernel_config(config: int):
+    """Force kernel configuration `config` (-1: automatic choice)."""
+    _check(load().axonn_set_kernel_config(int(config)))
+
+
+def axonn_device_info():
+    """(SM count, resident CTA pairs) of the current device."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().axonn_device_info(ctypes.byref(a), ctypes.byref(b)))
+    return a.value, b.value
+
+
+def axonn_num_kernel_configs() -> int:
+    return int(load().axonn_num_kernel_configs())
+
+
+def axonn_kernel_config_name(config: int) -> str:
+    return load().axonn_kernel_config_name(int(config)).decode()
+
+
+def axonn_last_kernel_config() -> int:
+    return int(load().axonn_last_kernel_config())
 
 
 def axonn_last_error() -> str:

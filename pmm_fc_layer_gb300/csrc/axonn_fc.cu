@@ -15,6 +15,7 @@
 
 #include "axonn_fc.h"
 #include "gemm_kernel.cuh"
+#include "gemm_pair_kernel.cuh"
 
 namespace {
 
@@ -60,21 +61,42 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // Per-device facts and one-time kernel attributes.
 struct DeviceState {
   int sms = 0;
+  int max_pairs = 0;  // CTA pairs (clusters of 2) resident at once
   bool attrs_set = false;
 };
+
+constexpr int kPairStages = 6;
 std::mutex g_dev_mu;
 std::vector<DeviceState> g_devs;
 
-template <int BN, int STAGES, int MAXP>
-void* kernel_ptr() {
-  return reinterpret_cast<void*>(&axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>);
+template <int BN, int BK, int STAGES, int MAXP>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              axonn::SmemLayout<BN, BK, STAGES>::kBytes);
 }
 
-template <int BN, int STAGES, int MAXP>
-cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>,
+template <int STAGES, int MAXP>
+cudaError_t set_pair_smem_attr() {
+  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_pair_kernel<STAGES, MAXP>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              axonn::SmemLayout<BN, STAGES>::kBytes);
+                              axonn::PairSmemLayout<STAGES>::kBytes);
+}
+
+// Clusters of 2 that can be resident at once (SM pairs inside a GPC).
+int max_active_pairs(int sms) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * sms, 1, 1);
+  cfg.blockDim = dim3(axonn::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = axonn::PairSmemLayout<kPairStages>::kBytes;
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(
+      &n, reinterpret_cast<const void*>(&axonn::fc_gemm_tcgen05_pair_kernel<kPairStages, 1>), &cfg);
+  if (e != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = sms / 2;
+  }
+  return n;
 }
 
 axonn_status_t device_state(DeviceState** out) {
@@ -93,11 +115,14 @@ axonn_status_t device_state(DeviceState** out) {
                   dev, major, minor);
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
-    cudaError_t es[] = {set_smem_attr<256, 4, 1>(), set_smem_attr<256, 4, kMaxProblems>(),
-                        set_smem_attr<128, 6, 1>(), set_smem_attr<128, 6, kMaxProblems>()};
+    cudaError_t es[] = {set_smem_attr<128, 64, 6, 1>(), set_smem_attr<128, 64, 6, kMaxProblems>(),
+                        set_smem_attr<256, 64, 4, 1>(), set_smem_attr<256, 64, 4, kMaxProblems>(),
+                        set_pair_smem_attr<kPairStages, 1>(),
+                        set_pair_smem_attr<kPairStages, kMaxProblems>()};
     for (cudaError_t x : es)
       if (x != cudaSuccess)
         return fail(AXONN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(x));
+    d.max_pairs = max_active_pairs(d.sms);
     d.attrs_set = true;
   }
   *out = &d;
@@ -215,6 +240,9 @@ axonn_status_t check_operand(const char* name, const void* p, int64_t ld, int64_
 
 axonn_status_t encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                          int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  // A box row of 128 B takes the 128-byte swizzle, one of 64 B the 64-byte.
+  const CUtensorMapSwizzle swz =
+      box_inner * 2 >= 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   auto fn = encode_fn();
   if (!fn) return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
   cuuint64_t dims[2] = {inner, outer};
@@ -222,7 +250,7 @@ axonn_status_t encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint6
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return AXONN_OK;
@@ -245,17 +273,40 @@ struct Block {
   int out_mode;
 };
 
+// Kernel configurations the library can run.  A configuration fixes the
+// output tile, whether a CTA pair shares each MMA, and the ring depth.
+struct KernelConfig {
+  const char* name;
+  int bm, bn;   // output tile of one CTA (or CTA pair)
+  int bk;       // reduction depth of one pipeline stage
+  bool pair;    // cta_group::2 across a cluster of 2
+};
+constexpr KernelConfig kConfigs[] = {
+    {"1cta_128x128", 128, 128, 64, false},
+    {"1cta_128x256", 128, 256, 64, false},
+    {"pair_256x256", 256, 256, 64, true},
+};
+// Throughput of each configuration relative to 1cta_128x256 on full waves
+// (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
+constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92};
+constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
+std::atomic<int> g_forced_config{-1};
+thread_local int t_last_config = -1;
+
 struct LaunchPlan {
-  int BN = 256;
+  int config = 1;
+  int group_m = 16;
   std::vector<Block> blocks;
 };
 
-template <int BN, int STAGES, int MAXP>
-axonn_status_t launch_gemm(const OpView& v, const std::vector<Block>& blocks, int sms,
-                           cudaStream_t stream) {
+template <int MAXP>
+axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vector<Block>& blocks,
+                           const KernelConfig& c, int group_m) {
   static_assert(sizeof(GemmParams<MAXP>) < 32000, "kernel parameter space");
-  GemmParams<MAXP> P;
   memset(&P, 0, sizeof(P));
+  // Rows of A and columns of B that one CTA loads per stage.
+  const uint32_t a_rows = 128;
+  const uint32_t b_cols = c.pair ? c.bn / 2 : c.bn;
   int tiles = 0, np = 0;
   for (const Block& b : blocks) {
     if (b.M == 0 || b.N == 0) continue;
@@ -266,57 +317,105 @@ axonn_status_t launch_gemm(const OpView& v, const std::vector<Block>& blocks, in
     d.M = static_cast<int32_t>(b.M);
     d.N = static_cast<int32_t>(b.N);
     d.R = static_cast<int32_t>(b.R);
-    d.tiles_m = static_cast<int32_t>((b.M + axonn::kBM - 1) / axonn::kBM);
-    d.tiles_n = static_cast<int32_t>((b.N + BN - 1) / BN);
+    d.tiles_m = static_cast<int32_t>((b.M + c.bm - 1) / c.bm);
+    d.tiles_n = static_cast<int32_t>((b.N + c.bn - 1) / c.bn);
     d.tile_start = tiles;
-    d.num_k = static_cast<int32_t>((b.R + axonn::kBK - 1) / axonn::kBK);
+    d.num_k = static_cast<int32_t>((b.R + c.bk - 1) / c.bk);
     d.a_mn = v.a_mn;
     d.b_mn = v.b_mn;
-    d.idesc = make_idesc(axonn::kBM, BN, v.a_mn, v.b_mn);
+    d.idesc = make_idesc(c.bm, c.bn, v.a_mn, v.b_mn);
     d.out_mode = b.out_mode;
     if (b.R > 0) {
       axonn_status_t s;
-      if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, 64);
-      else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, 64, axonn::kBM);
+      const uint32_t bk = static_cast<uint32_t>(c.bk);
+      if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, bk);
+      else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, bk, a_rows);
       if (s != AXONN_OK) return s;
-      if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, 64);
-      else s = encode_2d(&P.tmb[np], b.B, b.R, b.N, v.ldb, 64, BN);
+      if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, bk);
+      else s = encode_2d(&P.tmb[np], b.B, b.R, b.N, v.ldb, bk, b_cols);
       if (s != AXONN_OK) return s;
     }
     tiles += d.tiles_m * d.tiles_n;
     ++np;
   }
-  if (np == 0) return AXONN_OK;
   P.num_problems = np;
   P.total_tiles = tiles;
-  P.group_m = 16;
+  P.group_m = group_m;
   P.inject = g_inject.load();
   P.timeout_ns = g_timeout_ns.load();
-  const int grid = tiles < sms ? tiles : sms;
-  axonn::fc_gemm_tcgen05_kernel<BN, STAGES, MAXP>
-      <<<grid, axonn::kThreads, axonn::SmemLayout<BN, STAGES>::kBytes, stream>>>(P);
+  return AXONN_OK;
+}
+
+template <int BN, int BK, int STAGES, int MAXP>
+axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
+                             cudaStream_t stream) {
+  GemmParams<MAXP> P;
+  axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
+  if (st != AXONN_OK || P.num_problems == 0) return st;
+  const int grid = P.total_tiles < dev.sms ? P.total_tiles : dev.sms;
+  axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP>
+      <<<grid, axonn::kThreads, axonn::SmemLayout<BN, BK, STAGES>::kBytes, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return AXONN_OK;
 }
 
-axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, int sms, cudaStream_t stream) {
-  const bool many = plan.blocks.size() > 1;
-  if (plan.BN == 256)
-    return many ? launch_gemm<256, 4, kMaxProblems>(v, plan.blocks, sms, stream)
-                : launch_gemm<256, 4, 1>(v, plan.blocks, sms, stream);
-  return many ? launch_gemm<128, 6, kMaxProblems>(v, plan.blocks, sms, stream)
-              : launch_gemm<128, 6, 1>(v, plan.blocks, sms, stream);
+template <int STAGES, int MAXP>
+axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
+                           cudaStream_t stream) {
+  GemmParams<MAXP> P;
+  axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
+  if (st != AXONN_OK || P.num_problems == 0) return st;
+  const int pairs = P.total_tiles < dev.max_pairs ? P.total_tiles : dev.max_pairs;
+  axonn::fc_gemm_tcgen05_pair_kernel<STAGES, MAXP>
+      <<<2 * pairs, axonn::kThreads, axonn::PairSmemLayout<STAGES>::kBytes, stream>>>(P);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM pair launch: %s", cudaGetErrorString(e));
+  return AXONN_OK;
 }
 
-int choose_bn(const std::vector<Block>& blocks, int sms) {
-  int64_t tiles256 = 0, maxN = 0;
-  for (const Block& b : blocks) {
-    tiles256 += ((b.M + 127) / 128) * ((b.N + 255) / 256);
-    if (b.N > maxN) maxN = b.N;
+axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
+                          cudaStream_t stream) {
+  const bool many = plan.blocks.size() > 1;
+  t_last_config = plan.config;
+  switch (plan.config) {
+    case 0:
+      return many ? launch_single<128, 64, 6, kMaxProblems>(v, plan, dev, stream)
+                  : launch_single<128, 64, 6, 1>(v, plan, dev, stream);
+    case 1:
+      return many ? launch_single<256, 64, 4, kMaxProblems>(v, plan, dev, stream)
+                  : launch_single<256, 64, 4, 1>(v, plan, dev, stream);
+    default:
+      return many ? launch_pair<kPairStages, kMaxProblems>(v, plan, dev, stream)
+                  : launch_pair<kPairStages, 1>(v, plan, dev, stream);
   }
-  if (maxN <= 128 || tiles256 < sms / 2) return 128;
-  return 256;
+}
+
+// Work units (tile slots) a configuration needs, counted in waves of the
+// units the GPU runs at once; the rounding up is the wave-quantisation loss.
+double config_cost(const std::vector<Block>& blocks, const KernelConfig& c, const DeviceState& dev) {
+  int64_t tiles = 0;
+  for (const Block& b : blocks)
+    if (b.M > 0 && b.N > 0) tiles += ((b.M + c.bm - 1) / c.bm) * ((b.N + c.bn - 1) / c.bn);
+  const int64_t slots = c.pair ? dev.max_pairs : dev.sms;
+  const int64_t waves = (tiles + slots - 1) / slots;
+  // One wave costs the tile's area over the configuration's speed.
+  return static_cast<double>(waves) * c.bm * c.bn / kConfigSpeed[&c - kConfigs];
+}
+
+int choose_config(const std::vector<Block>& blocks, const DeviceState& dev) {
+  const int forced = g_forced_config.load();
+  if (forced >= 0 && forced < kNumConfigs) return forced;
+  int best = 1;
+  double best_cost = 0;
+  for (int i = 0; i < kNumConfigs; ++i) {
+    const double c = config_cost(blocks, kConfigs[i], dev);
+    if (i == 0 || c < best_cost) {
+      best = i;
+      best_cost = c;
+    }
+  }
+  return best;
 }
 
 // Shared body of the three entry points.  P and Q are the op's first and
@@ -439,8 +538,8 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     b.out_mode = user_mode;
     plan.blocks.push_back(b);
   }
-  plan.BN = choose_bn(plan.blocks, dev->sms);
-  st = run_blocks(v, plan, dev->sms, stream);
+  plan.config = choose_config(plan.blocks, *dev);
+  st = run_blocks(v, plan, *dev, stream);
   if (st != AXONN_OK) return st;
 
   if (partials) {
@@ -572,6 +671,30 @@ axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail) {
 void axonn_set_wait_timeout_ns(uint64_t ns) { g_timeout_ns.store(ns ? ns : 1); }
 
 void axonn_debug_set_inject(int mode) { g_inject.store(mode); }
+
+axonn_status_t axonn_set_kernel_config(int config) {
+  if (config < -1 || config >= kNumConfigs)
+    return fail(AXONN_ERR_INVALID_ARG, "kernel configuration %d not in [-1, %d)", config, kNumConfigs);
+  g_forced_config.store(config);
+  return ok();
+}
+
+int axonn_num_kernel_configs(void) { return kNumConfigs; }
+
+axonn_status_t axonn_device_info(int* sms, int* max_pairs) {
+  DeviceState* d = nullptr;
+  axonn_status_t st = device_state(&d);
+  if (st != AXONN_OK) return st;
+  if (sms) *sms = d->sms;
+  if (max_pairs) *max_pairs = d->max_pairs;
+  return ok();
+}
+
+const char* axonn_kernel_config_name(int config) {
+  return (config >= 0 && config < kNumConfigs) ? kConfigs[config].name : "";
+}
+
+int axonn_last_kernel_config(void) { return t_last_config; }
 
 const char* axonn_last_error(void) { return t_last_error.c_str(); }
 

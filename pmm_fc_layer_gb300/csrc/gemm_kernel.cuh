@@ -29,7 +29,7 @@
 namespace axonn {
 
 constexpr int kBM = 128;       // rows per tile (UMMA M, one CTA)
-constexpr int kBK = 64;        // reduction depth per stage: 64 bf16 = 128 B
+constexpr int kBK = 64;        // reduction depth per stage of the CTA-pair kernel
 constexpr int kThreads = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
 
@@ -190,10 +190,10 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int BK, int STAGES>
 struct SmemLayout {
-  static constexpr int kABytes = kBM * kBK * 2;
-  static constexpr int kBBytes = BN * kBK * 2;
+  static constexpr int kABytes = kBM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   // 1024 B of slack for aligning the tile ring, the ring, barriers, TMEM slot
@@ -201,10 +201,22 @@ struct SmemLayout {
   static constexpr int kBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
 };
 
-template <int BN, int STAGES, int MAXP>
+// Shared-memory descriptor of the K=16 slice kk of a stage's operand tile.
+// K-major tiles hold rows of BK elements (128 B with 128-byte swizzle for
+// BK = 64, 64 B with 64-byte swizzle for BK = 32); MN-major tiles hold
+// 64-element MN chunks of BK rows of 128 B, BK * 128 bytes apart.
+template <int BK>
+__device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk, bool mn_major) {
+  if (mn_major) return sdesc_sw128(tile + kk * 2048, BK * 128, 1024);
+  if (BK == 64) return sdesc_sw128(tile + kk * 32, 16, 1024);
+  return sdesc_sw64(tile + kk * 32, 16, 512);
+}
+
+template <int BN, int BK, int STAGES, int MAXP>
 __global__ void __launch_bounds__(kThreads, 1)
     fc_gemm_tcgen05_kernel(const __grid_constant__ GemmParams<MAXP> P) {
-  using L = SmemLayout<BN, STAGES>;
+  using L = SmemLayout<BN, BK, STAGES>;
+  static_assert(BK == 64 || BK == 32, "stage depth");
   constexpr uint32_t kTmemCols = 2 * BN;
   static_assert(BN == 128 || BN == 256, "UMMA N");
 
@@ -278,16 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, L::kStageBytes);
-          const int r0 = k * kBK;
+          const int r0 = k * BK;
           if (d.a_mn) {
 #pragma unroll
-            for (int h = 0; h < kBM / 64; ++h) tma_load_2d(a_tile(stage) + h * 8192, ma, fb, m0 + 64 * h, r0);
+            for (int h = 0; h < kBM / 64; ++h)
+              tma_load_2d(a_tile(stage) + h * (BK * 128), ma, fb, m0 + 64 * h, r0);
           } else {
             tma_load_2d(a_tile(stage), ma, fb, r0, m0);
           }
           if (d.b_mn) {
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) tma_load_2d(b_tile(stage) + h * 8192, mb, fb, n0 + 64 * h, r0);
+            for (int h = 0; h < BN / 64; ++h)
+              tma_load_2d(b_tile(stage) + h * (BK * 128), mb, fb, n0 + 64 * h, r0);
           } else {
             tma_load_2d(b_tile(stage), mb, fb, r0, n0);
           }
@@ -332,11 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sa = a_tile(stage);
           const uint32_t sb = b_tile(stage);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = d.a_mn ? sdesc_sw128(sa + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(sa + kk * 32, 16, 1024);
-            const uint64_t bd = d.b_mn ? sdesc_sw128(sb + kk * 2048, 8192, 1024)
-                                       : sdesc_sw128(sb + kk * 32, 16, 1024);
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = operand_desc<BK>(sa, kk, d.a_mn);
+            const uint64_t bd = operand_desc<BK>(sb, kk, d.b_mn);
             umma_bf16(d_tmem, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
           }
           umma_commit(empty_bar(stage));

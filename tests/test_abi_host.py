@@ -42,6 +42,17 @@ def test_version(fc):
     assert "sm_103a" in fc.axonn_version()
 
 
+def test_kernel_config_table(fc):
+    n = fc.axonn_num_kernel_configs()
+    assert n == 3
+    assert [fc.axonn_kernel_config_name(i) for i in range(n)] == \
+        ["1cta_128x128", "1cta_128x256", "pair_256x256"]
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_set_kernel_config(n)
+    fc.axonn_set_kernel_config(2)
+    fc.axonn_set_kernel_config(-1)
+
+
 @pytest.mark.parametrize("D", [0, 1, 7, 8, 300, 1000, 5000, 6144, 24576, 53248])
 @pytest.mark.parametrize("G", [1, 2, 3, 4, 8])
 def test_block_range_matches_oracle_rule(fc, D, G):

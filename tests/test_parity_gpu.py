@@ -15,16 +15,29 @@ from fc_cases import (assert_within_bound, host_bits, host_f64, make_operand, op
 pytestmark = pytest.mark.gpu
 
 LAYOUTS = [(False, False), (False, True), (True, False), (True, True)]
+CONFIGS = [0, 1, 2]   # every kernel configuration of the library
 
 
+@pytest.fixture
+def forced(cuda_lib, request):
+    """Force one kernel configuration for the test, restore automatic after."""
+    cfg = request.param
+    cuda_lib.axonn_set_kernel_config(cfg)
+    yield cfg
+    cuda_lib.axonn_set_kernel_config(-1)
+
+
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("p_t,q_t", LAYOUTS)
-@pytest.mark.parametrize("T,K,N", [(128, 64, 256), (300, 200, 520), (129, 1000, 257)])
-def test_integer_exact_layouts_and_tails(cuda_lib, op, p_t, q_t, T, K, N):
+@pytest.mark.parametrize("T,K,N", [(128, 64, 256), (300, 200, 520), (129, 1000, 257),
+                                   (520, 136, 776)])
+def test_integer_exact_layouts_and_tails(cuda_lib, forced, op, p_t, q_t, T, K, N):
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, p_t, seed=21, kind="int")
     Q = make_operand(qn, T, K, N, q_t, seed=21, kind="int")
     out = run_gpu(cuda_lib, op, P, Q, p_t, q_t, T, K, N)
+    assert cuda_lib.axonn_last_kernel_config() == forced
     C, _ = oracle.fc(op, P, Q, p_t, q_t)
     want = oracle.bf16_rne(C)
     got = host_bits(out)
@@ -32,8 +45,9 @@ def test_integer_exact_layouts_and_tails(cuda_lib, op, p_t, q_t, T, K, N):
     assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
 
 
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
-def test_config1_single_layer_random(cuda_lib, op):
+def test_config1_single_layer_random(cuda_lib, forced, op):
     """X[256x512] ~N(0,1), W[512x2048] ~N(0,0.02), dY[256x2048] ~N(0,1)."""
     T, K, N = 256, 512, 2048
     pn, qn = operand_names(op)
@@ -44,9 +58,10 @@ def test_config1_single_layer_random(cuda_lib, op):
     assert_within_bound(host_f64(out), C, S, f"config1 {op}")
 
 
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("grid", [(2, 2, 2), (1, 4, 4), (3, 1, 2), (2, 3, 1)])
-def test_vgrid_integer_exact(cuda_lib, op, grid):
+def test_vgrid_integer_exact(cuda_lib, forced, op, grid):
     T, K, N = 300, 200, 520
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, False, seed=31, kind="int")
@@ -69,9 +84,10 @@ def test_vgrid_random_config3_shape_scaled(cuda_lib, op):
     assert_within_bound(host_f64(out), C, S, f"vgrid {op}")
 
 
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("coords", [(0, 0, 0), (1, 0, 1), (1, 1, 1)])
-def test_block_full_operands(cuda_lib, op, coords):
+def test_block_full_operands(cuda_lib, forced, op, coords):
     """One block product addressed inside the full matrices; fp32 partial."""
     T, K, N = 300, 200, 520
     grid = (2, 2, 2)
@@ -133,8 +149,9 @@ def test_vgrid_accumulate_f32(cuda_lib):
     assert np.array_equal(host_f64(out), C + 3.0)
 
 
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("T,K,N", [(1, 1, 1), (7, 9, 5), (1, 300, 1), (513, 8, 3)])
-def test_degenerate_small_shapes(cuda_lib, T, K, N):
+def test_degenerate_small_shapes(cuda_lib, forced, T, K, N):
     for op in ("fwd", "dgrad", "wgrad"):
         pn, qn = operand_names(op)
         P = make_operand(pn, T, K, N, False, seed=61, kind="int", pad=True)
@@ -165,7 +182,8 @@ def test_empty_output_is_noop(cuda_lib):
     assert torch.all(out == 5.0)
 
 
-def test_bounded_wait_timeout_reports_and_recovers(cuda_lib):
+@pytest.mark.parametrize("forced", CONFIGS, indirect=True)
+def test_bounded_wait_timeout_reports_and_recovers(cuda_lib, forced):
     """A producer that withholds its loads makes every bounded wait expire;
     the library reports AXONN_ERR_TIMEOUT and the context stays usable."""
     T, K, N = 128, 64, 256
