@@ -1,24 +1,29 @@
 #!/usr/bin/env python
-"""Benchmark of the FC-layer GEMMs of one GPT block on GB300.
+"""Benchmark of the FC-layer GEMMs of a GPT block on GB300.
 
-A step is one pass of the whole path over one batch: for each of the four
-FC layers of a GPT block with hidden size H = 6144 and T = 8192 tokens
-(batch 4 x sequence 2048) -- QKV [H -> 3H], attention-out [H -> H],
-MLP-up [H -> 4H], MLP-down [4H -> H] -- the forward product Y = X.W, the
-data gradient dX = dY.W^T and the weight gradient dW = X^T.dY, all through
-the C ABI of libaxonn_fc.so (12 tcgen05 GEMM launches).
+A step is one pass of the whole path over one batch.  For each FC layer of
+the workload it computes the forward product Y = X.W, the data gradient
+dX = dY.W^T and the weight gradient dW = X^T.dY, all through the C ABI of
+libaxonn_fc.so.  The default workload, on which the metric is quoted, is a GPT
+block with hidden size H = 6144 and T = 8192 tokens (batch 4 x sequence 2048).
+Its four layers are QKV [H -> 3H], attention-out [H -> H], MLP-up [H -> 4H]
+and MLP-down [4H -> H], for 12 GEMM launches per step.  `--workload` selects
+the other FC workloads: the single small layer, the 3D-grid shards on a
+virtual grid, the hidden-16384 model and the layout sweep.
 
-Inputs are seeded synthetic bf16 (SplitMix64 + Box-Muller): activations and
-gradients ~N(0,1), weights ~N(0,0.02).  Every GEMM's operands are larger than
-the 129 MB L2, so no flush is needed between timed iterations.
+Inputs are seeded synthetic bf16: activations and gradients ~N(0,1), weights
+~N(0,0.02), and the sweep N(0,1)*0.05.  Every large GEMM's operands exceed the
+129 MB L2.  The small single-layer workload flushes L2 between timed steps by
+writing a 512 MB buffer.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--config C]
 
-Prints one JSON line (rank 0).  Under torchrun with N > 1 every rank runs
-an independent replica on its own GPU (the path needs no collective on one
-GPU per rank); the value is the total over ranks divided by the slowest
-rank's time.  `--impl reference` times the fp64 CPU oracle on the host
-cores over a bounded sample of the same workload.
+Rank 0 prints one JSON line.  Under torchrun with N > 1, every rank runs an
+independent replica on its own GPU; the path needs no collective when each
+rank has its own GPU.  The value is then the total over ranks divided by the
+slowest rank's time.  `--impl reference` times the fp64 CPU oracle on the
+host cores over a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -36,27 +41,59 @@ if ROOT not in sys.path:
 
 METRIC = "TFLOP/s per FC GEMM (fwd/dgrad/wgrad) and % of GB300 dense bf16 peak, 1 GPU"
 UNIT = "TFLOP/s"
-H, T_TOK, BATCH, SEQ = 6144, 8192, 4, 2048
-LAYERS = [("qkv", H, 3 * H), ("out", H, H), ("up", H, 4 * H), ("down", 4 * H, H)]
-SEED = 1002
-WORKLOAD = (f"GPT block FC layers, H={H}, T={T_TOK} (batch {BATCH} x seq {SEQ}): "
-            "qkv [H->3H], out [H->H], up [H->4H], down [4H->H]; fwd+dgrad+wgrad each, full layers")
+CPU_STRIPE_ROWS = 16      # output rows of every GEMM the CPU oracle computes per sample
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _gpt(H, T, mlp):
+    return [("qkv", T, H, 3 * H), ("out", T, H, H), ("up", T, H, mlp), ("down", T, mlp, H)]
+
+
+SWEEP_DIMS = (1000, 4096, 5000, 12288)
+WORKLOADS = {
+    "gpt_h6144_t8192": dict(
+        desc="GPT block FC layers, H=6144, T=8192 (batch 4 x seq 2048): qkv [H->3H], "
+             "out [H->H], up [H->4H], down [4H->H]; fwd+dgrad+wgrad each, full layers",
+        layers=_gpt(6144, 8192, 4 * 6144), batch=4, seq=2048, seed=1002),
+    "single_layer_t256": dict(
+        desc="single FC layer X[256x512] W[512x2048], grid 1x1x1; L2 flushed between steps",
+        layers=[("fc", 256, 512, 2048)], batch=1, seq=256, seed=1001, flush=True),
+    "gpt_h6144_t8192_vgrid_2x2x2": dict(
+        desc="GPT block H=6144, T=8192 as a virtual 2x2x2 grid of 3D-PMM block products "
+             "(T by Gz, K by Gx, N by Gy), partials summed on device",
+        layers=_gpt(6144, 8192, 4 * 6144), batch=4, seq=2048, seed=1003, grid=(2, 2, 2)),
+    "large_h16384_t4096": dict(
+        desc="large-model FC layers, hidden 16384, MLP 53248, T=4096: qkv [16384->18432], "
+             "out [16384->16384], up [16384->53248], down [53248->16384]; full layers",
+        layers=[("qkv", 4096, 16384, 18432), ("out", 4096, 16384, 16384),
+                ("up", 4096, 16384, 53248), ("down", 4096, 53248, 16384)],
+        batch=2, seq=2048, seed=1004),
+    "large_h16384_t4096_vgrid_1x4x4": dict(
+        desc="large-model FC layers (hidden 16384, MLP 53248, T=4096) as a virtual 1x4x4 "
+             "grid (T_blk=1024), partials summed on device",
+        layers=[("qkv", 4096, 16384, 18432), ("out", 4096, 16384, 16384),
+                ("up", 4096, 16384, 53248), ("down", 4096, 53248, 16384)],
+        batch=2, seq=2048, seed=1004, grid=(1, 4, 4)),
+    "layout_sweep": dict(
+        desc="layout/shape sweep: T in {512,2048,8192,16384} x K,N in {1000,4096,5000,12288}, "
+             "NN (fwd) / NT (dgrad) / TN (wgrad), values N(0,1)*0.05",
+        layers=[(f"T{T}_K{K}_N{N}", T, K, N) for T in (512, 2048, 8192, 16384)
+                for K in SWEEP_DIMS for N in SWEEP_DIMS],
+        batch=None, seq=None, seed=1005, scale=0.05, device_inputs=True),
+}
+DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 DATA = ("synthetic, seeded: SplitMix64 + Box-Muller bf16; activations/grads N(0,1), "
         "weights N(0,0.02)")
-CPU_STRIPE_ROWS = 16      # rows of every GEMM the CPU oracle computes per sample
 
 
-def gemms():
-    """The 12 products of one step: (layer, op, M, N, R, tensor names)."""
+def gemms(layers):
+    """The products of one step: (layer, op, T, K, N, M, Ncols, R, tensor names)."""
     out = []
-    for name, K, N in LAYERS:
-        out.append((name, "fwd", T_TOK, N, K, ("X", "W", "Y")))
-        out.append((name, "dgrad", T_TOK, K, N, ("dY", "W", "dX")))
-        out.append((name, "wgrad", K, N, T_TOK, ("X", "dY", "dW")))
+    for name, T, K, N in layers:
+        out.append((name, "fwd", T, K, N, T, N, K, ("X", "W", "Y")))
+        out.append((name, "dgrad", T, K, N, T, K, N, ("dY", "W", "dX")))
+        out.append((name, "wgrad", T, K, N, K, N, T, ("X", "dY", "dW")))
     return out
-
-
-FLOPS_PER_STEP = sum(2.0 * m * n * r for _, _, m, n, r, _ in gemms())
 
 
 def read_peaks():
@@ -66,25 +103,41 @@ def read_peaks():
             d = json.load(f)
         return {"burst": float(d["bf16_tflops"]),
                 "sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
-                "hbm_gbs": float(d.get("hbm_gbs", 0.0)) or None,
+                "hbm_gbs": float(d.get("hbm_gbs", 6800.0)),
                 "source": "measured"}
     except (OSError, KeyError, ValueError, TypeError):
         return {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
 
 
 # ------------------------------------------------------------------ inputs
-def host_inputs(layers=LAYERS):
+def host_inputs(wl, layers):
     """Seeded bf16 bits of the layers' X, W and dY (numpy uint16)."""
     import fc_inputs
+    scale = wl.get("scale")
     data = {}
-    for name, K, N in layers:
-        tid = 16 * ([l[0] for l in LAYERS].index(name) + 1)
+    names = [l[0] for l in wl["layers"]]
+    for name, T, K, N in layers:
+        tid = 16 * (names.index(name) + 1)
         data[name] = {
-            "X": fc_inputs.normal_bf16((T_TOK, K), SEED, tid + 1),
-            "W": fc_inputs.normal_bf16((K, N), SEED, tid + 2, sigma=0.02),
-            "dY": fc_inputs.normal_bf16((T_TOK, N), SEED, tid + 3),
+            "X": fc_inputs.normal_bf16((T, K), wl["seed"], tid + 1, sigma=scale or 1.0),
+            "W": fc_inputs.normal_bf16((K, N), wl["seed"], tid + 2, sigma=scale or 0.02),
+            "dY": fc_inputs.normal_bf16((T, N), wl["seed"], tid + 3, sigma=scale or 1.0),
         }
     return data
+
+
+def device_inputs(wl, layers, dev):
+    """Seeded bf16 operands drawn on the device (for workloads too large to
+    draw on the host in a benchmark run)."""
+    import torch
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl["seed"])
+    scale = wl.get("scale") or 1.0
+    out = {}
+    for name, T, K, N in layers:
+        out[name] = {k: (torch.randn(shape, generator=g, device=dev) * scale).to(torch.bfloat16)
+                     for k, shape in (("X", (T, K)), ("W", (K, N)), ("dY", (T, N)))}
+    return out
 
 
 # ------------------------------------------------------------------ clocks
@@ -98,6 +151,7 @@ class ClockSampler:
     def __init__(self, gpu_index):
         self.proc = None
         self.gpu_index = gpu_index
+        self.lines = []
 
     def __enter__(self):
         try:
@@ -111,7 +165,6 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
-        self.lines = []
         if self.proc is not None:
             time.sleep(0.25)
             self.proc.terminate()
@@ -125,7 +178,7 @@ class ClockSampler:
 
     def summary(self):
         sm, smax, reasons = [], [], set()
-        for ln in getattr(self, "lines", []):
+        for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -144,13 +197,13 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle
-def oracle_stripes(data, which, rows):
+def oracle_stripes(data, glist, which, rows):
     """fp64 oracle on the first `rows` output rows of the listed GEMMs;
     returns (flops, seconds, threads used)."""
     import oracle
     flops, secs = 0.0, 0.0
     for gi in which:
-        name, op, m, n, r, (pn, qn, _) = gemms()[gi]
+        name, op, T, K, N, m, n, r, (pn, qn, _) = glist[gi]
         d = data[name]
         if op == "wgrad":
             P = d[pn][:, :rows]        # X[:, k-stripe] -> rows of dW
@@ -160,28 +213,45 @@ def oracle_stripes(data, which, rows):
         t0 = time.perf_counter()
         oracle.fc(op, P, Q)
         secs += time.perf_counter() - t0
-        flops += 2.0 * rows * n * r
+        flops += 2.0 * min(rows, m) * n * r
     return flops, secs, min(oracle.max_threads(), rows)
 
 
-def cpu_baseline(data):
-    flops, secs, cores = oracle_stripes(data, range(len(gemms())), CPU_STRIPE_ROWS)
+def cpu_baseline(data, glist):
+    flops, secs, cores = oracle_stripes(data, glist, range(len(glist)), CPU_STRIPE_ROWS)
     return {"value": flops / secs / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"first {CPU_STRIPE_ROWS} output rows of each of the 12 GEMMs "
+            "sample": f"first {CPU_STRIPE_ROWS} output rows of each of the {len(glist)} GEMMs "
                       f"({flops / 1e9:.1f} GFLOP, {secs:.1f} s)"}
+
+
+def config_block(wl, name, world):
+    cfg = {"workload": f"{name}: {wl['desc']}"}
+    if wl.get("batch"):
+        cfg.update(global_batch=wl["batch"] * world, seq_len=wl["seq"])
+    cfg["grid"] = "x".join(str(g) for g in wl.get("grid", (1, 1, 1)))
+    cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
+    cfg["l2"] = ("L2 flushed between timed steps (512 MB write)" if wl.get("flush")
+                 else "operands exceed the 129 MB L2; no flush")
+    return cfg
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    data = host_inputs()
-    n = len(gemms())
+    wl = WORKLOADS[args.workload]
+    if wl.get("device_inputs"):
+        layers = wl["layers"][:: max(1, len(wl["layers"]) // 8)]
+    else:
+        layers = wl["layers"]
+    data = host_inputs(wl, layers)
+    glist = gemms(layers)
+    n = len(glist)
     for s in range(args.warmup):
-        oracle_stripes(data, [s % n], CPU_STRIPE_ROWS)
+        oracle_stripes(data, glist, [s % n], CPU_STRIPE_ROWS)
     tot_f, tot_s, cores = 0.0, 0.0, 1
     for s in range(args.steps):
-        f, sec, cores = oracle_stripes(data, [s % n], CPU_STRIPE_ROWS)
+        f, sec, cores = oracle_stripes(data, glist, [s % n], CPU_STRIPE_ROWS)
         tot_f += f
         tot_s += sec
     value = tot_f / tot_s / 1e12
@@ -189,11 +259,11 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
-            "config": {"workload": WORKLOAD, "global_batch": BATCH, "seq_len": SEQ,
+            "config": {**config_block(wl, args.workload, 1),
                        "parallelism": "host cores (OpenMP)"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": f"each step: first {CPU_STRIPE_ROWS} output rows of one "
-                                       "of the 12 GEMMs, cycling"},
+                                       f"of the {n} GEMMs, cycling"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -202,7 +272,6 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args):
-    import numpy as np
     import torch
     import torch.distributed as dist
 
@@ -225,107 +294,132 @@ def run_ours(args):
     fc.axonn_set_kernel_config(args.config)
     sms, max_pairs = fc.axonn_device_info()
 
+    wl = WORKLOADS[args.workload]
+    grid = wl.get("grid", (1, 1, 1))
+    flags = fc.VGRID if grid != (1, 1, 1) else 0
     only = tuple(args.only.split(":")) if args.only else None
-    layers = [l for l in LAYERS if only is None or l[0] == only[0]]
-    data = host_inputs(layers)
-    dbuf, hbuf_in, hbuf_out = {}, {}, {}
-    for name, K, N in layers:
-        d = {k: fc_inputs.as_torch_bf16(v, dev) for k, v in data[name].items()}
-        d["Y"] = torch.empty((T_TOK, N), dtype=torch.bfloat16, device=dev)
-        d["dX"] = torch.empty((T_TOK, K), dtype=torch.bfloat16, device=dev)
-        d["dW"] = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
-        dbuf[name] = d
-    stream = torch.cuda.Stream(device=dev)
+    layers = [l for l in wl["layers"] if only is None or l[0] == only[0]]
+    glist = [g for g in gemms(layers) if only is None or (g[0], g[1]) == only]
+
+    data = None
+    if wl.get("device_inputs"):
+        dbuf = device_inputs(wl, layers, dev)
+    else:
+        data = host_inputs(wl, layers)
+        dbuf = {name: {k: fc_inputs.as_torch_bf16(v, dev) for k, v in data[name].items()}
+                for name in data}
+    for name, T, K, N in layers:
+        dbuf[name]["Y"] = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+        dbuf[name]["dX"] = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
+        dbuf[name]["dW"] = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+
     plan = []
-    for name, op, m, n, r, (pn, qn, cn) in gemms():
-        if only is not None and (name, op) != only:
-            continue
-        K = dict((l, k) for l, k, _ in LAYERS)[name]
-        N = dict((l, nn) for l, _, nn in LAYERS)[name]
-        plan.append((name, op, 2.0 * m * n * r, dbuf[name][pn], dbuf[name][qn], dbuf[name][cn],
-                     fc.Shape(T_TOK, K, N), (m, n, r)))
+    ws_need = 0
+    for name, op, T, K, N, m, n, r, (pn, qn, cn) in glist:
+        shape = fc.Shape(T, K, N, grid)
+        ws_need = max(ws_need, fc.axonn_fc_workspace_size(op, shape, flags))
+        plan.append(dict(name=name, op=op, flops=2.0 * m * n * r, mnr=(m, n, r),
+                         P=dbuf[name][pn], Q=dbuf[name][qn], C=dbuf[name][cn], shape=shape,
+                         bytes=2.0 * (m * r + r * n + m * n)))
+    ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if wl.get("flush") else None
+    stream = torch.cuda.Stream(device=dev)
+    used = [None] * len(plan)
+    reduce_launches = sum(1 for g in glist
+                          if flags and {"fwd": grid[0], "dgrad": grid[1], "wgrad": grid[2]}[g[1]] > 1)
 
     def step(events=None):
-        for gi, (name, op, _, P, Q, C, shape, _mnr) in enumerate(plan):
+        for gi, g in enumerate(plan):
             if events is not None:
                 events[gi][0].record(stream)
-            fc.call(op, P, Q, C, shape, 0, None, stream=stream)
+            fc.call(g["op"], g["P"], g["Q"], g["C"], g["shape"], flags, ws, stream=stream)
             if events is not None:
                 events[gi][1].record(stream)
                 used[gi] = fc.axonn_last_kernel_config()
 
-    used = [None] * len(plan)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
+            if flush is not None:
+                flush.fill_(1)
     fc.axonn_sync_status(stream)
 
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in plan]
           for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gpu_index = int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local)).split(",")[0]) \
-        if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    gpu_index = int(vis) if vis.isdigit() else local
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clocks:
-        t0.record(stream)
-        for s in range(args.steps):
-            step(ev[s])
-        t1.record(stream)
+        with torch.cuda.stream(stream):
+            for s in range(args.steps):
+                step_ev[s][0].record(stream)
+                step(ev[s])
+                step_ev[s][1].record(stream)
+                if flush is not None:
+                    flush.fill_(1)        # outside the step's events
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     fc.axonn_sync_status(stream)
-    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     if world > 1:
         t = torch.tensor([elapsed_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_ms = float(t.item())
-    launches = args.steps * len(plan)
+    launches = args.steps * (len(plan) + reduce_launches)
 
-    # per-GEMM device times (median over steps) and the dominant kernel's rate
+    peaks = read_peaks()
     per = []
     gemm_ms_total = 0.0
-    flops_per_step = sum(p[2] for p in plan)
-    for gi, (name, op, fl, P, Q, C, shape, (m, n, r)) in enumerate(plan):
+    flops_per_step = sum(g["flops"] for g in plan)
+    for gi, g in enumerate(plan):
         ms = [ev[s][gi][0].elapsed_time(ev[s][gi][1]) for s in range(args.steps)]
         gemm_ms_total += sum(ms)
         med = statistics.median(ms)
-        per.append({"layer": name, "op": op, "M": m, "N": n, "R": r, "layout": {"fwd": "NN", "dgrad": "NT", "wgrad": "TN"}[op],
-                    "ms": round(med, 4), "tflops": round(fl / med / 1e9, 1),
+        tf = g["flops"] / med / 1e9
+        gbs = g["bytes"] / med / 1e6
+        m, n, r = g["mnr"]
+        per.append({"layer": g["name"], "op": g["op"], "M": m, "N": n, "R": r,
+                    "layout": {"fwd": "NN", "dgrad": "NT", "wgrad": "TN"}[g["op"]],
+                    "ms": round(med, 4), "tflops": round(tf, 1),
+                    "frac_of_sustained": round(tf / peaks["sustained"], 4),
+                    "frac_of_burst": round(tf / peaks["burst"], 4),
+                    "gbs": round(gbs, 1), "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
                     "config": fc.axonn_kernel_config_name(used[gi])})
-    peaks = read_peaks()
-    for p in per:
-        p["frac_of_sustained"] = round(p["tflops"] / peaks["sustained"], 4)
-        p["frac_of_burst"] = round(p["tflops"] / peaks["burst"], 4)
     achieved = flops_per_step * args.steps / (gemm_ms_total * 1e9)
 
-    # end to end: host (pinned) -> device copies, the 12 GEMMs, device -> host
+    # end to end: host (pinned) -> device copies, the GEMMs, device -> host
     h2d_bytes = d2h_bytes = 0
-    e2e_steps = 0 if (args.no_e2e or only is not None) else max(1, min(args.steps, 10))
-    for name, K, N in (layers if e2e_steps else []):
-        hbuf_in[name] = {k: torch.empty(v.shape, dtype=torch.bfloat16, pin_memory=True)
-                         for k, v in dbuf[name].items() if k in ("X", "W", "dY")}
-        for k in hbuf_in[name]:
-            hbuf_in[name][k].copy_(dbuf[name][k])
-            h2d_bytes += hbuf_in[name][k].numel() * 2
-        hbuf_out[name] = {k: torch.empty(dbuf[name][k].shape, dtype=torch.bfloat16,
-                                         pin_memory=True) for k in ("Y", "dX", "dW")}
-        for k in hbuf_out[name]:
-            d2h_bytes += hbuf_out[name][k].numel() * 2
+    io_bytes = sum(t.numel() * 2 for d in dbuf.values() for t in d.values())
+    e2e_steps = 0
+    if not (args.no_e2e or only is not None or io_bytes > (24 << 30)):
+        e2e_steps = max(1, min(args.steps, 10))
+    hin, hout = {}, {}
+    for name, T, K, N in (layers if e2e_steps else []):
+        hin[name] = {k: torch.empty(dbuf[name][k].shape, dtype=torch.bfloat16, pin_memory=True)
+                     for k in ("X", "W", "dY")}
+        for k, hb in hin[name].items():
+            hb.copy_(dbuf[name][k])
+            h2d_bytes += hb.numel() * 2
+        hout[name] = {k: torch.empty(dbuf[name][k].shape, dtype=torch.bfloat16, pin_memory=True)
+                      for k in ("Y", "dX", "dW")}
+        d2h_bytes += sum(hb.numel() * 2 for hb in hout[name].values())
 
     def e2e_step():
-        for name, _, _ in layers:
-            for k, hb in hbuf_in[name].items():
+        for name in hin:
+            for k, hb in hin[name].items():
                 dbuf[name][k].copy_(hb, non_blocking=True)
         step()
-        for name, _, _ in layers:
-            for k, hb in hbuf_out[name].items():
+        for name in hout:
+            for k, hb in hout[name].items():
                 hb.copy_(dbuf[name][k], non_blocking=True)
 
     e2e_ms = 0.0
     if e2e_steps:
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e2e_step()
             torch.cuda.synchronize()
@@ -337,11 +431,11 @@ def run_ours(args):
             t1.record(stream)
             torch.cuda.synchronize()
         e2e_ms = t0.elapsed_time(t1)
-    fc.axonn_sync_status(stream)
-    if world > 1 and e2e_steps:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+        fc.axonn_sync_status(stream)
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
 
     if rank == 0:
         line = {
@@ -349,18 +443,18 @@ def run_ours(args):
             "value": round(world * flops_per_step * args.steps / (elapsed_ms * 1e9), 2),
             "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(elapsed_ms / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": DATA,
-            "config": {"workload": WORKLOAD, "global_batch": BATCH * world, "seq_len": SEQ,
-                       "hidden": H, "tokens_per_gpu": T_TOK,
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                       "l2": "every GEMM's operands exceed the 129 MB L2; no flush"},
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": DATA if not wl.get("scale") else
+            DATA.replace("activations/grads N(0,1), weights N(0,0.02)", "all operands N(0,1)*0.05"),
+            "config": config_block(wl, args.workload, world),
             "per_gemm": per,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                          "peak": peaks["sustained"], "unit": "TFLOP/s",
                          "frac": round(achieved / peaks["sustained"], 4),
                          "frac_of_burst": round(achieved / peaks["burst"], 4),
                          "peak_source": f"{peaks['source']} (sustained; burst {peaks['burst']})",
-                         "kernel": "fc_gemm_tcgen05_kernel",
+                         "kernel": "fc_gemm_tcgen05_kernel" + (
+                             " (+ vgrid_reduce_kernel inside each timed call)" if flags else ""),
                          "traffic": None},
             "e2e": ({"value": round(world * flops_per_step * e2e_steps / (e2e_ms * 1e9), 2),
                      "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
@@ -373,9 +467,8 @@ def run_ours(args):
         }
         if only is not None:
             line["profile_case"] = f"{only[0]}:{only[1]} only"
-            line["config"]["workload"] = f"{WORKLOAD}; this run: {only[0]} {only[1]} only"
-        elif not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline(data)
+        elif data is not None and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(data, glist)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -388,11 +481,12 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--config", type=int, default=-1,
+                    help="force one kernel configuration (-1: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--config", type=int, default=-1,
-                    help="force one kernel configuration (-1: the library's choice)")
     ap.add_argument("--only", default=None, metavar="LAYER:OP",
                     help="time one GEMM (e.g. out:fwd) for profiling; not a bench line")
     args = ap.parse_args()
