@@ -149,8 +149,46 @@ axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void*
                                      int64_t ldq, int64_t ldc, const axonn_fc_shape_t* shape,
                                      uint32_t flags, cudaStream_t stream);
 
+/*
+ * Per-shape tuning -- the GB300 counterpart of the pages' "automated BLAS
+ * kernel tuning" (TL;DR of the sciencestack.ai page; "The reading", review of
+ * arXiv 2502.08145).  Runs this call once per candidate -- every kernel
+ * configuration x rasterisation group {8, 16, 32}, and, for products that
+ * leave SMs idle and have workspace, reduction splits {2, 4, 8} -- times
+ * each with CUDA events on `stream` (the call synchronises the stream), and
+ * records the fastest for later calls with the same op, sizes, grid, block
+ * and flags on a GPU with the same SM count.  Arguments are those of the
+ * op's entry point (op is an axonn_op_t); the caller's output is
+ * overwritten (with AXONN_ACCUM_F32 the runs overwrite instead of adding,
+ * so tune on a scratch output).  Not for use during stream capture.  Any
+ * of the result pointers may be NULL.
+ */
+axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int64_t ldp,
+                             int64_t ldq, int64_t ldc, const axonn_fc_shape_t* shape,
+                             uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream,
+                             int* best_config, int* best_split, int* best_group_m,
+                             float* best_us);
+
+/* The tuning table as text, one JSON object per line:
+ *   {"key": "...", "config": "<name>", "split": S, "group_m": G, "us": t}
+ * save writes every entry; load merges a file's entries into the table
+ * (AXONN_ERR_INVALID_ARG on an unreadable file or a malformed line, leaving
+ * the table unchanged).  Host-only. */
+axonn_status_t axonn_tune_cache_save(const char* path);
+axonn_status_t axonn_tune_cache_load(const char* path);
+void axonn_tune_cache_clear(void);
+int axonn_tune_cache_size(void);
+
+/* How the last call on this thread ran: kernel configuration, reduction
+ * split and rasterisation group. */
+void axonn_last_choice(int* config, int* split, int* group_m);
+
 /* Workspace bytes an op needs with these flags (0 when none).  `op` is an
- * axonn_op_t.  Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
+ * axonn_op_t.  With AXONN_VGRID it is the fp32 partials of the reduced grid
+ * axis; without, it is nonzero only for products that leave most SMs idle
+ * (fewer 128x256 tiles than two waves), which may then split their
+ * reduction range -- passing less workspace just disables the split.
+ * Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
                                        size_t* bytes);
 

@@ -27,7 +27,9 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ER
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]
 
 EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_static",
-           "axonn_fc_workspace_size",
+           "axonn_fc_workspace_size", "axonn_fc_tune", "axonn_tune_cache_save",
+           "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
+           "axonn_last_choice",
            "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs", "axonn_device_info",
            "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
@@ -79,6 +81,19 @@ def load(path: str | None = None):
         lib.axonn_fc_vgrid_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64,
                                               ctypes.POINTER(Shape), u32, vp]
         lib.axonn_fc_vgrid_static.restype = ctypes.c_int
+        lib.axonn_fc_tune.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64, ctypes.POINTER(Shape),
+                                      u32, vp, sz, vp, ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                      ctypes.POINTER(ctypes.c_float)]
+        lib.axonn_fc_tune.restype = ctypes.c_int
+        lib.axonn_tune_cache_save.argtypes = [ctypes.c_char_p]
+        lib.axonn_tune_cache_save.restype = ctypes.c_int
+        lib.axonn_tune_cache_load.argtypes = [ctypes.c_char_p]
+        lib.axonn_tune_cache_load.restype = ctypes.c_int
+        lib.axonn_tune_cache_clear.restype = None
+        lib.axonn_tune_cache_size.restype = ctypes.c_int
+        lib.axonn_last_choice.argtypes = [ctypes.POINTER(ctypes.c_int)] * 3
+        lib.axonn_last_choice.restype = None
         lib.axonn_fc_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(Shape), u32,
                                                 ctypes.POINTER(sz)]
         lib.axonn_fc_workspace_size.restype = ctypes.c_int
@@ -175,6 +190,43 @@ def axonn_fc_vgrid_static(op, P, Q, C, shape: Shape, flags: int = 0, ldp=None, l
     st = load().axonn_fc_vgrid_static(int(op), _ptr(P), _ptr(Q), _ptr(C), _ld(P, ldp), _ld(Q, ldq),
                                       _ld(C, ldc), ctypes.byref(shape), flags, _stream(stream))
     _check(st)
+
+
+def axonn_fc_tune(op, P, Q, C, shape: Shape, flags: int = 0, ws=None, ldp=None, ldq=None,
+                  ldc=None, stream=None):
+    """Time every candidate way to run this call and remember the fastest;
+    returns (config, split, group_m, microseconds).  Overwrites C."""
+    op = OPS.get(op, op)
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    c, sp, gm, us = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_float()
+    _check(load().axonn_fc_tune(int(op), _ptr(P), _ptr(Q), _ptr(C), _ld(P, ldp), _ld(Q, ldq),
+                                _ld(C, ldc), ctypes.byref(shape), flags, _ptr(ws), ws_bytes,
+                                _stream(stream), ctypes.byref(c), ctypes.byref(sp),
+                                ctypes.byref(gm), ctypes.byref(us)))
+    return c.value, sp.value, gm.value, us.value
+
+
+def axonn_tune_cache_save(path: str):
+    _check(load().axonn_tune_cache_save(os.fsencode(path)))
+
+
+def axonn_tune_cache_load(path: str):
+    _check(load().axonn_tune_cache_load(os.fsencode(path)))
+
+
+def axonn_tune_cache_clear():
+    load().axonn_tune_cache_clear()
+
+
+def axonn_tune_cache_size() -> int:
+    return int(load().axonn_tune_cache_size())
+
+
+def axonn_last_choice():
+    """(config, split, group_m) of the last call on this thread."""
+    c, s, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    load().axonn_last_choice(ctypes.byref(c), ctypes.byref(s), ctypes.byref(g))
+    return c.value, s.value, g.value
 
 
 def axonn_fc_workspace_size(op, shape: Shape, flags: int = 0) -> int:

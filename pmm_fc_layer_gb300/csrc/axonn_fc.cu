@@ -5,12 +5,17 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
+#include <fstream>
 #include <mutex>
+#include <sstream>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "axonn_fc.h"
@@ -299,6 +304,26 @@ struct LaunchPlan {
   std::vector<Block> blocks;
 };
 
+// One way to run a call: kernel configuration, split of the reduction range
+// into `split` slices summed in fixed order (needs workspace), and the
+// rasterisation group height.
+struct TuneChoice {
+  int config = -1;
+  int split = 1;
+  int group_m = 16;
+};
+thread_local TuneChoice t_last_choice;
+
+struct TuneEntry {
+  TuneChoice choice;
+  double us = 0;
+};
+std::mutex g_tune_mu;
+std::unordered_map<std::string, TuneEntry> g_tune;  // call signature -> fastest choice
+
+constexpr int kMaxSplit = 8;
+constexpr int64_t kSplitMinR = 128;
+
 template <int MAXP>
 axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vector<Block>& blocks,
                            const KernelConfig& c, int group_m) {
@@ -418,11 +443,41 @@ int choose_config(const std::vector<Block>& blocks, const DeviceState& dev) {
   return best;
 }
 
+// Split of the reduction range is offered for products that leave most
+// SMs idle: fewer 128x256 tiles than two waves, and a reduction of at least
+// 512.  Slices are whole 64-deep stages.
+bool split_eligible(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
+  const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  return tiles < 2 * dev.sms && R >= 4 * kSplitMinR;
+}
+
+size_t split_ws_bytes(int64_t M, int64_t N, int split) {
+  const int64_t ldp = (N + 7) / 8 * 8;
+  return static_cast<size_t>(split) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * 4u;
+}
+
+// Default split: the largest power of two up to kMaxSplit that keeps the
+// 128x128 tiles within one wave and every slice at least kSplitMinR deep.
+int choose_split(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
+  const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  int split = 1;
+  while (split < kMaxSplit && tiles * split * 2 <= dev.sms && R / (split * 2) >= kSplitMinR) split *= 2;
+  return split;
+}
+
+std::string tune_key(int op, const axonn_fc_shape_t& s, uint32_t flags, int sms) {
+  char buf[256];
+  snprintf(buf, sizeof(buf), "op%d_T%lld_K%lld_N%lld_g%dx%dx%d_at%d.%d.%d_f%x_sm%d", op,
+           (long long)s.T, (long long)s.K, (long long)s.N, s.gx, s.gy, s.gz, s.x, s.y, s.z, flags,
+           sms);
+  return buf;
+}
+
 // Shared body of the three entry points.  P and Q are the op's first and
-// second stored operands, C its output.
+// second stored operands, C its output.  `force` (tuning) fixes the choice.
 axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp, int64_t ldq,
                      int64_t ldc, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
-                     size_t ws_bytes, cudaStream_t stream) {
+                     size_t ws_bytes, cudaStream_t stream, const TuneChoice* force = nullptr) {
   axonn_status_t st = check_shape(op, shape, flags);
   if (st != AXONN_OK) return st;
   const axonn_fc_shape_t& s = *shape;
@@ -538,9 +593,79 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     b.out_mode = user_mode;
     plan.blocks.push_back(b);
   }
-  plan.config = choose_config(plan.blocks, *dev);
+
+  // How to run it: forced (tuning), tuned earlier, or the default choice.
+  TuneChoice ch;
+  if (force) {
+    ch = *force;
+  } else {
+    bool found = false;
+    {
+      std::lock_guard<std::mutex> lk(g_tune_mu);
+      auto it = g_tune.find(tune_key(op, s, flags, dev->sms));
+      if (it != g_tune.end()) {
+        ch = it->second.choice;
+        found = true;
+      }
+    }
+    if (!found) {
+      const Block& b0 = plan.blocks[0];
+      ch.split = (!vgrid && split_eligible(b0.M, b0.N, b0.R, *dev))
+                     ? choose_split(b0.M, b0.N, b0.R, *dev) : 1;
+      ch.config = ch.split > 1 ? 0 : choose_config(plan.blocks, *dev);
+      ch.group_m = 16;
+    }
+    const int forced_cfg = g_forced_config.load();
+    if (forced_cfg >= 0) ch.config = forced_cfg;
+  }
+  if (ch.config < 0 || ch.config >= kNumConfigs) ch.config = choose_config(plan.blocks, *dev);
+  if (ch.group_m < 1) ch.group_m = 16;
+
+  // Split of the reduction range: S slices of whole stages, fp32 partials in
+  // the workspace, then the fixed-order sum into the caller's output.
+  Block whole;
+  if (ch.split > 1) {
+    const Block& b0 = plan.blocks[0];
+    const bool ws_ok = !vgrid && ws && aligned16(ws) &&
+                       ws_bytes >= split_ws_bytes(b0.M, b0.N, ch.split) && b0.R >= ch.split;
+    if (!ws_ok) ch.split = 1;
+  }
+  int64_t ld_split = 0;
+  if (ch.split > 1) {
+    whole = plan.blocks[0];
+    plan.blocks.clear();
+    ld_split = (whole.N + 7) / 8 * 8;
+    const int64_t units = (whole.R + 63) / 64;
+    for (int sidx = 0; sidx < ch.split; ++sidx) {
+      const int64_t u0 = units * sidx / ch.split, u1 = units * (sidx + 1) / ch.split;
+      const int64_t r0 = 64 * u0, r1 = std::min<int64_t>(64 * u1, whole.R);
+      Block b = whole;
+      b.A = whole.A + 2 * (v.a_mn ? r0 * v.lda : r0);
+      b.B = whole.B + 2 * (v.b_mn ? r0 * v.ldb : r0);
+      b.R = r1 > r0 ? r1 - r0 : 0;
+      b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(sidx) * whole.M * ld_split);
+      b.ldc = ld_split;
+      b.out_mode = axonn::kOutF32;
+      plan.blocks.push_back(b);
+    }
+  }
+  plan.config = ch.config;
+  plan.group_m = ch.group_m;
+  t_last_choice = ch;
   st = run_blocks(v, plan, *dev, stream);
   if (st != AXONN_OK) return st;
+
+  if (ch.split > 1) {
+    const int64_t groups = whole.M * ((whole.N + 7) / 8);
+    int64_t nblk = (groups + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(dev->sms) * 8;
+    if (nblk > cap) nblk = cap;
+    axonn::vgrid_reduce_kernel<<<static_cast<int>(nblk), 256, 0, stream>>>(
+        static_cast<const float*>(ws), ch.split, whole.M * ld_split, ld_split,
+        static_cast<int>(whole.M), static_cast<int>(whole.N), whole.C, whole.ldc, whole.out_mode);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "split reduction launch: %s", cudaGetErrorString(e));
+  }
 
   if (partials) {
     const int64_t groups = M * ((N + 7) / 8);
@@ -635,12 +760,177 @@ axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t l
   return fc_op(AXONN_OP_WGRAD, X, dY, dW, ldx, lddy, lddw, shape, flags, ws, ws_bytes, stream);
 }
 
+axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int64_t ldp, int64_t ldq,
+                             int64_t ldc, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                             size_t ws_bytes, cudaStream_t stream, int* best_config, int* best_split,
+                             int* best_group_m, float* best_us) {
+  axonn_status_t st = check_shape(op, shape, flags);
+  if (st != AXONN_OK) return st;
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+  const axonn_fc_shape_t& s = *shape;
+  // Tuning runs the product many times: an accumulating call is timed as an
+  // overwriting one (the caller's output is overwritten either way).
+  const uint32_t run_flags =
+      (flags & AXONN_ACCUM_F32) ? ((flags & ~AXONN_ACCUM_F32) | AXONN_OUT_F32) : flags;
+  int64_t M, N, R;
+  full_dims(op, s, &M, &N, &R);
+  Range rows{0, M}, red{0, R}, cols{0, N};
+  if (s.gx * s.gy * s.gz > 1 && !(flags & AXONN_VGRID))
+    block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
+
+  std::vector<TuneChoice> cands;
+  for (int c = 0; c < kNumConfigs; ++c)
+    for (int gm : {8, 16, 32}) cands.push_back(TuneChoice{c, 1, gm});
+  if (!(flags & AXONN_VGRID) && split_eligible(rows.len(), cols.len(), red.len(), *dev))
+    for (int c = 0; c < 2; ++c)
+      for (int sp = 2; sp <= kMaxSplit; sp *= 2)
+        if (red.len() / sp >= kSplitMinR && ws && ws_bytes >= split_ws_bytes(rows.len(), cols.len(), sp))
+          cands.push_back(TuneChoice{c, sp, 16});
+
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
+    if (e0) cudaEventDestroy(e0);
+    return fail(AXONN_ERR_CUDA, "cudaEventCreate failed");
+  }
+  constexpr int kReps = 3;
+  TuneEntry best;
+  best.us = -1;
+  for (const TuneChoice& c : cands) {
+    if (fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) != AXONN_OK)
+      continue;
+    if (t_last_choice.split != c.split) continue;  // the split could not be applied
+    cudaEventRecord(e0, stream);
+    bool okrun = true;
+    for (int r = 0; r < kReps && okrun; ++r)
+      okrun = fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) == AXONN_OK;
+    cudaEventRecord(e1, stream);
+    if (cudaEventSynchronize(e1) != cudaSuccess || !okrun) continue;
+    float ms = 0;
+    cudaEventElapsedTime(&ms, e0, e1);
+    const double us = 1e3 * ms / kReps;
+    if (best.us < 0 || us < best.us) {
+      best.us = us;
+      best.choice = c;
+    }
+  }
+  cudaEventDestroy(e0);
+  cudaEventDestroy(e1);
+  if (best.us < 0) return fail(AXONN_ERR_CUDA, "no candidate configuration ran");
+  {
+    std::lock_guard<std::mutex> lk(g_tune_mu);
+    g_tune[tune_key(op, s, flags, dev->sms)] = best;
+  }
+  if (best_config) *best_config = best.choice.config;
+  if (best_split) *best_split = best.choice.split;
+  if (best_group_m) *best_group_m = best.choice.group_m;
+  if (best_us) *best_us = static_cast<float>(best.us);
+  return ok();
+}
+
+axonn_status_t axonn_tune_cache_save(const char* path) {
+  if (!path) return fail(AXONN_ERR_INVALID_ARG, "path is NULL");
+  std::ofstream f(path);
+  if (!f) return fail(AXONN_ERR_INVALID_ARG, "cannot write %s", path);
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  for (const auto& kv : g_tune) {
+    char line[512];
+    snprintf(line, sizeof(line),
+             "{\"key\": \"%s\", \"config\": \"%s\", \"split\": %d, \"group_m\": %d, \"us\": %.3f}\n",
+             kv.first.c_str(), kConfigs[kv.second.choice.config].name, kv.second.choice.split,
+             kv.second.choice.group_m, kv.second.us);
+    f << line;
+  }
+  return f ? ok() : fail(AXONN_ERR_INVALID_ARG, "write to %s failed", path);
+}
+
+namespace {
+// Value of "name" in one line written by axonn_tune_cache_save.
+bool json_field(const std::string& line, const char* name, std::string* out) {
+  const std::string tag = std::string("\"") + name + "\": ";
+  const size_t p = line.find(tag);
+  if (p == std::string::npos) return false;
+  size_t b = p + tag.size(), e;
+  if (b < line.size() && line[b] == '"') {
+    e = line.find('"', b + 1);
+    if (e == std::string::npos) return false;
+    *out = line.substr(b + 1, e - b - 1);
+  } else {
+    e = line.find_first_of(",}", b);
+    if (e == std::string::npos) return false;
+    *out = line.substr(b, e - b);
+  }
+  return true;
+}
+}  // namespace
+
+axonn_status_t axonn_tune_cache_load(const char* path) {
+  if (!path) return fail(AXONN_ERR_INVALID_ARG, "path is NULL");
+  std::ifstream f(path);
+  if (!f) return fail(AXONN_ERR_INVALID_ARG, "cannot read %s", path);
+  std::string line;
+  std::unordered_map<std::string, TuneEntry> loaded;
+  int lineno = 0;
+  while (std::getline(f, line)) {
+    ++lineno;
+    if (line.find_first_not_of(" \t\r") == std::string::npos) continue;
+    std::string key, cfg, split, gm, us;
+    if (!json_field(line, "key", &key) || !json_field(line, "config", &cfg) ||
+        !json_field(line, "split", &split) || !json_field(line, "group_m", &gm) ||
+        !json_field(line, "us", &us))
+      return fail(AXONN_ERR_INVALID_ARG, "%s:%d: malformed tuning entry", path, lineno);
+    TuneEntry e;
+    e.choice.config = -1;
+    for (int c = 0; c < kNumConfigs; ++c)
+      if (cfg == kConfigs[c].name) e.choice.config = c;
+    e.choice.split = atoi(split.c_str());
+    e.choice.group_m = atoi(gm.c_str());
+    e.us = atof(us.c_str());
+    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m < 1)
+      return fail(AXONN_ERR_INVALID_ARG, "%s:%d: unknown configuration", path, lineno);
+    loaded[key] = e;
+  }
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  for (auto& kv : loaded) g_tune[kv.first] = kv.second;
+  return ok();
+}
+
+void axonn_tune_cache_clear(void) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  g_tune.clear();
+}
+
+int axonn_tune_cache_size(void) {
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  return static_cast<int>(g_tune.size());
+}
+
+void axonn_last_choice(int* config, int* split, int* group_m) {
+  if (config) *config = t_last_choice.config;
+  if (split) *split = t_last_choice.split;
+  if (group_m) *group_m = t_last_choice.group_m;
+}
+
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
                                        size_t* bytes) {
   if (!bytes) return fail(AXONN_ERR_INVALID_ARG, "bytes is NULL");
   axonn_status_t st = check_shape(op, shape, flags);
   if (st != AXONN_OK) return st;
   *bytes = vgrid_ws_bytes(op, *shape, flags);
+  if (!(flags & AXONN_VGRID)) {
+    // Products that leave SMs idle may split their reduction range.
+    DeviceState* dev = nullptr;
+    if (device_state(&dev) == AXONN_OK) {
+      const axonn_fc_shape_t& s = *shape;
+      int64_t M, N, R;
+      full_dims(op, s, &M, &N, &R);
+      Range rows{0, M}, red{0, R}, cols{0, N};
+      if (s.gx * s.gy * s.gz > 1) block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
+      if (rows.len() > 0 && cols.len() > 0 && split_eligible(rows.len(), cols.len(), red.len(), *dev))
+        *bytes = split_ws_bytes(rows.len(), cols.len(), kMaxSplit);
+    }
+  }
   return ok();
 }
 
