@@ -120,9 +120,11 @@ axonn_status_t device_state(DeviceState** out) {
                   dev, major, minor);
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
-    cudaError_t es[] = {set_smem_attr<128, 64, 6, 1>(), set_smem_attr<128, 64, 6, kMaxProblems>(),
-                        set_smem_attr<256, 64, 4, 1>(), set_smem_attr<256, 64, 4, kMaxProblems>(),
-                        set_pair_smem_attr<kPairStages, 1>(),
+    cudaError_t es[] = {set_smem_attr<128, 64, 6, 1>(), set_smem_attr<128, 64, 6, 8>(),
+                        set_smem_attr<128, 64, 6, kMaxProblems>(),
+                        set_smem_attr<256, 64, 4, 1>(), set_smem_attr<256, 64, 4, 8>(),
+                        set_smem_attr<256, 64, 4, kMaxProblems>(),
+                        set_pair_smem_attr<kPairStages, 1>(), set_pair_smem_attr<kPairStages, 8>(),
                         set_pair_smem_attr<kPairStages, kMaxProblems>()};
     for (cudaError_t x : es)
       if (x != cudaSuccess)
@@ -276,6 +278,10 @@ struct Block {
   int64_t ldc;
   int64_t M, N, R;
   int out_mode;
+  int phase = 1;               // 0: writes an fp32 partial that a phase-1 block reads
+  int red_count = 0;           // partials to add in the epilogue (last partial only)
+  const float* red_src = nullptr;
+  int64_t red_stride = 0, red_ld = 0;
 };
 
 // Kernel configurations the library can run.  A configuration fixes the
@@ -350,6 +356,10 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.b_mn = v.b_mn;
     d.idesc = make_idesc(c.bm, c.bn, v.a_mn, v.b_mn);
     d.out_mode = b.out_mode;
+    d.red_count = b.red_count;
+    d.red_src = b.red_src;
+    d.red_stride = b.red_stride;
+    d.red_ld = b.red_ld;
     if (b.R > 0) {
       axonn_status_t s;
       const uint32_t bk = static_cast<uint32_t>(c.bk);
@@ -399,21 +409,29 @@ axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const Device
   return AXONN_OK;
 }
 
+// The kernel parameter block holds a tensor-map pair per problem, so a
+// launch with few problems uses a smaller instantiation (less to copy per
+// launch): 1 problem, up to kFewProblems, or up to kMaxProblems.
+constexpr int kFewProblems = 8;
+
+template <int P1>
+axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
+                          const DeviceState& dev, cudaStream_t stream) {
+  switch (config) {
+    case 0: return launch_single<128, 64, 6, P1>(v, plan, dev, stream);
+    case 1: return launch_single<256, 64, 4, P1>(v, plan, dev, stream);
+    default: return launch_pair<kPairStages, P1>(v, plan, dev, stream);
+  }
+}
+
 axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
                           cudaStream_t stream) {
-  const bool many = plan.blocks.size() > 1;
   t_last_config = plan.config;
-  switch (plan.config) {
-    case 0:
-      return many ? launch_single<128, 64, 6, kMaxProblems>(v, plan, dev, stream)
-                  : launch_single<128, 64, 6, 1>(v, plan, dev, stream);
-    case 1:
-      return many ? launch_single<256, 64, 4, kMaxProblems>(v, plan, dev, stream)
-                  : launch_single<256, 64, 4, 1>(v, plan, dev, stream);
-    default:
-      return many ? launch_pair<kPairStages, kMaxProblems>(v, plan, dev, stream)
-                  : launch_pair<kPairStages, 1>(v, plan, dev, stream);
-  }
+  const size_t n = plan.blocks.size();
+  if (n <= 1) return launch_cfg<1>(plan.config, v, plan, dev, stream);
+  if (n <= static_cast<size_t>(kFewProblems))
+    return launch_cfg<kFewProblems>(plan.config, v, plan, dev, stream);
+  return launch_cfg<kMaxProblems>(plan.config, v, plan, dev, stream);
 }
 
 // Work units (tile slots) a configuration needs, counted in waves of the
@@ -570,11 +588,22 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
           b.A = a_at(br.s, bred.s);
           b.B = b_at(bred.s, bc.s);
           b.M = br.len(); b.N = bc.len(); b.R = bred.len();
-          if (partials) {
-            const int g = reduce_coord(op, x, y, z);
+          const int g = reduce_coord(op, x, y, z);
+          if (partials && g < G - 1) {
+            // partial g of the reduced axis, fp32, at its place in slot g
             b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(g) * M * ldpart + br.s * ldpart + bc.s);
             b.ldc = ldpart;
             b.out_mode = axonn::kOutF32;
+            b.phase = 0;
+          } else if (partials) {
+            // the last partial sums slots 0..G-2 and itself into the output
+            b.C = v.C + celt * (br.s * ldc + bc.s);
+            b.ldc = ldc;
+            b.out_mode = user_mode;
+            b.red_count = G - 1;
+            b.red_src = reinterpret_cast<const float*>(ws) + (br.s * ldpart + bc.s);
+            b.red_stride = M * ldpart;
+            b.red_ld = ldpart;
           } else {
             b.C = v.C + celt * (br.s * ldc + bc.s);
             b.ldc = ldc;
@@ -643,41 +672,38 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
       b.A = whole.A + 2 * (v.a_mn ? r0 * v.lda : r0);
       b.B = whole.B + 2 * (v.b_mn ? r0 * v.ldb : r0);
       b.R = r1 > r0 ? r1 - r0 : 0;
-      b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(sidx) * whole.M * ld_split);
-      b.ldc = ld_split;
-      b.out_mode = axonn::kOutF32;
+      if (sidx < ch.split - 1) {
+        b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(sidx) * whole.M * ld_split);
+        b.ldc = ld_split;
+        b.out_mode = axonn::kOutF32;
+        b.phase = 0;
+      } else {
+        b.red_count = ch.split - 1;
+        b.red_src = reinterpret_cast<const float*>(ws);
+        b.red_stride = whole.M * ld_split;
+        b.red_ld = ld_split;
+      }
       plan.blocks.push_back(b);
     }
   }
   plan.config = ch.config;
   plan.group_m = ch.group_m;
   t_last_choice = ch;
-  st = run_blocks(v, plan, *dev, stream);
-  if (st != AXONN_OK) return st;
-
-  if (ch.split > 1) {
-    const int64_t groups = whole.M * ((whole.N + 7) / 8);
-    int64_t nblk = (groups + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(dev->sms) * 8;
-    if (nblk > cap) nblk = cap;
-    axonn::vgrid_reduce_kernel<<<static_cast<int>(nblk), 256, 0, stream>>>(
-        static_cast<const float*>(ws), ch.split, whole.M * ld_split, ld_split,
-        static_cast<int>(whole.M), static_cast<int>(whole.N), whole.C, whole.ldc, whole.out_mode);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "split reduction launch: %s", cudaGetErrorString(e));
+  // Products whose epilogue sums earlier partials run in a second launch,
+  // after every partial they read has been written by the first.
+  LaunchPlan first = plan, last = plan;
+  first.blocks.clear();
+  last.blocks.clear();
+  for (const Block& b : plan.blocks) (b.phase == 0 ? first : last).blocks.push_back(b);
+  if (!first.blocks.empty()) {
+    st = run_blocks(v, first, *dev, stream);
+    if (st != AXONN_OK) return st;
+  }
+  if (!last.blocks.empty()) {
+    st = run_blocks(v, last, *dev, stream);
+    if (st != AXONN_OK) return st;
   }
 
-  if (partials) {
-    const int64_t groups = M * ((N + 7) / 8);
-    int64_t nblk = (groups + 255) / 256;
-    const int64_t cap = static_cast<int64_t>(dev->sms) * 8;
-    if (nblk > cap) nblk = cap;
-    axonn::vgrid_reduce_kernel<<<static_cast<int>(nblk), 256, 0, stream>>>(
-        static_cast<const float*>(ws), G, M * ldpart, ldpart, static_cast<int>(M), static_cast<int>(N), C,
-        ldc, user_mode);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "reduction launch: %s", cudaGetErrorString(e));
-  }
   return ok();
 }
 

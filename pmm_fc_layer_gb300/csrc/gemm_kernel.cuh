@@ -1,5 +1,6 @@
-// Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores, plus the
-// fixed-order reduction of 3D-grid partial products.
+// Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores, with an
+// epilogue that can fold in earlier fp32 partial products (the fixed-order
+// reduction of 3D-grid partials and of split reduction ranges).
 //
 //   C[M x N] (op)= A[M x R] . B[R x N]      bf16 in, fp32 accumulate in TMEM
 //
@@ -47,7 +48,10 @@ struct ProblemDesc {
   int32_t a_mn;        // A stored M-contiguous (else R-contiguous)
   int32_t b_mn;        // B stored N-contiguous (else R-contiguous)
   int32_t out_mode;
-  int32_t pad_;
+  int32_t red_count;      // > 0: add red_count fp32 partials before storing
+  const float* red_src;   // partial 0 of this problem's output, element (0,0)
+  int64_t red_stride;     // elements between consecutive partials
+  int64_t red_ld;         // row stride of a partial, elements
 };
 
 template <int MAXP>
@@ -132,10 +136,44 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint32_t lo_bits, uint32_t hi_bi
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// Sum, in order, the fp32 partials 0..red_count-1 of 32 columns of one row
+// and then this problem's own accumulator: the fixed-order reduction of the
+// grid's partial products, fused into the epilogue of the last one.
+__device__ __forceinline__ void add_partials(const ProblemDesc& d, int row, int col0, int ncols,
+                                             uint32_t (&r)[32]) {
+  float s[32];
+  const float* src = d.red_src + row * d.red_ld + col0;
+  if (ncols == 32) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 a = reinterpret_cast<const float4*>(src)[v];
+      s[4 * v] = a.x; s[4 * v + 1] = a.y; s[4 * v + 2] = a.z; s[4 * v + 3] = a.w;
+    }
+    for (int g = 1; g < d.red_count; ++g) {
+      const float* pg = src + g * d.red_stride;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 a = reinterpret_cast<const float4*>(pg)[v];
+        s[4 * v] += a.x; s[4 * v + 1] += a.y; s[4 * v + 2] += a.z; s[4 * v + 3] += a.w;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) s[j] = j < ncols ? src[j] : 0.0f;
+    for (int g = 1; g < d.red_count; ++g)
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) s[j] += src[g * d.red_stride + j];
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(s[j] + __uint_as_float(r[j]));
+}
+
 // Writes 32 accumulator columns [col0, col0+32) of one output row.
 __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int col0,
-                                            const uint32_t (&r)[32]) {
+                                            uint32_t (&r)[32]) {
   const int ncols = min(32, d.N - col0);
+  if (d.red_count > 0) add_partials(d, row, col0, ncols, r);
   if (d.out_mode == kOutBF16) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + col0;
     uint32_t pk[16];
@@ -177,16 +215,14 @@ __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int c
   }
 }
 
-// Row of zeros for a problem with an empty reduction range.
+// Row of a tile whose reduction range is empty: the product is zero (plus
+// any partials to add).
 __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, int n0, int BN) {
-  if (d.out_mode == kOutF32Accum) return;
-  const int n1 = min(d.N, n0 + BN);
-  if (d.out_mode == kOutBF16) {
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc;
-    for (int c = n0; c < n1; ++c) out[c] = __float2bfloat16_rn(0.0f);
-  } else {
-    float* out = reinterpret_cast<float*>(d.C) + row * d.ldc;
-    for (int c = n0; c < n1; ++c) out[c] = 0.0f;
+  for (int col0 = n0; col0 < min(d.N, n0 + BN); col0 += 32) {
+    uint32_t r[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) r[j] = 0u;
+    store_chunk(d, row, col0, r);
   }
 }
 
@@ -408,65 +444,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);
-  }
-}
-
-// -------------------------------------------------------------------------
-// Partial-sum reduction of the virtual grid: out = sum_{g=0..G-1} P[g] in
-// fp32, fixed order, then one bf16 RNE (or fp32 add into out).  Each thread
-// owns 8 consecutive columns of one row; grid-stride over all such groups.
-// -------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) vgrid_reduce_kernel(const float* __restrict__ part,
-                                                           int G, int64_t part_stride,
-                                                           int64_t ldp, int M, int N,
-                                                           void* out, int64_t ldo,
-                                                           int out_mode) {
-  const int groups_per_row = (N + 7) / 8;
-  const int64_t total = static_cast<int64_t>(M) * groups_per_row;
-  for (int64_t gidx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; gidx < total;
-       gidx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int row = static_cast<int>(gidx / groups_per_row);
-    const int col0 = static_cast<int>(gidx % groups_per_row) * 8;
-    const int ncols = min(8, N - col0);
-    float s[8];
-    const float* src = part + row * ldp + col0;
-    if (ncols == 8) {
-      float4 a = reinterpret_cast<const float4*>(src)[0];
-      float4 b = reinterpret_cast<const float4*>(src)[1];
-      s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
-      s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
-      for (int g = 1; g < G; ++g) {
-        const float* pg = src + g * part_stride;
-        a = reinterpret_cast<const float4*>(pg)[0];
-        b = reinterpret_cast<const float4*>(pg)[1];
-        s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
-        s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) s[j] = j < ncols ? src[j] : 0.0f;
-      for (int g = 1; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j < ncols) s[j] += src[g * part_stride + j];
-    }
-    if (out_mode == kOutBF16) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row * ldo + col0;
-      if (ncols == 8) {
-        uint4 v;
-        v.x = pack_bf16x2(__float_as_uint(s[0]), __float_as_uint(s[1]));
-        v.y = pack_bf16x2(__float_as_uint(s[2]), __float_as_uint(s[3]));
-        v.z = pack_bf16x2(__float_as_uint(s[4]), __float_as_uint(s[5]));
-        v.w = pack_bf16x2(__float_as_uint(s[6]), __float_as_uint(s[7]));
-        *reinterpret_cast<uint4*>(o) = v;
-      } else {
-        for (int j = 0; j < ncols; ++j) o[j] = __float2bfloat16_rn(s[j]);
-      }
-    } else {
-      float* o = reinterpret_cast<float*>(out) + row * ldo + col0;
-      const bool acc = out_mode == kOutF32Accum;
-      for (int j = 0; j < ncols; ++j) o[j] = s[j] + (acc ? o[j] : 0.0f);
-    }
   }
 }
 
