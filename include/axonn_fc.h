@@ -218,6 +218,8 @@ void axonn_debug_set_inject(int mode);
  *   1  1cta_128x256      one CTA per 128x256 output tile, 64-deep stages
  *   2  pair_256x256      a CTA pair (cluster of 2, cta_group::2 MMA) per
  *                        256x256 output tile, 64-deep stages
+ *   3  1cta_256x256      one CTA per 256x256 output tile (two M=128 MMAs
+ *                        per B slice), 3 stages, single-buffered TMEM
  * axonn_set_kernel_config(c) forces configuration c for all later calls in
  * the process (-1 restores automatic choice); AXONN_ERR_INVALID_ARG if c is
  * out of range.  axonn_last_kernel_config() is the configuration the last

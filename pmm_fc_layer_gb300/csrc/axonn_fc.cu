@@ -74,11 +74,11 @@ constexpr int kPairStages = 6;
 std::mutex g_dev_mu;
 std::vector<DeviceState> g_devs;
 
-template <int BN, int BK, int STAGES, int MAXP>
+template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP>,
+  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              axonn::SmemLayout<BN, BK, STAGES>::kBytes);
+                              axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes);
 }
 
 template <int STAGES, int MAXP>
@@ -124,6 +124,8 @@ axonn_status_t device_state(DeviceState** out) {
                         set_smem_attr<128, 64, 6, kMaxProblems>(),
                         set_smem_attr<256, 64, 4, 1>(), set_smem_attr<256, 64, 4, 8>(),
                         set_smem_attr<256, 64, 4, kMaxProblems>(),
+                        set_smem_attr<256, 64, 3, 1, 2>(), set_smem_attr<256, 64, 3, 8, 2>(),
+                        set_smem_attr<256, 64, 3, kMaxProblems, 2>(),
                         set_pair_smem_attr<kPairStages, 1>(), set_pair_smem_attr<kPairStages, 8>(),
                         set_pair_smem_attr<kPairStages, kMaxProblems>()};
     for (cudaError_t x : es)
@@ -291,15 +293,17 @@ struct KernelConfig {
   int bm, bn;   // output tile of one CTA (or CTA pair)
   int bk;       // reduction depth of one pipeline stage
   bool pair;    // cta_group::2 across a cluster of 2
+  int mma_m;    // rows of one tcgen05.mma
 };
 constexpr KernelConfig kConfigs[] = {
-    {"1cta_128x128", 128, 128, 64, false},
-    {"1cta_128x256", 128, 256, 64, false},
-    {"pair_256x256", 256, 256, 64, true},
+    {"1cta_128x128", 128, 128, 64, false, 128},
+    {"1cta_128x256", 128, 256, 64, false, 128},
+    {"pair_256x256", 256, 256, 64, true, 256},
+    {"1cta_256x256", 256, 256, 64, false, 128},
 };
 // Throughput of each configuration relative to 1cta_128x256 on full waves
 // (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
-constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92};
+constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06};
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
 std::atomic<int> g_forced_config{-1};
 thread_local int t_last_config = -1;
@@ -354,7 +358,7 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.num_k = static_cast<int32_t>((b.R + c.bk - 1) / c.bk);
     d.a_mn = v.a_mn;
     d.b_mn = v.b_mn;
-    d.idesc = make_idesc(c.bm, c.bn, v.a_mn, v.b_mn);
+    d.idesc = make_idesc(c.mma_m, c.bn, v.a_mn, v.b_mn);
     d.out_mode = b.out_mode;
     d.red_count = b.red_count;
     d.red_src = b.red_src;
@@ -381,15 +385,15 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
   return AXONN_OK;
 }
 
-template <int BN, int BK, int STAGES, int MAXP>
+template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
 axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
                              cudaStream_t stream) {
   GemmParams<MAXP> P;
   axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int grid = P.total_tiles < dev.sms ? P.total_tiles : dev.sms;
-  axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP>
-      <<<grid, axonn::kThreads, axonn::SmemLayout<BN, BK, STAGES>::kBytes, stream>>>(P);
+  axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>
+      <<<grid, axonn::cta_threads<MH>(), axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes, stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return AXONN_OK;
@@ -420,6 +424,7 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
   switch (config) {
     case 0: return launch_single<128, 64, 6, P1>(v, plan, dev, stream);
     case 1: return launch_single<256, 64, 4, P1>(v, plan, dev, stream);
+    case 3: return launch_single<256, 64, 3, P1, 2>(v, plan, dev, stream);
     default: return launch_pair<kPairStages, P1>(v, plan, dev, stream);
   }
 }

@@ -29,10 +29,14 @@
 
 namespace axonn {
 
-constexpr int kBM = 128;       // rows per tile (UMMA M, one CTA)
+constexpr int kBM = 128;       // rows of one UMMA (cta_group::1)
 constexpr int kBK = 64;        // reduction depth per stage of the CTA-pair kernel
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 192;  // 6 warps: producer, MMA issuer, 4 epilogue
 constexpr int kEpiWarps = 4;
+
+// A CTA may own MH row halves of 128 (an MH*128 x BN tile): 2 + 4*MH warps.
+template <int MH>
+constexpr int cta_threads() { return 64 + 128 * MH; }
 
 // Output modes of the epilogue.
 enum OutMode : int32_t { kOutBF16 = 0, kOutF32 = 1, kOutF32Accum = 2 };
@@ -226,9 +230,10 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
   }
 }
 
-template <int BN, int BK, int STAGES>
+template <int BN, int BK, int STAGES, int MH = 1>
 struct SmemLayout {
-  static constexpr int kABytes = kBM * BK * 2;
+  static constexpr int kAHalfBytes = kBM * BK * 2;
+  static constexpr int kABytes = MH * kAHalfBytes;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
@@ -248,13 +253,23 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk, bool mn_
   return sdesc_sw64(tile + kk * 32, 16, 512);
 }
 
-template <int BN, int BK, int STAGES, int MAXP>
-__global__ void __launch_bounds__(kThreads, 1)
+// MH = 1: 128 x BN tiles, accumulator double-buffered in TMEM (2 x BN
+// columns), so the epilogue of a tile overlaps the next mainloop.
+// MH = 2: 256 x BN tiles as two M = 128 MMAs sharing each B slice (a third
+// fewer operand bytes per FLOP); the two accumulators fill TMEM (2 x BN
+// columns, single-buffered) and 8 epilogue warps drain them.
+template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
+__global__ void __launch_bounds__(cta_threads<MH>(), 1)
     fc_gemm_tcgen05_kernel(const __grid_constant__ GemmParams<MAXP> P) {
-  using L = SmemLayout<BN, BK, STAGES>;
+  using L = SmemLayout<BN, BK, STAGES, MH>;
   static_assert(BK == 64 || BK == 32, "stage depth");
-  constexpr uint32_t kTmemCols = 2 * BN;
+  static_assert(MH == 1 || MH == 2, "row halves per CTA");
+  constexpr int kAccBufs = MH == 1 ? 2 : 1;
+  constexpr uint32_t kAccCols = MH * BN;  // TMEM columns of one accumulator
+  constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
+  constexpr int kTileM = MH * kBM;
   static_assert(BN == 128 || BN == 256, "UMMA N");
+  static_assert(kTmemCols <= 512, "TMEM columns");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -283,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiWarps);
+      mbar_init(tempty_bar(b), kEpiWarps * MH);
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -317,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ProblemDesc& d = P.prob[tc.p];
         const CUtensorMap* ma = &P.tma[tc.p];
         const CUtensorMap* mb = &P.tmb[tc.p];
-        const int m0 = tc.m_blk * kBM;
+        const int m0 = tc.m_blk * kTileM;
         const int n0 = tc.n_blk * BN;
         for (int k = 0; k < d.num_k; ++k) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
@@ -327,12 +342,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, L::kStageBytes);
           const int r0 = k * BK;
-          if (d.a_mn) {
 #pragma unroll
-            for (int h = 0; h < kBM / 64; ++h)
-              tma_load_2d(a_tile(stage) + h * (BK * 128), ma, fb, m0 + 64 * h, r0);
-          } else {
-            tma_load_2d(a_tile(stage), ma, fb, r0, m0);
+          for (int hh = 0; hh < MH; ++hh) {
+            const uint32_t at = a_tile(stage) + hh * L::kAHalfBytes;
+            if (d.a_mn) {
+#pragma unroll
+              for (int h = 0; h < kBM / 64; ++h)
+                tma_load_2d(at + h * (BK * 128), ma, fb, m0 + kBM * hh + 64 * h, r0);
+            } else {
+              tma_load_2d(at, ma, fb, r0, m0 + kBM * hh);
+            }
           }
           if (d.b_mn) {
 #pragma unroll
@@ -368,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
         if (d.num_k == 0) continue;
-        const uint32_t b = acc & 1u;
-        const uint32_t acc_phase = (acc >> 1) & 1u;
+        const uint32_t b = acc % kAccBufs;
+        const uint32_t acc_phase = (acc / kAccBufs) & 1u;
         if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * BN;
+        const uint32_t d_tmem = tmem_base + b * kAccCols;
         for (int k = 0; k < d.num_k; ++k) {
           if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
             ok = false;
@@ -383,9 +402,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t sb = b_tile(stage);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = operand_desc<BK>(sa, kk, d.a_mn);
             const uint64_t bd = operand_desc<BK>(sb, kk, d.b_mn);
-            umma_bf16(d_tmem, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int hh = 0; hh < MH; ++hh) {
+              const uint64_t ad = operand_desc<BK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
+              umma_bf16(d_tmem + hh * BN, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit(empty_bar(stage));
           if (++stage == STAGES) {
@@ -403,25 +425,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int hh = (warp - 2) >> 2;  // row half (accumulator) it drains
     uint32_t acc = 0;
     for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile(P, t);
       const ProblemDesc& d = P.prob[tc.p];
-      const int row = tc.m_blk * kBM + q * 32 + lane;
+      const int row = tc.m_blk * kTileM + hh * kBM + q * 32 + lane;
       const int n0 = tc.n_blk * BN;
       if (d.num_k == 0) {
         if (row < d.M) store_zero_row(d, row, n0, BN);
         continue;
       }
-      const uint32_t b = acc & 1u;
-      const uint32_t acc_phase = (acc >> 1) & 1u;
+      const uint32_t b = acc % kAccBufs;
+      const uint32_t acc_phase = (acc / kAccBufs) & 1u;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull_bar(b), acc_phase, tmo, abort_flag, kSiteEpiTmemFull);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * BN;
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * BN;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col0 = n0 + c * 32;
