@@ -220,6 +220,10 @@ void axonn_debug_set_inject(int mode);
  *                        256x256 output tile, 64-deep stages
  *   3  1cta_256x256      one CTA per 256x256 output tile (two M=128 MMAs
  *                        per B slice), 3 stages, single-buffered TMEM
+ *   4  1cta_128x192      one CTA per 128x192 output tile, 5 stages
+ *   5  1cta_256x192      one CTA per 256x192 output tile, 4 stages
+ * (the N=192 tiles trade a little operand reuse for fewer idle SMs in the
+ * last wave on shapes such as 8192 x 6144) 
  * axonn_set_kernel_config(c) forces configuration c for all later calls in
  * the process (-1 restores automatic choice); AXONN_ERR_INVALID_ARG if c is
  * out of range.  axonn_last_kernel_config() is the configuration the last

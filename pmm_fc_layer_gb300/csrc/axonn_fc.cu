@@ -126,6 +126,10 @@ axonn_status_t device_state(DeviceState** out) {
                         set_smem_attr<256, 64, 4, kMaxProblems>(),
                         set_smem_attr<256, 64, 3, 1, 2>(), set_smem_attr<256, 64, 3, 8, 2>(),
                         set_smem_attr<256, 64, 3, kMaxProblems, 2>(),
+                        set_smem_attr<192, 64, 5, 1>(), set_smem_attr<192, 64, 5, 8>(),
+                        set_smem_attr<192, 64, 5, kMaxProblems>(),
+                        set_smem_attr<192, 64, 4, 1, 2>(), set_smem_attr<192, 64, 4, 8, 2>(),
+                        set_smem_attr<192, 64, 4, kMaxProblems, 2>(),
                         set_pair_smem_attr<kPairStages, 1>(), set_pair_smem_attr<kPairStages, 8>(),
                         set_pair_smem_attr<kPairStages, kMaxProblems>()};
     for (cudaError_t x : es)
@@ -300,10 +304,12 @@ constexpr KernelConfig kConfigs[] = {
     {"1cta_128x256", 128, 256, 64, false, 128},
     {"pair_256x256", 256, 256, 64, true, 256},
     {"1cta_256x256", 256, 256, 64, false, 128},
+    {"1cta_128x192", 128, 192, 64, false, 128},
+    {"1cta_256x192", 256, 192, 64, false, 128},
 };
 // Throughput of each configuration relative to 1cta_128x256 on full waves
 // (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
-constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06};
+constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12};
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
 std::atomic<int> g_forced_config{-1};
 thread_local int t_last_config = -1;
@@ -425,6 +431,8 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
     case 0: return launch_single<128, 64, 6, P1>(v, plan, dev, stream);
     case 1: return launch_single<256, 64, 4, P1>(v, plan, dev, stream);
     case 3: return launch_single<256, 64, 3, P1, 2>(v, plan, dev, stream);
+    case 4: return launch_single<192, 64, 5, P1>(v, plan, dev, stream);
+    case 5: return launch_single<192, 64, 4, P1, 2>(v, plan, dev, stream);
     default: return launch_pair<kPairStages, P1>(v, plan, dev, stream);
   }
 }

@@ -265,11 +265,15 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   static_assert(BK == 64 || BK == 32, "stage depth");
   static_assert(MH == 1 || MH == 2, "row halves per CTA");
   constexpr int kAccBufs = MH == 1 ? 2 : 1;
-  constexpr uint32_t kAccCols = MH * BN;  // TMEM columns of one accumulator
-  constexpr uint32_t kTmemCols = kAccBufs * kAccCols;
+  // Each row half's accumulator starts on a 128-column boundary of TMEM
+  // (a 192-wide one takes 256 columns); TMEM is allocated in powers of two.
+  constexpr uint32_t kHalfCols = BN <= 128 ? 128 : 256;
+  constexpr uint32_t kAccCols = MH * kHalfCols;  // TMEM columns of one accumulator
+  constexpr uint32_t kTmemUsed = kAccBufs * kAccCols;
+  constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
   constexpr int kTileM = MH * kBM;
-  static_assert(BN == 128 || BN == 256, "UMMA N");
-  static_assert(kTmemCols <= 512, "TMEM columns");
+  static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "UMMA N: 128, 192 or 256");
+  static_assert(kTmemUsed <= 512, "TMEM columns");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -406,7 +410,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
 #pragma unroll
             for (int hh = 0; hh < MH; ++hh) {
               const uint64_t ad = operand_desc<BK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
-              umma_bf16(d_tmem + hh * BN, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem + hh * kHalfCols, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
             }
           }
           umma_commit(empty_bar(stage));
@@ -445,7 +449,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t t_row =
-          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * BN;
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         const int col0 = n0 + c * 32;
