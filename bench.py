@@ -339,11 +339,15 @@ def run_ours(args):
 
     # Per-shape tuning (outside every timed region): each GEMM's candidate
     # configurations are timed once and the fastest is kept by the library.
-    if not args.no_tune:
+    if args.tune_cache and os.path.exists(args.tune_cache):
+        fc.axonn_tune_cache_load(args.tune_cache)
+    elif not args.no_tune:
         with torch.cuda.stream(stream):
             for g in plan:
                 fc.axonn_fc_tune(g["op"], g["P"], g["Q"], g["C"], g["shape"], flags, ws,
                                  stream=stream)
+        if args.tune_cache:
+            fc.axonn_tune_cache_save(args.tune_cache)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -528,6 +532,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-tune", action="store_true",
                     help="skip the per-shape tuning before the warm-up (use default choices)")
+    ap.add_argument("--tune-cache", default=None, metavar="PATH",
+                    help="load tuned choices from PATH if it exists (no tuning), else tune "
+                         "and save them there")
     ap.add_argument("--only", default=None, metavar="LAYER:OP",
                     help="time one GEMM (e.g. out:fwd) for profiling; not a bench line")
     args = ap.parse_args()
