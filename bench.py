@@ -82,6 +82,22 @@ WORKLOADS = {
         batch=None, seq=None, seed=1005, scale=0.05, device_inputs=True),
 }
 DEFAULT_WORKLOAD = "gpt_h6144_t8192"
+
+# DRAM traffic of the GEMM kernel from one ncu capture of the default
+# workload (dram__bytes_read.sum + dram__bytes_write.sum over the 12 launches
+# of one tuned step; summary and command in profiles/).  It is reported only
+# while the kernel sources hash to the value the capture was taken with.
+TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "6bfd19f727a71498",
+           "bytes_per_step": (17914.5 + 2368.0) * 1e6, "launches_per_step": 12}
+
+
+def kernel_sources_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "pmm_fc_layer_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 DATA = ("synthetic, seeded: SplitMix64 + Box-Muller bf16; activations/grads N(0,1), "
         "weights N(0,0.02)")
 
@@ -270,6 +286,18 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(value, device):
+    """The largest `value` over all ranks of the default process group (the
+    slowest rank's time); `value` itself when there is no group."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------------ GPU arm
 def run_ours(args):
     import torch
@@ -375,11 +403,7 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
     fc.axonn_sync_status(stream)
-    elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_ev), dev)
     split_reduces = sum(1 for u in used if u and u[1] > 1)
     launches = args.steps * (len(plan) + reduce_launches + split_reduces)
 
@@ -471,12 +495,8 @@ def run_ours(args):
         h2d_stream.wait_stream(stream)
         t1.record(h2d_stream)
         torch.cuda.synchronize()
-        e2e_ms = t0.elapsed_time(t1)
         fc.axonn_sync_status(stream)
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(t0.elapsed_time(t1), dev)
 
     if rank == 0:
         line = {
@@ -496,7 +516,12 @@ def run_ours(args):
                          "peak_source": f"{peaks['source']} (sustained; burst {peaks['burst']})",
                          "kernel": "fc_gemm_tcgen05_kernel" + (
                              " (+ vgrid_reduce_kernel inside each timed call)" if flags else ""),
-                         "traffic": None},
+                         "traffic": (TRAFFIC["bytes_per_step"] / TRAFFIC["launches_per_step"]
+                                     if args.workload == TRAFFIC["workload"] and only is None
+                                     and kernel_sources_hash() == TRAFFIC["kernel_sources"]
+                                     else None),
+                         "traffic_unit": "bytes per launch (mean over the step)",
+                         "algorithmic_bytes": round(sum(g["bytes"] for g in plan) / len(plan))},
             "e2e": ({"value": round(world * flops_per_step * e2e_steps / (e2e_ms * 1e9), 2),
                      "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
                      "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps,
