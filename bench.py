@@ -259,10 +259,11 @@ def config_block(wl, name, world):
         cfg.update(global_batch=wl["batch"] * world, seq_len=wl["seq"])
     cfg["grid"] = "x".join(str(g) for g in wl.get("grid", (1, 1, 1)))
     cfg["parallelism"] = f"replicas x{world}" if world > 1 else "single GPU"
-    big = any(2 * (T * K + K * N + T * N) > (129 << 20) for _, T, K, N in wl["layers"])
+    big = [2 * (T * K + K * N + T * N) > (129 << 20) for _, T, K, N in wl["layers"]]
     cfg["l2"] = ("L2 flushed between timed steps (512 MB write)" if wl.get("flush")
-                 else "operands exceed the 129 MB L2; no flush" if big
-                 else "operands L2-resident (warm), by design of this workload")
+                 else "operands exceed the 129 MB L2; no flush" if all(big)
+                 else "operands L2-resident (warm), by design of this workload" if not any(big)
+                 else "mixed: the larger shapes exceed L2, the smallest can stay resident")
     return cfg
 
 
