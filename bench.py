@@ -605,13 +605,99 @@ def run_ours(args):
     return 0
 
 
+def run_zsharded(args):
+    """Z-sharded weights of the 2x2x2 grid on the GPT block (H=6144,
+    T=8192): for every layer and weight block (x, y), the all-gather of its
+    two row shards and the Z-group weight gradient written as
+    reduce-scattered shards.  Reports the gather's HBM rate against the HBM
+    peak (algorithmic bytes: each block read once and written once) and the
+    sharded weight gradient's TFLOP/s."""
+    import torch
+    import pmm_fc_layer_gb300 as fc
+    from pmm_fc_layer_gb300 import build as _b
+    torch.cuda.set_device(0)
+    _b.build()
+    fc.load()
+    dev = torch.device("cuda", 0)
+    grid = (2, 2, 2)
+    layers = _gpt(6144, 8192, 4 * 6144)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1006)
+    stream = torch.cuda.Stream(device=dev)
+    jobs, gather_bytes, wgrad_flops, ws_need = [], 0.0, 0.0, 0
+    for name, T, K, N in layers:
+        X = torch.randn((T, K), generator=g, device=dev).to(torch.bfloat16)
+        dY = torch.randn((T, N), generator=g, device=dev).to(torch.bfloat16)
+        for x in range(grid[0]):
+            for y in range(grid[1]):
+                shape = fc.Shape(T, K, N, grid, (x, y, 0))
+                k0, k1 = fc.axonn_block_range(K, grid[0], x)
+                n0, n1 = fc.axonn_block_range(N, grid[1], y)
+                rows, cols = k1 - k0, n1 - n0
+                cuts = [fc.axonn_block_range(rows, grid[2], z) for z in range(grid[2])]
+                W_sh = [(0.02 * torch.randn((b - a, cols), generator=g, device=dev)).to(torch.bfloat16)
+                        for a, b in cuts]
+                W_blk = torch.empty((rows, cols), dtype=torch.bfloat16, device=dev)
+                dW_sh = [torch.empty((b - a, cols), dtype=torch.bfloat16, device=dev) for a, b in cuts]
+                ws_need = max(ws_need, fc.axonn_fc_workspace_size("wgrad", shape, fc.ZSHARDED))
+                jobs.append((X, dY, W_sh, W_blk, dW_sh, shape, rows, cols))
+                gather_bytes += 2.0 * 2 * rows * cols
+                wgrad_flops += 2.0 * rows * cols * T
+    ws = torch.empty(ws_need, dtype=torch.uint8, device=dev)
+
+    def gathers():
+        for X, dY, W_sh, W_blk, dW_sh, shape, rows, cols in jobs:
+            fc.axonn_shards_gather(W_sh, W_blk, rows, cols, stream=stream)
+
+    def wgrads():
+        for X, dY, W_sh, W_blk, dW_sh, shape, rows, cols in jobs:
+            fc.axonn_fc_wgrad_zsharded(X, dY, dW_sh, shape, 0, ws, stream=stream)
+
+    times = {}
+    with torch.cuda.stream(stream):
+        for label, fn in (("gather", gathers), ("wgrad", wgrads)):
+            for _ in range(args.warmup):
+                fn()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                fn()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            gr.replay()
+            e0.record(stream)
+            for _ in range(args.steps):
+                gr.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            times[label] = e0.elapsed_time(e1) / args.steps
+    fc.axonn_sync_status(stream)
+    peaks = read_peaks()
+    gbs = gather_bytes / times["gather"] / 1e6
+    tf = wgrad_flops / times["wgrad"] / 1e9
+    print(json.dumps({
+        "metric": "Z-sharded weights on a 2x2x2 grid: shard all-gather GB/s and sharded "
+                  "weight-gradient TFLOP/s", "value": round(tf, 2), "unit": UNIT,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+        "dtype": "bf16", "data": "synthetic, seeded (torch generator on the device)",
+        "config": {"workload": "zsharded_h6144_2x2x2: GPT block H=6144, T=8192, grid 2x2x2; "
+                               "all four layers x four weight blocks (x, y)"},
+        "gather": {"ms_per_step": round(times["gather"], 4), "gbs": round(gbs, 1),
+                   "algorithmic_bytes_per_step": gather_bytes, "bound": "hbm",
+                   "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                   "peak_source": peaks["source"]},
+        "wgrad_zsharded": {"ms_per_step": round(times["wgrad"], 4), "tflops": round(tf, 1),
+                           "frac_of_sustained": round(tf / peaks["sustained"], 4)},
+        "timing": "CUDA-graph replays"}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["zsharded_h6144_2x2x2"],
+                    default=DEFAULT_WORKLOAD)
     ap.add_argument("--config", type=int, default=-1,
                     help="force one kernel configuration (-1: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true",
@@ -631,6 +717,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "zsharded_h6144_2x2x2":
+        return run_zsharded(args)
     return run_ours(args)
 
 

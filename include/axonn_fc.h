@@ -90,6 +90,7 @@ typedef struct {
 #define AXONN_VGRID 0x8u          /* all blocks + on-device partial sum */
 #define AXONN_FULL_OPERANDS 0x10u /* block mode: pointers are full matrices */
 #define AXONN_OUT_F32 0x20u       /* output is fp32, overwritten */
+#define AXONN_ZSHARDED 0x40u      /* axonn_fc_workspace_size of axonn_fc_wgrad_zsharded */
 
 /*
  * Forward product Y = X . W of the layer, of block (x,y,z), or of the whole
@@ -124,6 +125,41 @@ axonn_status_t axonn_fc_dgrad(const void* dY, const void* W, void* dX, int64_t l
 axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t ldx,
                               int64_t lddy, int64_t lddw, const axonn_fc_shape_t* shape,
                               uint32_t flags, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Z-sharded weights of the 3D grid.  Each rank (x, y, z) keeps only shard z
+ * of its weight block W_{x,y}; the grid all-gathers the block over the Z
+ * group before using it and reduce-scatters the weight-gradient partials
+ * over the Z group into shards ("the weight matrix sharded along the Z axis
+ * ... all-gather, reduce-scatter, and all-reduce collectives moving data" --
+ * "What carries the argument", review of arXiv 2502.08145).  Shards are row
+ * blocks of W_{x,y} cut by the grid's split rule (units of 8 rows, leading
+ * shards take the extra unit; see axonn_block_range).
+ *
+ * axonn_shards_gather -- the all-gather, on one GPU: copies g bf16 row
+ * shards, shard z = rows [split(rows, g, z)) stored row-major with leading
+ * dimension ld_shard at shards[z] (a HOST array of g DEVICE pointers), into
+ * `out` [rows x cols] (leading dimension ld_out).  cols, ld_shard and ld_out
+ * must be multiples of 8 and every pointer 16-byte aligned
+ * (AXONN_ERR_ALIGNMENT); 1 <= g <= 64.
+ *
+ * axonn_fc_wgrad_zsharded -- the Z-group weight gradient with its
+ * reduce-scatter, on one GPU: for block (shape->x, shape->y) it computes
+ * every partial dW^(z)_{x,y} = X[Tz,Kx]^T . dY[Tz,Ny], z = 0..G_z-1, sums
+ * them in fixed order z = 0..G_z-1 and writes row shard z' of the sum to
+ * dW_shards[z'] (a HOST array of G_z DEVICE pointers; each [rows of shard z'
+ * x Ny], leading dimension ld_shard; bf16, or fp32 with AXONN_OUT_F32 /
+ * AXONN_ACCUM_F32).  X and dY are the full [T x K] and [T x N] matrices (or
+ * transposed with AXONN_A_T / AXONN_B_T); shape->z is ignored.  Partials
+ * 0..G_z-2 go to `ws`: axonn_fc_workspace_size(AXONN_OP_WGRAD, shape,
+ * AXONN_ZSHARDED) bytes.
+ */
+axonn_status_t axonn_shards_gather(const void* const* shards, int32_t g, int64_t rows, int64_t cols,
+                                   int64_t ld_shard, void* out, int64_t ld_out, cudaStream_t stream);
+axonn_status_t axonn_fc_wgrad_zsharded(const void* X, const void* dY, void* const* dW_shards,
+                                       int64_t ldx, int64_t lddy, int64_t ld_shard,
+                                       const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream);
 
 /*
  * Virtual-grid product (as the entry points above with AXONN_VGRID) that

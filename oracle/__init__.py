@@ -289,6 +289,35 @@ def fc_vgrid(op, P, Q, p_t, q_t, T, K, N, grid):
 
 
 # --------------------------------------------------------------------------
+# Z-sharded weights: all-gather and reduce-scatter over the Z group
+# --------------------------------------------------------------------------
+def shard_rows(Wblk: np.ndarray, G: int):
+    """Row shards of a weight block: shard z = rows split_range(rows, G, z)."""
+    return [Wblk[slice(*split_range(Wblk.shape[0], G, z))] for z in range(G)]
+
+
+def gather_shards(shards):
+    """The all-gather over the Z group: the shards stacked back in order."""
+    return np.concatenate(list(shards), axis=0)
+
+
+def wgrad_zsharded(X, dY, x_t, dy_t, T, K, N, grid, xy):
+    """Weight gradient of block (x, y): the Z-group partials dW^(z)_{x,y} summed
+    in order z = 0..Gz-1 (fp64), then cut into the Gz row shards that the
+    reduce-scatter leaves on the ranks -> (list of C shards, list of S shards)."""
+    gx, gy, gz = grid
+    x, y = xy
+    Kx, Ny = split_range(K, gx, x), split_range(N, gy, y)
+    C = np.zeros((Kx[1] - Kx[0], Ny[1] - Ny[0]))
+    S = np.zeros_like(C)
+    for z in range(gz):
+        Cb, Sb, _, _ = fc_block("wgrad", X, dY, x_t, dy_t, T, K, N, grid, (x, y, z))
+        C += Cb
+        S += Sb
+    return shard_rows(C, gz), shard_rows(S, gz)
+
+
+# --------------------------------------------------------------------------
 # acceptance bound
 # --------------------------------------------------------------------------
 def error_ratio(c_test: np.ndarray, C: np.ndarray, S: np.ndarray,

@@ -22,11 +22,13 @@ ACCUM_F32 = 0x4
 VGRID = 0x8
 FULL_OPERANDS = 0x10
 OUT_F32 = 0x20
+ZSHARDED = 0x40
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]
 
 EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_static",
+           "axonn_shards_gather", "axonn_fc_wgrad_zsharded",
            "axonn_fc_workspace_size", "axonn_fc_tune", "axonn_tune_cache_save",
            "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
            "axonn_last_choice",
@@ -78,6 +80,11 @@ def load(path: str | None = None):
             f = getattr(lib, name)
             f.argtypes = sig
             f.restype = ctypes.c_int
+        lib.axonn_shards_gather.argtypes = [ctypes.POINTER(vp), i32, i64, i64, i64, vp, i64, vp]
+        lib.axonn_shards_gather.restype = ctypes.c_int
+        lib.axonn_fc_wgrad_zsharded.argtypes = [vp, vp, ctypes.POINTER(vp), i64, i64, i64,
+                                                ctypes.POINTER(Shape), u32, vp, sz, vp]
+        lib.axonn_fc_wgrad_zsharded.restype = ctypes.c_int
         lib.axonn_fc_vgrid_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64,
                                               ctypes.POINTER(Shape), u32, vp]
         lib.axonn_fc_vgrid_static.restype = ctypes.c_int
@@ -179,6 +186,35 @@ def axonn_fc_wgrad(X, dY, dW, shape: Shape, flags: int = 0, ws=None, ldx=None, l
                    lddw=None, stream=None):
     """dW = X^T . dY (layer, block or virtual grid)."""
     _call("axonn_fc_wgrad", X, dY, dW, shape, flags, ws, ldx, lddy, lddw, stream)
+
+
+def _ptr_array(ts):
+    arr = (ctypes.c_void_p * len(ts))()
+    for i, t in enumerate(ts):
+        arr[i] = _ptr(t)
+    return arr
+
+
+def axonn_shards_gather(shards, out, rows: int, cols: int, ld_shard=None, ld_out=None,
+                        stream=None):
+    """All-gather of row shards on one GPU: out[rows x cols] <- shards
+    (shard z holds rows split_range(rows, len(shards), z))."""
+    ld_s = ld_shard if ld_shard is not None else next(
+        (_ld(t, None) for t in shards if t is not None and t.numel()), cols)
+    _check(load().axonn_shards_gather(_ptr_array(shards), len(shards), rows, cols, ld_s, _ptr(out),
+                                      _ld(out, ld_out), _stream(stream)))
+
+
+def axonn_fc_wgrad_zsharded(X, dY, dW_shards, shape: Shape, flags: int = 0, ws=None, ldx=None,
+                            lddy=None, ld_shard=None, stream=None):
+    """Weight gradient of block (x, y) summed over the Z group and written as
+    row shards (the grid's reduce-scatter) into dW_shards."""
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    ld_s = ld_shard if ld_shard is not None else next(
+        (_ld(t, None) for t in dW_shards if t is not None and t.numel()), 8)
+    _check(load().axonn_fc_wgrad_zsharded(_ptr(X), _ptr(dY), _ptr_array(dW_shards), _ld(X, ldx),
+                                          _ld(dY, lddy), ld_s, ctypes.byref(shape), flags,
+                                          _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def axonn_fc_vgrid_static(op, P, Q, C, shape: Shape, flags: int = 0, ldp=None, ldq=None,

@@ -202,7 +202,7 @@ void full_dims(int op, const axonn_fc_shape_t& s, int64_t* M, int64_t* N, int64_
 }
 
 constexpr uint32_t kKnownFlags = AXONN_A_T | AXONN_B_T | AXONN_ACCUM_F32 | AXONN_VGRID |
-                                 AXONN_FULL_OPERANDS | AXONN_OUT_F32;
+                                 AXONN_FULL_OPERANDS | AXONN_OUT_F32 | AXONN_ZSHARDED;
 
 axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
   if (op < AXONN_OP_FWD || op > AXONN_OP_WGRAD) return fail(AXONN_ERR_INVALID_ARG, "bad op %d", op);
@@ -511,6 +511,8 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
                      size_t ws_bytes, cudaStream_t stream, const TuneChoice* force = nullptr) {
   axonn_status_t st = check_shape(op, shape, flags);
   if (st != AXONN_OK) return st;
+  if (flags & AXONN_ZSHARDED)
+    return fail(AXONN_ERR_INVALID_ARG, "AXONN_ZSHARDED is for axonn_fc_workspace_size only");
   const axonn_fc_shape_t& s = *shape;
   const bool vgrid = (flags & AXONN_VGRID) != 0;
   const bool single = s.gx * s.gy * s.gz == 1;
@@ -721,6 +723,36 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
 }
 
 // ----------------------------------------------------------------------
+// Z-sharded weights.  Inside the 3D grid the weight block W_{x,y} (and its
+// gradient) is kept as G_z row shards, shard z on rank (x, y, z): an
+// all-gather over the Z group rebuilds the block before it is used and a
+// reduce-scatter over the Z group turns the G_z weight-gradient partials into
+// the shards of their sum.  Row shards follow the grid's split rule (units of
+// 8 rows, leading shards take the extra unit).
+// ----------------------------------------------------------------------
+__global__ void __launch_bounds__(256) copy_rows_kernel(const char* __restrict__ src,
+                                                        int64_t src_ld, char* __restrict__ dst,
+                                                        int64_t dst_ld, int64_t rows,
+                                                        int64_t chunks_per_row) {
+  const int64_t total = rows * chunks_per_row;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / chunks_per_row, c = i - r * chunks_per_row;
+    *reinterpret_cast<uint4*>(dst + r * dst_ld + 16 * c) =
+        *reinterpret_cast<const uint4*>(src + r * src_ld + 16 * c);
+  }
+}
+
+size_t zsharded_ws_bytes(const axonn_fc_shape_t& s) {
+  if (s.gz <= 1) return 0;
+  Range Kx, Ny;
+  split_range(s.K, s.gx, s.x, &Kx.s, &Kx.e);
+  split_range(s.N, s.gy, s.y, &Ny.s, &Ny.e);
+  return static_cast<size_t>(s.gz - 1) * static_cast<size_t>(Kx.len()) *
+         static_cast<size_t>((Ny.len() + 7) / 8 * 8) * 4u;
+}
+
+// ----------------------------------------------------------------------
 // Fixed scratch for callers that cannot allocate device memory.
 //
 // The virtual-grid path needs an fp32 buffer for the partial products of
@@ -799,6 +831,150 @@ axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t l
   return fc_op(AXONN_OP_WGRAD, X, dY, dW, ldx, lddy, lddw, shape, flags, ws, ws_bytes, stream);
 }
 
+axonn_status_t axonn_shards_gather(const void* const* shards, int32_t g, int64_t rows, int64_t cols,
+                                   int64_t ld_shard, void* out, int64_t ld_out, cudaStream_t stream) {
+  if (g < 1 || g > kMaxProblems) return fail(AXONN_ERR_INVALID_ARG, "shard count %d not in [1, %d]", g, kMaxProblems);
+  if (rows < 0 || cols < 0) return fail(AXONN_ERR_INVALID_ARG, "negative extent");
+  if (rows == 0 || cols == 0) return ok();
+  if (!shards || !out) return fail(AXONN_ERR_INVALID_ARG, "NULL shard table or output");
+  if (cols % 8 != 0) return fail(AXONN_ERR_ALIGNMENT, "row length %lld is not a multiple of 8", (long long)cols);
+  if (ld_shard < cols || ld_out < cols) return fail(AXONN_ERR_INVALID_ARG, "leading dimension below row length");
+  if (ld_shard % 8 != 0 || ld_out % 8 != 0 || !aligned16(out))
+    return fail(AXONN_ERR_ALIGNMENT, "leading dimensions must be multiples of 8, pointers 16-byte aligned");
+  for (int z = 0; z < g; ++z) {
+    int64_t s0, s1;
+    split_range(rows, g, z, &s0, &s1);
+    if (s1 > s0 && (!shards[z] || !aligned16(shards[z])))
+      return fail(AXONN_ERR_ALIGNMENT, "shard %d is NULL or not 16-byte aligned", z);
+  }
+  DeviceState* dev = nullptr;
+  axonn_status_t st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+  const int64_t chunks = cols * 2 / 16;
+  for (int z = 0; z < g; ++z) {
+    int64_t s0, s1;
+    split_range(rows, g, z, &s0, &s1);
+    if (s1 <= s0) continue;
+    const int64_t total = (s1 - s0) * chunks;
+    int64_t blocks = (total + 255) / 256;
+    if (blocks > static_cast<int64_t>(dev->sms) * 16) blocks = static_cast<int64_t>(dev->sms) * 16;
+    copy_rows_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(
+        static_cast<const char*>(shards[z]), ld_shard * 2, static_cast<char*>(out) + s0 * ld_out * 2,
+        ld_out * 2, s1 - s0, chunks);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "gather launch: %s", cudaGetErrorString(e));
+  }
+  return ok();
+}
+
+axonn_status_t axonn_fc_wgrad_zsharded(const void* X, const void* dY, void* const* dW_shards,
+                                       int64_t ldx, int64_t lddy, int64_t ld_shard,
+                                       const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
+                                       size_t ws_bytes, cudaStream_t stream) {
+  if (!shape) return fail(AXONN_ERR_INVALID_ARG, "shape is NULL");
+  if (flags & (AXONN_VGRID | AXONN_FULL_OPERANDS | AXONN_ZSHARDED))
+    return fail(AXONN_ERR_INVALID_ARG, "grid-mode flags are implied by this entry point");
+  axonn_fc_shape_t s = *shape;
+  s.z = 0;
+  axonn_status_t st = check_shape(AXONN_OP_WGRAD, &s, flags);
+  if (st != AXONN_OK) return st;
+  const bool out_f32 = (flags & (AXONN_ACCUM_F32 | AXONN_OUT_F32)) != 0;
+  const int user_mode = (flags & AXONN_ACCUM_F32) ? axonn::kOutF32Accum
+                        : (flags & AXONN_OUT_F32) ? axonn::kOutF32
+                                                  : axonn::kOutBF16;
+  // Full operands: X [T x K], dY [T x N] (transposed storage by flags).
+  OpView v;
+  v.A = static_cast<const char*>(X);
+  v.lda = ldx;
+  v.B = static_cast<const char*>(dY);
+  v.ldb = lddy;
+  v.C = nullptr;
+  v.ldc = ld_shard;
+  v.M = s.K; v.N = s.N; v.R = s.T;
+  v.a_mn = !(flags & AXONN_A_T);
+  v.b_mn = !(flags & AXONN_B_T);
+  st = v.a_mn ? check_operand("X", X, ldx, s.T, s.K) : check_operand("X", X, ldx, s.K, s.T);
+  if (st != AXONN_OK) return st;
+  st = v.b_mn ? check_operand("dY", dY, lddy, s.T, s.N) : check_operand("dY", dY, lddy, s.N, s.T);
+  if (st != AXONN_OK) return st;
+  Range Kx, Ny;
+  split_range(s.K, s.gx, s.x, &Kx.s, &Kx.e);
+  split_range(s.N, s.gy, s.y, &Ny.s, &Ny.e);
+  const int64_t Mb = Kx.len(), Nb = Ny.len();
+  if (Mb == 0 || Nb == 0) return ok();
+  if (!dW_shards) return fail(AXONN_ERR_INVALID_ARG, "shard table is NULL");
+  if (ld_shard < Nb) return fail(AXONN_ERR_INVALID_ARG, "shard leading dimension %lld < %lld",
+                                 (long long)ld_shard, (long long)Nb);
+  if (ld_shard % (out_f32 ? 4 : 8) != 0) return fail(AXONN_ERR_ALIGNMENT, "shard leading dimension misaligned");
+  for (int z = 0; z < s.gz; ++z) {
+    int64_t r0, r1;
+    split_range(Mb, s.gz, z, &r0, &r1);
+    if (r1 > r0 && (!dW_shards[z] || !aligned16(dW_shards[z])))
+      return fail(AXONN_ERR_ALIGNMENT, "shard %d is NULL or not 16-byte aligned", z);
+  }
+  const size_t need = zsharded_ws_bytes(s);
+  if (need > 0 && (!ws || ws_bytes < need))
+    return fail(AXONN_ERR_WORKSPACE, "Z-sharded weight gradient needs %zu workspace bytes, got %zu", need,
+                ws_bytes);
+  if (need > 0 && !aligned16(ws)) return fail(AXONN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+
+  auto a_at = [&](int64_t i, int64_t r) { return v.A + 2 * (v.a_mn ? r * v.lda + i : i * v.lda + r); };
+  auto b_at = [&](int64_t r, int64_t j) { return v.B + 2 * (v.b_mn ? r * v.ldb + j : j * v.ldb + r); };
+  const int64_t ldp = (Nb + 7) / 8 * 8;
+  float* part = static_cast<float*>(ws);
+  LaunchPlan first, last;
+  for (int z = 0; z < s.gz; ++z) {
+    Range Tz;
+    split_range(s.T, s.gz, z, &Tz.s, &Tz.e);
+    if (z < s.gz - 1) {  // partial z of the Z group, fp32, into workspace slot z
+      Block b;
+      b.A = a_at(Kx.s, Tz.s);
+      b.B = b_at(Tz.s, Ny.s);
+      b.C = reinterpret_cast<char*>(part + static_cast<int64_t>(z) * Mb * ldp);
+      b.ldc = ldp;
+      b.M = Mb; b.N = Nb; b.R = Tz.len();
+      b.out_mode = axonn::kOutF32;
+      b.phase = 0;
+      first.blocks.push_back(b);
+    } else {  // the last partial, cut at the shard rows, sums the others into each shard
+      for (int zz = 0; zz < s.gz; ++zz) {
+        int64_t r0, r1;
+        split_range(Mb, s.gz, zz, &r0, &r1);
+        if (r1 <= r0) continue;
+        Block b;
+        b.A = a_at(Kx.s + r0, Tz.s);
+        b.B = b_at(Tz.s, Ny.s);
+        b.C = static_cast<char*>(dW_shards[zz]);
+        b.ldc = ld_shard;
+        b.M = r1 - r0; b.N = Nb; b.R = Tz.len();
+        b.out_mode = user_mode;
+        if (s.gz > 1) {
+          b.red_count = s.gz - 1;
+          b.red_src = part + r0 * ldp;
+          b.red_stride = Mb * ldp;
+          b.red_ld = ldp;
+        }
+        last.blocks.push_back(b);
+      }
+    }
+  }
+  std::vector<Block> all = first.blocks;
+  all.insert(all.end(), last.blocks.begin(), last.blocks.end());
+  const int forced = g_forced_config.load();
+  first.config = last.config = (forced >= 0) ? forced : choose_config(all, *dev);
+  t_last_choice = TuneChoice{first.config, 1, first.group_m};
+  if (!first.blocks.empty()) {
+    st = run_blocks(v, first, *dev, stream);
+    if (st != AXONN_OK) return st;
+  }
+  st = run_blocks(v, last, *dev, stream);
+  if (st != AXONN_OK) return st;
+  return ok();
+}
+
 axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int64_t ldp, int64_t ldq,
                              int64_t ldc, const axonn_fc_shape_t* shape, uint32_t flags, void* ws,
                              size_t ws_bytes, cudaStream_t stream, int* best_config, int* best_split,
@@ -836,8 +1012,47 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   // Two rounds over all candidates, each candidate timed over kReps runs
   // per round; a candidate's time is its best round, so slow drifts of the
   // clock (power capping) do not favour the candidates measured first.
+  // Each candidate's kReps runs are captured into a CUDA graph and the graph
+  // is timed, so small products are measured on the device timeline rather
+  // than through host launch overhead.  Streams that cannot be captured
+  // (the legacy default stream) are timed with eager launches instead.
   constexpr int kReps = 3, kRounds = 2;
   std::vector<double> cand_us(cands.size(), -1.0);
+  auto time_candidate = [&](const TuneChoice& c, double* us) -> bool {
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+    bool ok_run = true;
+    if (cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) == cudaSuccess) {
+      for (int r = 0; r < kReps && ok_run; ++r)
+        ok_run = fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) == AXONN_OK;
+      const cudaError_t ec = cudaStreamEndCapture(stream, &graph);
+      if (ec != cudaSuccess || !ok_run || !graph ||
+          cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        (void)cudaGetLastError();
+        return false;
+      }
+      bool good = cudaGraphLaunch(exec, stream) == cudaSuccess;  // warm
+      good = good && cudaEventRecord(e0, stream) == cudaSuccess;
+      good = good && cudaGraphLaunch(exec, stream) == cudaSuccess;
+      good = good && cudaEventRecord(e1, stream) == cudaSuccess;
+      good = good && cudaEventSynchronize(e1) == cudaSuccess;
+      cudaGraphExecDestroy(exec);
+      cudaGraphDestroy(graph);
+      if (!good) return false;
+    } else {
+      (void)cudaGetLastError();
+      cudaEventRecord(e0, stream);
+      for (int r = 0; r < kReps && ok_run; ++r)
+        ok_run = fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) == AXONN_OK;
+      cudaEventRecord(e1, stream);
+      if (cudaEventSynchronize(e1) != cudaSuccess || !ok_run) return false;
+    }
+    float ms = 0;
+    cudaEventElapsedTime(&ms, e0, e1);
+    *us = 1e3 * ms / kReps;
+    return true;
+  };
   for (int round = 0; round < kRounds; ++round) {
     for (size_t i = 0; i < cands.size(); ++i) {
       const TuneChoice& c = cands[i];
@@ -845,15 +1060,8 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
       if (fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) != AXONN_OK)
         continue;
       if (t_last_choice.split != c.split) continue;  // the split could not be applied
-      cudaEventRecord(e0, stream);
-      bool okrun = true;
-      for (int r = 0; r < kReps && okrun; ++r)
-        okrun = fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) == AXONN_OK;
-      cudaEventRecord(e1, stream);
-      if (cudaEventSynchronize(e1) != cudaSuccess || !okrun) continue;
-      float ms = 0;
-      cudaEventElapsedTime(&ms, e0, e1);
-      const double us = 1e3 * ms / kReps;
+      double us = 0;
+      if (!time_candidate(c, &us)) continue;
       if (cand_us[i] < 0 || us < cand_us[i]) cand_us[i] = us;
     }
   }
@@ -966,6 +1174,11 @@ axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, ui
   if (!bytes) return fail(AXONN_ERR_INVALID_ARG, "bytes is NULL");
   axonn_status_t st = check_shape(op, shape, flags);
   if (st != AXONN_OK) return st;
+  if (flags & AXONN_ZSHARDED) {
+    if (op != AXONN_OP_WGRAD) return fail(AXONN_ERR_INVALID_ARG, "AXONN_ZSHARDED applies to the weight gradient");
+    *bytes = zsharded_ws_bytes(*shape);
+    return ok();
+  }
   *bytes = vgrid_ws_bytes(op, *shape, flags);
   if (!(flags & AXONN_VGRID)) {
     // Products that leave SMs idle may split their reduction range.

@@ -44,10 +44,13 @@ def make_operand(name, T, K, N, stored_t, seed, kind="normal", scale=None, h=1, 
 def to_device(bits):
     """bf16 bits (possibly a row-padded view) -> CUDA tensor view with the
     same row stride."""
-    import torch
-    base = bits.base if bits.base is not None and bits.base.ndim == 2 else bits
-    t = fc_inputs.as_torch_bf16(np.ascontiguousarray(base), "cuda")
-    return t[:, : bits.shape[1]] if base is not bits else t
+    base = bits.base
+    padded_view = (base is not None and isinstance(base, np.ndarray) and base.ndim == 2
+                   and base.shape[0] == bits.shape[0] and bits.strides == base.strides
+                   and bits.ctypes.data == base.ctypes.data and base.flags.c_contiguous)
+    if padded_view:       # a column slice of a wider array: keep its row stride
+        return fc_inputs.as_torch_bf16(base, "cuda")[:, : bits.shape[1]]
+    return fc_inputs.as_torch_bf16(np.ascontiguousarray(bits).copy(), "cuda")
 
 
 def run_gpu(fc, op, P, Q, p_t, q_t, T, K, N, grid=(1, 1, 1), coords=(0, 0, 0), extra=0,

@@ -167,3 +167,23 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     assert fc.axonn_tune_cache_size() == 2
     fc.axonn_tune_cache_clear()
     assert fc.axonn_tune_cache_size() == 0
+
+
+def test_zsharded_validation(fc):
+    lib = fc.load()
+    shards = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    # row length not a multiple of 8
+    assert lib.axonn_shards_gather(shards, 2, 64, 12, 16, FAKE, 16, 0) == fc.ERR_ALIGNMENT
+    # too many shards
+    big = (ctypes.c_void_p * 65)(*([FAKE] * 65))
+    assert lib.axonn_shards_gather(big, 65, 640, 8, 8, FAKE, 8, 0) == fc.ERR_INVALID_ARG
+    # the flag is only for the workspace query of the weight gradient
+    s = fc.Shape(64, 64, 64, (2, 2, 2))
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_fc_workspace_size("fwd", s, fc.ZSHARDED)
+    assert fc.axonn_fc_workspace_size("wgrad", s, fc.ZSHARDED) == 1 * 32 * 32 * 4
+    assert _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, fc.Shape(64, 64, 64),
+                fc.ZSHARDED) == fc.ERR_INVALID_ARG
+    # missing workspace
+    st = lib.axonn_fc_wgrad_zsharded(FAKE, FAKE, shards, 64, 64, 32, ctypes.byref(s), 0, 0, 0, 0)
+    assert st == fc.ERR_WORKSPACE

@@ -206,3 +206,26 @@ def test_planted_mistake_is_caught(monkeypatch):
     with pytest.raises(AssertionError):
         dX, _ = oracle.fc_dgrad(_bits(g["dY"]), _bits(g["W"]))
         assert np.array_equal(dX, np.array(g["dX"], float))
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 4])
+def test_shards_gather_back_to_the_block(G):
+    Wb = fc_inputs.normal_bf16((45, 24), seed=14, tid=1)
+    shards = oracle.shard_rows(Wb, G)
+    assert [s.shape[0] for s in shards] == [b - a for a, b in
+                                           (oracle.split_range(45, G, z) for z in range(G))]
+    assert np.array_equal(oracle.gather_shards(shards), Wb)
+
+
+@pytest.mark.parametrize("grid,xy", [((2, 2, 2), (1, 0)), ((1, 4, 4), (0, 3)), ((3, 1, 2), (2, 0))])
+def test_wgrad_zsharded_is_the_vgrid_block_cut_in_shards(grid, xy):
+    T, K, N = 41, 50, 36
+    X = fc_inputs.small_int_bf16((T, K), seed=15, tid=1, h=2)
+    dY = fc_inputs.small_int_bf16((T, N), seed=15, tid=3, h=2)
+    Cs, Ss = oracle.wgrad_zsharded(X, dY, False, False, T, K, N, grid, xy)
+    full, Sfull = oracle.fc_vgrid("wgrad", X, dY, False, False, T, K, N, grid)
+    Kx = oracle.split_range(K, grid[0], xy[0])
+    Ny = oracle.split_range(N, grid[1], xy[1])
+    assert np.array_equal(oracle.gather_shards(Cs), full[Kx[0]:Kx[1], Ny[0]:Ny[1]])
+    assert np.array_equal(oracle.gather_shards(Ss), Sfull[Kx[0]:Kx[1], Ny[0]:Ny[1]])
+    assert len(Cs) == grid[2]
