@@ -188,10 +188,14 @@ axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void*
 /*
  * Per-shape tuning -- the GB300 counterpart of the pages' "automated BLAS
  * kernel tuning" (TL;DR of the sciencestack.ai page; "The reading", review of
- * arXiv 2502.08145).  Runs this call once per candidate -- every kernel
- * configuration x rasterisation group {8, 16, 32}, and, for products that
- * leave SMs idle and have workspace, reduction splits {2, 4, 8} -- times
- * each with CUDA events on `stream` (the call synchronises the stream), and
+ * arXiv 2502.08145).  Runs this call once per candidate -- kernel
+ * configuration x rasterisation group {8, 16 tile rows; 8, 16 tile columns,
+ * written -8, -16}, every configuration for products that leave SMs idle
+ * (with reduction splits {2, 4, 8} when workspace is given), the 128x256 and
+ * 256-row configurations otherwise -- and times each (through a captured
+ * CUDA graph where the stream allows it) relative to the default choice run
+ * just before and after it, so clock drift under the power cap cancels.  The
+ * call synchronises `stream`.  It
  * records the fastest for later calls with the same op, sizes, grid, block
  * and flags on a GPU with the same SM count.  Arguments are those of the
  * op's entry point (op is an axonn_op_t); the caller's output is

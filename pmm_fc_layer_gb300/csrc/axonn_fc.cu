@@ -663,7 +663,7 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     if (forced_cfg >= 0) ch.config = forced_cfg;
   }
   if (ch.config < 0 || ch.config >= kNumConfigs) ch.config = choose_config(plan.blocks, *dev);
-  if (ch.group_m < 1) ch.group_m = 16;
+  if (ch.group_m == 0) ch.group_m = 16;
 
   // Split of the reduction range: S slices of whole stages, fp32 partials in
   // the workspace, then the fixed-order sum into the caller's output.
@@ -995,10 +995,16 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   if (s.gx * s.gy * s.gz > 1 && !(flags & AXONN_VGRID))
     block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
 
+  // Candidates.  Products that fill the GPU many times over only try the
+  // configurations that ever win there (the 128x256 and 256-row tiles);
+  // under-filled products try everything, reduction splits included.
+  const bool small = split_eligible(rows.len(), cols.len(), red.len(), *dev);
   std::vector<TuneChoice> cands;
-  for (int c = 0; c < kNumConfigs; ++c)
-    for (int gm : {8, 16, 32}) cands.push_back(TuneChoice{c, 1, gm});
-  if (!(flags & AXONN_VGRID) && split_eligible(rows.len(), cols.len(), red.len(), *dev))
+  for (int c = 0; c < kNumConfigs; ++c) {
+    if (!small && !(c == 1 || c == 3 || c == 5)) continue;
+    for (int gm : {8, 16, -8, -16}) cands.push_back(TuneChoice{c, 1, gm});
+  }
+  if (!(flags & AXONN_VGRID) && small)
     for (int c = 0; c < 2; ++c)
       for (int sp = 2; sp <= kMaxSplit; sp *= 2)
         if (red.len() / sp >= kSplitMinR && ws && ws_bytes >= split_ws_bytes(rows.len(), cols.len(), sp))
@@ -1053,22 +1059,44 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
     *us = 1e3 * ms / kReps;
     return true;
   };
-  for (int round = 0; round < kRounds; ++round) {
+  // Under a power cap the SM clock drifts while candidates run, so every
+  // candidate is timed between two runs of a reference (the default choice)
+  // and scored by its time over theirs; a candidate's score is its best
+  // round.
+  TuneChoice ref;
+  {
+    std::vector<Block> probe(1);
+    probe[0].M = rows.len(); probe[0].N = cols.len(); probe[0].R = red.len();
+    ref.config = choose_config(probe, *dev);
+  }
+  std::vector<double> cand_ratio(cands.size(), -1.0);
+  double ref_us = 0;
+  bool ref_ok = fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &ref) == AXONN_OK &&
+                time_candidate(ref, &ref_us);
+  for (int round = 0; round < kRounds && ref_ok; ++round) {
     for (size_t i = 0; i < cands.size(); ++i) {
       const TuneChoice& c = cands[i];
       if (round > 0 && cand_us[i] < 0) continue;  // failed in the first round
       if (fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) != AXONN_OK)
         continue;
       if (t_last_choice.split != c.split) continue;  // the split could not be applied
-      double us = 0;
+      double us = 0, ref_next = 0;
       if (!time_candidate(c, &us)) continue;
-      if (cand_us[i] < 0 || us < cand_us[i]) cand_us[i] = us;
+      if (!time_candidate(ref, &ref_next)) ref_next = ref_us;
+      const double ratio = us / (0.5 * (ref_us + ref_next));
+      ref_us = ref_next;
+      if (cand_ratio[i] < 0 || ratio < cand_ratio[i]) {
+        cand_ratio[i] = ratio;
+        cand_us[i] = us;
+      }
     }
   }
   TuneEntry best;
   best.us = -1;
+  double best_ratio = 0;
   for (size_t i = 0; i < cands.size(); ++i)
-    if (cand_us[i] >= 0 && (best.us < 0 || cand_us[i] < best.us)) {
+    if (cand_ratio[i] >= 0 && (best.us < 0 || cand_ratio[i] < best_ratio)) {
+      best_ratio = cand_ratio[i];
       best.us = cand_us[i];
       best.choice = cands[i];
     }
@@ -1144,7 +1172,7 @@ axonn_status_t axonn_tune_cache_load(const char* path) {
     e.choice.split = atoi(split.c_str());
     e.choice.group_m = atoi(gm.c_str());
     e.us = atof(us.c_str());
-    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m < 1)
+    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m == 0)
       return fail(AXONN_ERR_INVALID_ARG, "%s:%d: unknown configuration", path, lineno);
     loaded[key] = e;
   }

@@ -121,17 +121,30 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams<MAXP>& P, int 
   while (p + 1 < P.num_problems && t >= P.prob[p + 1].tile_start) ++p;
   const ProblemDesc& d = P.prob[p];
   const int lt = t - d.tile_start;
-  // Grouped rasterisation: walk group_m tile rows down one tile column before
-  // moving right, so concurrently running CTAs share A and B panels in L2.
-  const int per_group = P.group_m * d.tiles_n;
-  const int group = lt / per_group;
-  const int first_m = group * P.group_m;
-  const int gsize = min(P.group_m, d.tiles_m - first_m);
-  const int in_group = lt - group * per_group;
+  // Grouped rasterisation, so that concurrently running CTAs share operand
+  // panels in L2.  group_m > 0: walk group_m tile rows down one tile column
+  // before moving right.  group_m < 0: walk -group_m tile columns along one
+  // tile row before moving down.
   TileCoord c;
   c.p = p;
-  c.m_blk = first_m + in_group % gsize;
-  c.n_blk = in_group / gsize;
+  if (P.group_m > 0) {
+    const int per_group = P.group_m * d.tiles_n;
+    const int group = lt / per_group;
+    const int first_m = group * P.group_m;
+    const int gsize = min(P.group_m, d.tiles_m - first_m);
+    const int in_group = lt - group * per_group;
+    c.m_blk = first_m + in_group % gsize;
+    c.n_blk = in_group / gsize;
+  } else {
+    const int gn = -P.group_m;
+    const int per_group = gn * d.tiles_m;
+    const int group = lt / per_group;
+    const int first_n = group * gn;
+    const int gsize = min(gn, d.tiles_n - first_n);
+    const int in_group = lt - group * per_group;
+    c.n_blk = first_n + in_group % gsize;
+    c.m_blk = in_group / gsize;
+  }
   return c;
 }
 
