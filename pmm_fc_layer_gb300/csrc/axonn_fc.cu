@@ -269,6 +269,26 @@ axonn_status_t encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint6
   return AXONN_OK;
 }
 
+// MN-major operand stored [R rows x MN] as a 3-D map {64, R, MN/64} (chunk
+// stride 128 B): one box {64, bk, chunks} loads every 64-wide chunk of a
+// tile.  Needs MN % 64 == 0 so that no chunk runs past the end of a row;
+// chunks past the last one are zero-filled like any out-of-range box.
+axonn_status_t encode_mn_3d(CUtensorMap* m, const void* base, uint64_t mn, uint64_t r, int64_t ld,
+                            uint32_t bk, uint32_t chunks) {
+  auto fn = encode_fn();
+  if (!fn) return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+  cuuint64_t dims[3] = {64, r, mn / 64};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2u, 128};
+  cuuint32_t box[3] = {64, bk, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult rr = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (rr != CUDA_SUCCESS)
+    return fail(AXONN_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", static_cast<int>(rr));
+  return AXONN_OK;
+}
+
 // tcgen05 instruction descriptor, kind::f16: bf16 A and B, fp32 D.
 uint32_t make_idesc(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
@@ -373,10 +393,14 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     if (b.R > 0) {
       axonn_status_t s;
       const uint32_t bk = static_cast<uint32_t>(c.bk);
-      if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, bk);
+      d.a_3d = !c.pair && v.a_mn && b.M % 64 == 0;
+      d.b_3d = !c.pair && v.b_mn && b.N % 64 == 0;
+      if (d.a_3d) s = encode_mn_3d(&P.tma[np], b.A, b.M, b.R, v.lda, bk, c.bm / 64);
+      else if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, bk);
       else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, bk, a_rows);
       if (s != AXONN_OK) return s;
-      if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, bk);
+      if (d.b_3d) s = encode_mn_3d(&P.tmb[np], b.B, b.N, b.R, v.ldb, bk, b_cols / 64);
+      else if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, bk);
       else s = encode_2d(&P.tmb[np], b.B, b.R, b.N, v.ldb, bk, b_cols);
       if (s != AXONN_OK) return s;
     }

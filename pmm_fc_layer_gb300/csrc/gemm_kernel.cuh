@@ -56,6 +56,8 @@ struct ProblemDesc {
   const float* red_src;   // partial 0 of this problem's output, element (0,0)
   int64_t red_stride;     // elements between consecutive partials
   int64_t red_ld;         // row stride of a partial, elements
+  int32_t a_3d, b_3d;     // MN-major operand whose tile comes in one 3-D box
+  int32_t pad_;
 };
 
 template <int MAXP>
@@ -359,6 +361,12 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, L::kStageBytes);
           const int r0 = k * BK;
+          // An MN-major tile is (rows or columns / 64) chunks of BK rows of
+          // 128 B; with a 3-D tensor map {64, R, MN/64} one box brings all of
+          // them (fewer TMA operations per stage), else one box per chunk.
+          if (d.a_3d) {
+            tma_load_3d(a_tile(stage), ma, fb, 0, r0, m0 / 64);
+          } else
 #pragma unroll
           for (int hh = 0; hh < MH; ++hh) {
             const uint32_t at = a_tile(stage) + hh * L::kAHalfBytes;
@@ -370,7 +378,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
               tma_load_2d(at, ma, fb, r0, m0 + kBM * hh);
             }
           }
-          if (d.b_mn) {
+          if (d.b_3d) {
+            tma_load_3d(b_tile(stage), mb, fb, 0, r0, n0 / 64);
+          } else if (d.b_mn) {
 #pragma unroll
             for (int h = 0; h < BN / 64; ++h)
               tma_load_2d(b_tile(stage) + h * (BK * 128), mb, fb, n0 + 64 * h, r0);

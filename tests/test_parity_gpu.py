@@ -31,7 +31,7 @@ def forced(cuda_lib, request):
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("p_t,q_t", LAYOUTS)
 @pytest.mark.parametrize("T,K,N", [(128, 64, 256), (300, 200, 520), (129, 1000, 257),
-                                   (520, 136, 776)])
+                                   (520, 136, 776), (384, 200, 448), (320, 448, 200)])
 def test_integer_exact_layouts_and_tails(cuda_lib, forced, op, p_t, q_t, T, K, N):
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, p_t, seed=21, kind="int")
