@@ -48,6 +48,10 @@
  *    wait inside a kernel that expired) is reported by axonn_sync_status.
  *  - Errors are status codes; axonn_last_error() gives a thread-local message.
  *    No C++ exception crosses this boundary.
+ *  - Threads: every entry point may be called from several host threads at
+ *    once (on different streams); the tuning table and per-device set-up are
+ *    guarded by locks.  The kernel-configuration override and the wait
+ *    timeout are process-wide.
  *  - Empty outputs (an extent of 0) return AXONN_OK and touch nothing; an
  *    empty reduction range writes zeros (leaves C unchanged with
  *    AXONN_ACCUM_F32).

@@ -71,8 +71,11 @@ struct DeviceState {
 };
 
 constexpr int kPairStages = 6;
+// Per-device state lives in a fixed table so that pointers handed out stay
+// valid while other threads initialise other devices.
+constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
-std::vector<DeviceState> g_devs;
+DeviceState g_devs[kMaxDevices];
 
 template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
 cudaError_t set_smem_attr() {
@@ -108,8 +111,8 @@ axonn_status_t device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(AXONN_ERR_UNSUPPORTED, "device index %d", dev);
   std::lock_guard<std::mutex> lk(g_dev_mu);
-  if (static_cast<int>(g_devs.size()) <= dev) g_devs.resize(dev + 1);
   DeviceState& d = g_devs[dev];
   if (!d.attrs_set) {
     int major = 0, minor = 0;
@@ -368,10 +371,13 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
   // Rows of A and columns of B that one CTA loads per stage.
   const uint32_t a_rows = 128;
   const uint32_t b_cols = c.pair ? c.bn / 2 : c.bn;
-  int tiles = 0, np = 0;
+  int64_t tiles = 0;
+  int np = 0;
   for (const Block& b : blocks) {
     if (b.M == 0 || b.N == 0) continue;
     if (np >= MAXP) return fail(AXONN_ERR_UNSUPPORTED, "too many block products");
+    if (tiles + ((b.M + c.bm - 1) / c.bm) * ((b.N + c.bn - 1) / c.bn) > (int64_t{1} << 30))
+      return fail(AXONN_ERR_UNSUPPORTED, "more than 2^30 output tiles in one launch");
     ProblemDesc& d = P.prob[np];
     d.C = b.C;
     d.ldc = b.ldc;
@@ -380,7 +386,7 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.R = static_cast<int32_t>(b.R);
     d.tiles_m = static_cast<int32_t>((b.M + c.bm - 1) / c.bm);
     d.tiles_n = static_cast<int32_t>((b.N + c.bn - 1) / c.bn);
-    d.tile_start = tiles;
+    d.tile_start = static_cast<int32_t>(tiles);
     d.num_k = static_cast<int32_t>((b.R + c.bk - 1) / c.bk);
     d.a_mn = v.a_mn;
     d.b_mn = v.b_mn;
@@ -408,7 +414,7 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     ++np;
   }
   P.num_problems = np;
-  P.total_tiles = tiles;
+  P.total_tiles = static_cast<int32_t>(tiles);
   P.group_m = group_m;
   P.inject = g_inject.load();
   P.timeout_ns = g_timeout_ns.load();
