@@ -107,11 +107,21 @@ int max_active_pairs(int sms) {
   return n;
 }
 
+// Host threads that never touched the runtime have no current context, and
+// the driver call that encodes tensor maps needs one: make the current
+// device's primary context current, once per thread and device.
+thread_local int t_context_device = -1;
+
 axonn_status_t device_state(DeviceState** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kMaxDevices) return fail(AXONN_ERR_UNSUPPORTED, "device index %d", dev);
+  if (t_context_device != dev) {
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "cudaSetDevice(%d): %s", dev, cudaGetErrorString(e));
+    t_context_device = dev;
+  }
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DeviceState& d = g_devs[dev];
   if (!d.attrs_set) {
