@@ -70,7 +70,8 @@ struct DeviceState {
   bool attrs_set = false;
 };
 
-constexpr int kPairStages = 6;
+constexpr int kPairStages = 6;   // 256 x 256 pair tiles, 32 KB stages
+constexpr int kPair2Stages = 4;  // 512 x 256 pair tiles, 48 KB stages
 // Per-device state lives in a fixed table so that pointers handed out stay
 // valid while other threads initialise other devices.
 constexpr int kMaxDevices = 64;
@@ -84,11 +85,11 @@ cudaError_t set_smem_attr() {
                               axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes);
 }
 
-template <int STAGES, int MAXP>
+template <int BN, int STAGES, int MAXP, int MH>
 cudaError_t set_pair_smem_attr() {
-  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_pair_kernel<STAGES, MAXP>,
+  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              axonn::PairSmemLayout<STAGES>::kBytes);
+                              axonn::PairSmemLayout<BN, STAGES, MH>::kBytes);
 }
 
 // Clusters of 2 that can be resident at once (SM pairs inside a GPC).
@@ -96,10 +97,11 @@ int max_active_pairs(int sms) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * sms, 1, 1);
   cfg.blockDim = dim3(axonn::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = axonn::PairSmemLayout<kPairStages>::kBytes;
+  cfg.dynamicSmemBytes = axonn::PairSmemLayout<256, kPairStages, 1>::kBytes;
   int n = 0;
   cudaError_t e = cudaOccupancyMaxActiveClusters(
-      &n, reinterpret_cast<const void*>(&axonn::fc_gemm_tcgen05_pair_kernel<kPairStages, 1>), &cfg);
+      &n, reinterpret_cast<const void*>(&axonn::fc_gemm_tcgen05_pair_kernel<256, kPairStages, 1, 1>),
+      &cfg);
   if (e != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = sms / 2;
@@ -143,8 +145,12 @@ axonn_status_t device_state(DeviceState** out) {
                         set_smem_attr<192, 64, 5, kMaxProblems>(),
                         set_smem_attr<192, 64, 4, 1, 2>(), set_smem_attr<192, 64, 4, 8, 2>(),
                         set_smem_attr<192, 64, 4, kMaxProblems, 2>(),
-                        set_pair_smem_attr<kPairStages, 1>(), set_pair_smem_attr<kPairStages, 8>(),
-                        set_pair_smem_attr<kPairStages, kMaxProblems>()};
+                        set_pair_smem_attr<256, kPairStages, 1, 1>(),
+                        set_pair_smem_attr<256, kPairStages, 8, 1>(),
+                        set_pair_smem_attr<256, kPairStages, kMaxProblems, 1>(),
+                        set_pair_smem_attr<256, kPair2Stages, 1, 2>(),
+                        set_pair_smem_attr<256, kPair2Stages, 8, 2>(),
+                        set_pair_smem_attr<256, kPair2Stages, kMaxProblems, 2>()};
     for (cudaError_t x : es)
       if (x != cudaSuccess)
         return fail(AXONN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(x));
@@ -339,10 +345,11 @@ constexpr KernelConfig kConfigs[] = {
     {"1cta_256x256", 256, 256, 64, false, 128},
     {"1cta_128x192", 128, 192, 64, false, 128},
     {"1cta_256x192", 256, 192, 64, false, 128},
+    {"pair_512x256", 512, 256, 64, true, 256},
 };
 // Throughput of each configuration relative to 1cta_128x256 on full waves
 // (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
-constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12};
+constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12, 1.2};
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
 std::atomic<int> g_forced_config{-1};
 thread_local int t_last_config = -1;
@@ -378,8 +385,10 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
                            const KernelConfig& c, int group_m) {
   static_assert(sizeof(GemmParams<MAXP>) < 32000, "kernel parameter space");
   memset(&P, 0, sizeof(P));
-  // Rows of A and columns of B that one CTA loads per stage.
+  // Rows of A and columns of B that one CTA loads per stage (A in boxes of
+  // 128 rows, or one 3-D box of all its rows).
   const uint32_t a_rows = 128;
+  const uint32_t cta_rows = c.pair ? c.bm / 2 : c.bm;
   const uint32_t b_cols = c.pair ? c.bn / 2 : c.bn;
   int64_t tiles = 0;
   int np = 0;
@@ -409,9 +418,9 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     if (b.R > 0) {
       axonn_status_t s;
       const uint32_t bk = static_cast<uint32_t>(c.bk);
-      d.a_3d = !c.pair && v.a_mn && b.M % 64 == 0;
-      d.b_3d = !c.pair && v.b_mn && b.N % 64 == 0;
-      if (d.a_3d) s = encode_mn_3d(&P.tma[np], b.A, b.M, b.R, v.lda, bk, c.bm / 64);
+      d.a_3d = v.a_mn && b.M % 64 == 0;
+      d.b_3d = v.b_mn && b.N % 64 == 0;
+      if (d.a_3d) s = encode_mn_3d(&P.tma[np], b.A, b.M, b.R, v.lda, bk, cta_rows / 64);
       else if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, bk);
       else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, bk, a_rows);
       if (s != AXONN_OK) return s;
@@ -445,15 +454,16 @@ axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const Devi
   return AXONN_OK;
 }
 
-template <int STAGES, int MAXP>
+template <int BN, int STAGES, int MAXP, int MH>
 axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
                            cudaStream_t stream) {
   GemmParams<MAXP> P;
   axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int pairs = P.total_tiles < dev.max_pairs ? P.total_tiles : dev.max_pairs;
-  axonn::fc_gemm_tcgen05_pair_kernel<STAGES, MAXP>
-      <<<2 * pairs, axonn::kThreads, axonn::PairSmemLayout<STAGES>::kBytes, stream>>>(P);
+  axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
+      <<<2 * pairs, axonn::cta_threads<MH>(), axonn::PairSmemLayout<BN, STAGES, MH>::kBytes,
+         stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM pair launch: %s", cudaGetErrorString(e));
   return AXONN_OK;
@@ -473,7 +483,8 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
     case 3: return launch_single<256, 64, 3, P1, 2>(v, plan, dev, stream);
     case 4: return launch_single<192, 64, 5, P1>(v, plan, dev, stream);
     case 5: return launch_single<192, 64, 4, P1, 2>(v, plan, dev, stream);
-    default: return launch_pair<kPairStages, P1>(v, plan, dev, stream);
+    case 6: return launch_pair<256, kPair2Stages, P1, 2>(v, plan, dev, stream);
+    default: return launch_pair<256, kPairStages, P1, 1>(v, plan, dev, stream);
   }
 }
 
@@ -1036,12 +1047,12 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
     block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
 
   // Candidates.  Products that fill the GPU many times over only try the
-  // configurations that ever win there (the 128x256 and 256-row tiles);
+  // configurations that ever win there (128x256, 256-row and 512-row tiles);
   // under-filled products try everything, reduction splits included.
   const bool small = split_eligible(rows.len(), cols.len(), red.len(), *dev);
   std::vector<TuneChoice> cands;
   for (int c = 0; c < kNumConfigs; ++c) {
-    if (!small && !(c == 1 || c == 3 || c == 5)) continue;
+    if (!small && !(c == 1 || c == 3 || c == 5 || c == 6)) continue;
     for (int gm : {8, 16, -8, -16}) cands.push_back(TuneChoice{c, 1, gm});
   }
   if (!(flags & AXONN_VGRID) && small)

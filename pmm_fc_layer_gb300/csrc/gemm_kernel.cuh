@@ -188,31 +188,49 @@ __device__ __forceinline__ void add_partials(const ProblemDesc& d, int row, int 
   for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(s[j] + __uint_as_float(r[j]));
 }
 
+// Writes 16 packed bf16 pairs, columns [col0, col0+32) of one output row.
+// Each thread writes its own row, so a warp's store instruction touches 32
+// rows: 32-byte stores (whole L2 sectors) take half the time of 16-byte ones
+// and are used whenever the address is 32-byte aligned.
+__device__ __forceinline__ void store_bf16_32(const ProblemDesc& d, int row, int col0,
+                                              const uint32_t* pk) {
+  const int ncols = min(32, d.N - col0);
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + col0;
+  if (ncols == 32) {
+    if ((reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+      st_global_v8(out, pk);
+      st_global_v8(out + 16, pk + 8);
+    } else {
+#pragma unroll
+      for (int v = 0; v < 4; ++v)
+        reinterpret_cast<uint4*>(out)[v] =
+            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+  } else {
+    unsigned short* o16 = reinterpret_cast<unsigned short*>(out);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) o16[j] = static_cast<unsigned short>((pk[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+  }
+}
+
 // Writes 32 accumulator columns [col0, col0+32) of one output row.
 __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int col0,
                                             uint32_t (&r)[32]) {
   const int ncols = min(32, d.N - col0);
   if (d.red_count > 0) add_partials(d, row, col0, ncols, r);
   if (d.out_mode == kOutBF16) {
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + col0;
     uint32_t pk[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(r[2 * j], r[2 * j + 1]);
-    if (ncols == 32) {
-#pragma unroll
-      for (int v = 0; v < 4; ++v)
-        reinterpret_cast<uint4*>(out)[v] =
-            make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-    } else {
-      unsigned short* o16 = reinterpret_cast<unsigned short*>(out);
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (j < ncols) o16[j] = static_cast<unsigned short>((pk[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-    }
+    store_bf16_32(d, row, col0, pk);
   } else {
     float* out = reinterpret_cast<float*>(d.C) + row * d.ldc + col0;
     const bool acc = d.out_mode == kOutF32Accum;
-    if (ncols == 32) {
+    if (ncols == 32 && !acc && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) st_global_v8(out + 8 * v, &r[8 * v]);
+    } else if (ncols == 32) {
 #pragma unroll
       for (int v = 0; v < 8; ++v) {
         float4 x = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
@@ -242,6 +260,57 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
 #pragma unroll
     for (int j = 0; j < 32; ++j) r[j] = 0u;
     store_chunk(d, row, col0, r);
+  }
+}
+
+// Epilogue of one warp: its 32 accumulator rows x BN columns (TMEM lanes
+// of t_row) to global memory, then one arrive on `tempty` by the lanes with
+// `arrive` set (a shared::cluster address of the peer CTA's barrier when
+// `remote`).  A plain bf16 output is
+// first packed into registers (BN / 2 words per thread) and TMEM is released
+// before any store, so the next tile's MMAs start while the stores drain.
+// The other output modes store chunk by chunk and release TMEM afterwards.
+template <int BN>
+__device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t t_row, int row,
+                                                  int n0, uint32_t tempty, bool arrive,
+                                                  bool remote) {
+  if (d.out_mode == kOutBF16 && d.red_count == 0) {
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[16 * c + j] = cvt_bf16x2_ordered(r[2 * j], r[2 * j + 1]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (arrive) {
+      if (remote) mbar_arrive_cluster(tempty);
+      else mbar_arrive(tempty);
+    }
+    if (row < d.M) {
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+        if (n0 + 32 * c < d.N) store_bf16_32(d, row, n0 + 32 * c, &pk[16 * c]);
+    }
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int col0 = n0 + c * 32;
+    if (col0 >= d.N) break;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, r);
+    tmem_ld_wait();
+    if (row < d.M) store_chunk(d, row, col0, r);
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (arrive) {
+    if (remote) mbar_arrive_cluster(tempty);
+    else mbar_arrive(tempty);
   }
 }
 
@@ -473,18 +542,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        if (col0 >= d.N) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tmem_ld_wait();
-        if (row < d.M) store_chunk(d, row, col0, r);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(b));
+      drain_accumulator<BN>(d, t_row, row, n0, tempty_bar(b), lane == 0, false);
       ++acc;
     }
   }

@@ -1,41 +1,56 @@
-// CTA-pair variant of the FC GEMM: one tcgen05 MMA of M = 256, N = 256 is
-// shared by the two CTAs of a cluster (cta_group::2).
+// CTA-pair variant of the FC GEMM: each tcgen05 MMA of M = 256 rows and
+// N = BN columns is shared by the two CTAs of a cluster (cta_group::2).
 //
-// Tile = 256 x 256 output elements per CTA pair.  CTA rank r of the pair
-//   * TMA-loads rows [128 r, 128 r + 128) of the A tile and columns
-//     [128 r, 128 r + 128) of the B tile into its OWN shared memory (no
-//     multicast); both CTAs' loads complete on the even CTA's mbarrier,
-//   * holds rows [128 r, 128 r + 128) x 256 columns of the fp32 accumulator
-//     in its own TMEM (double-buffered: 2 x 256 columns),
+// Pair tile = MH*256 x BN output elements.  CTA rank r of the pair
+//   * TMA-loads its own MH*128 rows [MH*128 r, MH*128 (r+1)) of the A tile
+//     and columns [BN/2 r, BN/2 (r+1)) of the B tile into its OWN shared
+//     memory (no multicast); both CTAs' loads complete on the even CTA's
+//     mbarrier,
+//   * holds its MH*128 rows x BN columns of the fp32 accumulator in its own
+//     TMEM,
 //   * runs its own epilogue over those rows.
+// MMA hh (0 <= hh < MH) multiplies rows [128 hh, 128 hh + 128) of each
+// CTA's A slice by the whole B tile, so one B slice serves MH MMAs.
+// MH = 1: 256 x BN tiles, accumulator double-buffered (2 x BN columns),
+//         6 stages of 32 KB.
+// MH = 2: 512 x BN tiles; each SM loads 48 KB per 64-deep stage for
+//         2 x 128 x BN x 64 multiply-adds (about 1.35x the FLOPs per loaded
+//         byte of MH = 1), the two accumulators fill TMEM (single-buffered)
+//         and 8 epilogue warps drain them.
 // The even CTA (rank 0) issues every MMA and commits stage releases and
-// accumulator-ready signals to both CTAs with one multicast commit; the odd
-// CTA's epilogue reports a drained accumulator to the even CTA's barrier.
-//
-// Per CTA and 64-deep stage: 16 KB of A + 16 KB of B, so 6 stages fit in
-// 192 KB.  Every wait is bounded exactly as in the single-CTA kernel.
+// accumulator-ready signals to both CTAs with one multicast commit (an
+// mbarrier signal, not a data copy); the odd CTA's epilogue reports a
+// drained accumulator to the even CTA's barrier.  Every wait is bounded
+// exactly as in the single-CTA kernel.
 #pragma once
 #include "gemm_kernel.cuh"
 
 namespace axonn {
 
-constexpr int kPairBM = 256;  // output rows per CTA pair
-constexpr int kPairBN = 256;  // output columns per CTA pair
-
-template <int STAGES>
+template <int BN, int STAGES, int MH>
 struct PairSmemLayout {
-  static constexpr int kABytes = 128 * kBK * 2;
-  static constexpr int kBBytes = (kPairBN / 2) * kBK * 2;
+  static constexpr int kAHalfBytes = 128 * kBK * 2;
+  static constexpr int kABytes = MH * kAHalfBytes;
+  static constexpr int kBBytes = (BN / 2) * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kNumBars = 2 * STAGES + 5;
   static constexpr int kBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
 };
 
-template <int STAGES, int MAXP>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <int BN, int STAGES, int MAXP, int MH>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH>(), 1)
     fc_gemm_tcgen05_pair_kernel(const __grid_constant__ GemmParams<MAXP> P) {
-  using L = PairSmemLayout<STAGES>;
-  constexpr uint32_t kTmemCols = 2 * kPairBN;
+  using L = PairSmemLayout<BN, STAGES, MH>;
+  static_assert(MH == 1 || MH == 2, "row halves per CTA");
+  static_assert(BN == 128 || BN == 256, "each CTA's B slice is whole 64-column chunks");
+  constexpr int kAccBufs = MH == 1 ? 2 : 1;
+  constexpr uint32_t kHalfCols = BN;
+  constexpr uint32_t kAccCols = MH * kHalfCols;
+  constexpr uint32_t kTmemUsed = kAccBufs * kAccCols;
+  constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
+  constexpr int kCtaM = MH * 128;   // output rows of one CTA
+  constexpr int kTileM = 2 * kCtaM;  // output rows of the pair
+  static_assert(kTmemUsed <= 512, "TMEM columns");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -67,7 +82,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), 2 * kEpiWarps);
+      mbar_init(tempty_bar(b), 2 * kEpiWarps * MH);
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -101,8 +116,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const ProblemDesc& d = P.prob[tc.p];
         const CUtensorMap* ma = &P.tma[tc.p];
         const CUtensorMap* mb = &P.tmb[tc.p];
-        const int m0 = tc.m_blk * kPairBM + static_cast<int>(rank) * 128;
-        const int n0 = tc.n_blk * kPairBN + static_cast<int>(rank) * (kPairBN / 2);
+        const int m0 = tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM;
+        const int n0 = tc.n_blk * BN + static_cast<int>(rank) * (BN / 2);
         for (int k = 0; k < d.num_k; ++k) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
             ok = false;
@@ -111,15 +126,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const int r0 = k * kBK;
-          if (d.a_mn) {
-            tma_load_2d_pair(a_tile(stage), ma, fb, m0, r0);
-            tma_load_2d_pair(a_tile(stage) + 8192, ma, fb, m0 + 64, r0);
-          } else {
-            tma_load_2d_pair(a_tile(stage), ma, fb, r0, m0);
+          if (d.a_3d) {
+            tma_load_3d_pair(a_tile(stage), ma, fb, 0, r0, m0 / 64);
+          } else
+#pragma unroll
+          for (int hh = 0; hh < MH; ++hh) {
+            const uint32_t at = a_tile(stage) + hh * L::kAHalfBytes;
+            if (d.a_mn) {
+              tma_load_2d_pair(at, ma, fb, m0 + 128 * hh, r0);
+              tma_load_2d_pair(at + kBK * 128, ma, fb, m0 + 128 * hh + 64, r0);
+            } else {
+              tma_load_2d_pair(at, ma, fb, r0, m0 + 128 * hh);
+            }
           }
-          if (d.b_mn) {
-            tma_load_2d_pair(b_tile(stage), mb, fb, n0, r0);
-            tma_load_2d_pair(b_tile(stage) + 8192, mb, fb, n0 + 64, r0);
+          if (d.b_3d) {
+            tma_load_3d_pair(b_tile(stage), mb, fb, 0, r0, n0 / 64);
+          } else if (d.b_mn) {
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              tma_load_2d_pair(b_tile(stage) + h * (kBK * 128), mb, fb, n0 + 64 * h, r0);
           } else {
             tma_load_2d_pair(b_tile(stage), mb, fb, r0, n0);
           }
@@ -152,11 +177,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
         if (d.num_k == 0) continue;
-        const uint32_t b = acc & 1u;
-        const uint32_t acc_phase = (acc >> 1) & 1u;
+        const uint32_t b = acc % kAccBufs;
+        const uint32_t acc_phase = (acc / kAccBufs) & 1u;
         if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * kPairBN;
+        const uint32_t d_tmem = tmem_base + b * kAccCols;
         for (int k = 0; k < d.num_k; ++k) {
           if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
             ok = false;
@@ -167,9 +192,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t sb = b_tile(stage);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t ad = operand_desc<kBK>(sa, kk, d.a_mn);
             const uint64_t bd = operand_desc<kBK>(sb, kk, d.b_mn);
-            umma_bf16_pair(d_tmem, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+#pragma unroll
+            for (int hh = 0; hh < MH; ++hh) {
+              const uint64_t ad = operand_desc<kBK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
+              umma_bf16_pair(d_tmem + hh * kHalfCols, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+            }
           }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
           if (++stage == STAGES) {
@@ -186,40 +214,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int hh = (warp - 2) >> 2;  // row half (accumulator) it drains
     uint32_t acc = 0;
     for (int t = pair; t < P.total_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile(P, t);
       const ProblemDesc& d = P.prob[tc.p];
-      const int row = tc.m_blk * kPairBM + static_cast<int>(rank) * 128 + q * 32 + lane;
-      const int n0 = tc.n_blk * kPairBN;
+      const int row =
+          tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM + hh * 128 + q * 32 + lane;
+      const int n0 = tc.n_blk * BN;
       if (d.num_k == 0) {
-        if (row < d.M) store_zero_row(d, row, n0, kPairBN);
+        if (row < d.M) store_zero_row(d, row, n0, BN);
         continue;
       }
-      const uint32_t b = acc & 1u;
-      const uint32_t acc_phase = (acc >> 1) & 1u;
+      const uint32_t b = acc % kAccBufs;
+      const uint32_t acc_phase = (acc / kAccBufs) & 1u;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull_bar(b), acc_phase, tmo, abort_flag, kSiteEpiTmemFull);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kPairBN;
-#pragma unroll 1
-      for (int c = 0; c < kPairBN / 32; ++c) {
-        const int col0 = n0 + c * 32;
-        if (col0 >= d.N) break;
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(t_row + c * 32, r);
-        tmem_ld_wait();
-        if (row < d.M) store_chunk(d, row, col0, r);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(tempty_bar(b));
-        else mbar_arrive_cluster(mapa_shared(tempty_bar(b), 0));
-      }
+      const uint32_t t_row =
+          tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
+      drain_accumulator<BN>(d, t_row, row, n0,
+                            leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), lane == 0,
+                            !leader);
       ++acc;
     }
   }
