@@ -92,6 +92,18 @@ cudaError_t set_pair_smem_attr() {
                               axonn::PairSmemLayout<BN, STAGES, MH>::kBytes);
 }
 
+// The 12-warp kernels move registers between warpgroups (setmaxnreg); the
+// split adds up to exactly the launch allocation of kRegsAtLaunch per thread.
+// A build whose kernels were allocated fewer registers would make the
+// increase wait forever, so such a kernel is refused before any launch.
+template <typename K>
+cudaError_t check_split_regs(K kernel, bool* ok) {
+  cudaFuncAttributes a = {};
+  cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(kernel));
+  if (e == cudaSuccess && a.numRegs != axonn::kRegsAtLaunch) *ok = false;
+  return e;
+}
+
 // Clusters of 2 that can be resident at once (SM pairs inside a GPC).
 int max_active_pairs(int sms) {
   cudaLaunchConfig_t cfg = {};
@@ -154,6 +166,19 @@ axonn_status_t device_state(DeviceState** out) {
     for (cudaError_t x : es)
       if (x != cudaSuccess)
         return fail(AXONN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(x));
+    bool split_ok = true;
+    cudaError_t rs[] = {
+        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, 1, 2>, &split_ok),
+        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, 8, 2>, &split_ok),
+        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, kMaxProblems, 2>,
+                         &split_ok)};
+    for (cudaError_t x : rs)
+      if (x != cudaSuccess)
+        return fail(AXONN_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(x));
+    if (!split_ok)
+      return fail(AXONN_ERR_UNSUPPORTED,
+                  "a 12-warp GEMM kernel was not built with %d registers per thread",
+                  axonn::kRegsAtLaunch);
     d.max_pairs = max_active_pairs(d.sms);
     d.attrs_set = true;
   }
@@ -415,6 +440,8 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.red_src = b.red_src;
     d.red_stride = b.red_stride;
     d.red_ld = b.red_ld;
+    d.fast_bf16 = b.out_mode == axonn::kOutBF16 && b.red_count == 0 &&
+                  reinterpret_cast<uintptr_t>(b.C) % 32 == 0 && b.ldc % 16 == 0;
     if (b.R > 0) {
       axonn_status_t s;
       const uint32_t bk = static_cast<uint32_t>(c.bk);
@@ -462,7 +489,7 @@ axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const Device
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int pairs = P.total_tiles < dev.max_pairs ? P.total_tiles : dev.max_pairs;
   axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
-      <<<2 * pairs, axonn::cta_threads<MH>(), axonn::PairSmemLayout<BN, STAGES, MH>::kBytes,
+      <<<2 * pairs, axonn::cta_threads<MH, MH == 2>(), axonn::PairSmemLayout<BN, STAGES, MH>::kBytes,
          stream>>>(P);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM pair launch: %s", cudaGetErrorString(e));

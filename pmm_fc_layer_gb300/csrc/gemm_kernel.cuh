@@ -10,10 +10,11 @@
 // so tile boxes that run past a block edge read zeros exactly as a GPU that
 // held only that shard would.
 //
-// CTA = 6 warps, one CTA per SM, persistent over a static tile schedule:
+// One CTA per SM, persistent over a static tile schedule:
 //   warp 0      TMA producer (one thread): smem ring of STAGES x (A | B) tiles
 //   warp 1      TMEM owner + MMA issuer (one thread): tcgen05.mma 128 x BN x 16
-//   warps 2..5  epilogue: tcgen05.ld -> fp32 -> bf16 RNE (or fp32) -> global
+//   epilogue    4 warps per 128-row half: tcgen05.ld -> fp32 -> bf16 RNE (or
+//               fp32) -> global
 // The accumulator is double-buffered in TMEM (2 x BN columns) so the epilogue
 // of tile i overlaps the mainloop of tile i+1.
 //
@@ -34,9 +35,36 @@ constexpr int kBK = 64;        // reduction depth per stage of the CTA-pair kern
 constexpr int kThreads = 192;  // 6 warps: producer, MMA issuer, 4 epilogue
 constexpr int kEpiWarps = 4;
 
-// A CTA may own MH row halves of 128 (an MH*128 x BN tile): 2 + 4*MH warps.
-template <int MH>
-constexpr int cta_threads() { return 64 + 128 * MH; }
+// A CTA may own MH row halves of 128 (an MH*128 x BN tile).  Warp roles:
+//   MH = 1:            6 warps: producer, MMA issuer, 4 epilogue warps (2..5).
+//   MH = 2:           10 warps: producer, MMA issuer, 8 epilogue warps (2..9).
+//   MH = 2, SPLIT:    12 warps in 3 warpgroups: warpgroup 0 holds the producer
+//                     (warp 0) and the MMA issuer (warp 1) and gives registers
+//                     to warpgroups 1 and 2 (setmaxnreg), which drain row
+//                     halves 0 and 1 holding a whole bf16 accumulator row of
+//                     up to 128 words per thread.
+// The split is used only where it measures faster (the CTA-pair kernel with
+// 256-column tiles); in the single-CTA kernel it slowed the operand supply.
+template <int MH, bool SPLIT = false>
+constexpr int cta_threads() { return MH == 1 ? 192 : (SPLIT ? 384 : 320); }
+template <int MH, bool SPLIT = false>
+constexpr int epi_first_warp() { return MH == 2 && SPLIT ? 4 : 2; }
+constexpr int kRegsAtLaunch = 168;  // 384 threads, one CTA per SM
+constexpr int kRegsControl = 56;    // warpgroup 0 after the split
+constexpr int kRegsEpilogue = 224;  // warpgroups 1 and 2 after the split
+static_assert(128 * kRegsControl + 256 * kRegsEpilogue <= 384 * kRegsAtLaunch,
+              "register split exceeds the launch allocation");
+
+// Register split of a 12-warp CTA (no-ops otherwise), made inside each
+// role's branch so that the compiler allocates each branch for its budget.
+template <int MH, bool SPLIT>
+__device__ __forceinline__ void shrink_registers() {
+  if constexpr (MH == 2 && SPLIT) setmaxnreg_dec<kRegsControl>();
+}
+template <int MH, bool SPLIT>
+__device__ __forceinline__ void grow_registers() {
+  if constexpr (MH == 2 && SPLIT) setmaxnreg_inc<kRegsEpilogue>();
+}
 
 // Output modes of the epilogue.
 enum OutMode : int32_t { kOutBF16 = 0, kOutF32 = 1, kOutF32Accum = 2 };
@@ -57,7 +85,7 @@ struct ProblemDesc {
   int64_t red_stride;     // elements between consecutive partials
   int64_t red_ld;         // row stride of a partial, elements
   int32_t a_3d, b_3d;     // MN-major operand whose tile comes in one 3-D box
-  int32_t pad_;
+  int32_t fast_bf16;      // bf16 output, no partials, every row 32-byte aligned
 };
 
 template <int MAXP>
@@ -266,15 +294,17 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
 // Epilogue of one warp: its 32 accumulator rows x BN columns (TMEM lanes
 // of t_row) to global memory, then one arrive on `tempty` by the lanes with
 // `arrive` set (a shared::cluster address of the peer CTA's barrier when
-// `remote`).  A plain bf16 output is
-// first packed into registers (BN / 2 words per thread) and TMEM is released
-// before any store, so the next tile's MMAs start while the stores drain.
-// The other output modes store chunk by chunk and release TMEM afterwards.
+// `remote`).  A plain bf16 tile that lies wholly inside the output is first
+// packed into registers (BN / 2 words per thread) and TMEM is released
+// before any store, so the next tile's MMAs start while the stores drain;
+// its rows are stored as 32-byte vectors.  Other tiles (partials to add,
+// fp32 output, a ragged right edge, rows not 32-byte aligned) are stored
+// chunk by chunk and release TMEM afterwards.
 template <int BN>
 __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t t_row, int row,
                                                   int n0, uint32_t tempty, bool arrive,
                                                   bool remote) {
-  if (d.out_mode == kOutBF16 && d.red_count == 0) {
+  if (d.fast_bf16 && n0 + BN <= d.N) {
     uint32_t pk[BN / 2];
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
@@ -291,9 +321,9 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
       else mbar_arrive(tempty);
     }
     if (row < d.M) {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + n0;
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c)
-        if (n0 + 32 * c < d.N) store_bf16_32(d, row, n0 + 32 * c, &pk[16 * c]);
+      for (int v = 0; v < BN / 16; ++v) st_global_v8(out + 16 * v, &pk[8 * v]);
     }
     return;
   }
@@ -519,10 +549,10 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       umma_commit(mma_done_bar);
       wait_bounded(mma_done_bar, 0, tmo, abort_flag, kSiteDrainMma, false);
     }
-  } else {
+  } else if (warp >= epi_first_warp<MH>()) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int hh = (warp - 2) >> 2;  // row half (accumulator) it drains
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int hh = (warp - epi_first_warp<MH>()) >> 2;  // row half it drains
     uint32_t acc = 0;
     for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
       const TileCoord tc = decode_tile(P, t);

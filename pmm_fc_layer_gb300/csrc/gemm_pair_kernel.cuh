@@ -16,7 +16,8 @@
 // MH = 2: 512 x BN tiles; each SM loads 48 KB per 64-deep stage for
 //         2 x 128 x BN x 64 multiply-adds (about 1.35x the FLOPs per loaded
 //         byte of MH = 1), the two accumulators fill TMEM (single-buffered)
-//         and 8 epilogue warps drain them.
+//         and 8 epilogue warps drain them; the CTA has 12 warps and moves
+//         registers from warpgroup 0 to the epilogue (see cta_threads).
 // The even CTA (rank 0) issues every MMA and commits stage releases and
 // accumulator-ready signals to both CTAs with one multicast commit (an
 // mbarrier signal, not a data copy); the odd CTA's epilogue reports a
@@ -38,7 +39,7 @@ struct PairSmemLayout {
 };
 
 template <int BN, int STAGES, int MAXP, int MH>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH>(), 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH == 2>(), 1)
     fc_gemm_tcgen05_pair_kernel(const __grid_constant__ GemmParams<MAXP> P) {
   using L = PairSmemLayout<BN, STAGES, MH>;
   static_assert(MH == 1 || MH == 2, "row halves per CTA");
@@ -104,6 +105,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH>(), 1
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tmo = P.timeout_ns;
 
+  constexpr bool kSplit = MH == 2;  // 12 warps, registers moved to the epilogue
+  if (warp < epi_first_warp<MH, kSplit>()) shrink_registers<MH, kSplit>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0 && P.inject != 1) {
@@ -212,10 +215,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH>(), 1
       umma_commit_pair(mma_done_bar);
       wait_bounded(mma_done_bar, 0, tmo, abort_flag, kSiteDrainMma, false);
     }
-  } else {
+  } else if (warp >= epi_first_warp<MH, kSplit>()) {
+    grow_registers<MH, kSplit>();
     // ------------------------------------------------------------ epilogue
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int hh = (warp - 2) >> 2;  // row half (accumulator) it drains
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int hh = (warp - epi_first_warp<MH, kSplit>()) >> 2;  // row half it drains
     uint32_t acc = 0;
     for (int t = pair; t < P.total_tiles; t += num_pairs) {
       const TileCoord tc = decode_tile(P, t);

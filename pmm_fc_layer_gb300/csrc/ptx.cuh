@@ -78,6 +78,18 @@ __device__ __forceinline__ uint32_t cvt_bf16x2_ordered(uint32_t lo, uint32_t hi)
   return r;
 }
 
+// Per-thread register budget of the executing warpgroup (all 128 threads
+// execute it).  An increase draws on registers released by decreases within
+// the CTA's launch allocation and waits until they are available.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // 32-byte global store of eight 32-bit words (address 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
