@@ -108,8 +108,10 @@ typedef struct {
  *   (X_blk [Tz x Kx], W_blk [Kx x Ny], Y_blk [Tz x Ny], each with its ld);
  *   with it they address the full matrices and the block is located by its
  *   offsets, its partial written at Y[Tz, Ny].
- *   ws / ws_bytes: device workspace, needed only with AXONN_VGRID when
- *   G_x > 1 (size from axonn_fc_workspace_size); may be NULL / 0 otherwise.
+ *   ws / ws_bytes: device workspace, needed with AXONN_VGRID when G_x > 1
+ *   (size from axonn_fc_workspace_size).  Otherwise optional: a full-size
+ *   one enables the reduction split of small products and the stream-K
+ *   tail of large ones; NULL / 0 runs without them.
  */
 axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw,
                             int64_t ldy, const axonn_fc_shape_t* shape, uint32_t flags,
@@ -214,7 +216,10 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
                              float* best_us);
 
 /* The tuning table as text, one JSON object per line:
- *   {"key": "...", "config": "<name>", "split": S, "group_m": G, "us": t}
+ *   {"key": "...", "config": "<name>", "split": S, "group_m": G,
+ *    "streamk": 0 | 1 | 2, "us": t}
+ * (streamk: off, on for a partial round at most a quarter full, on wherever
+ * it applies; a line without it loads as 1).
  * save writes every entry; load merges a file's entries into the table
  * (AXONN_ERR_INVALID_ARG on an unreadable file or a malformed line, leaving
  * the table unchanged).  Host-only. */
@@ -229,9 +234,11 @@ void axonn_last_choice(int* config, int* split, int* group_m);
 
 /* Workspace bytes an op needs with these flags (0 when none).  `op` is an
  * axonn_op_t.  With AXONN_VGRID it is the fp32 partials of the reduced grid
- * axis; without, it is nonzero only for products that leave most SMs idle
+ * axis.  Without it, it is nonzero for products that leave most SMs idle
  * (fewer 128x256 tiles than two waves), which may then split their
- * reduction range -- passing less workspace just disables the split.
+ * reduction range, and for products of more than one wave of 128x128 tiles,
+ * which may run a stream-K tail (see axonn_set_streamk; up to about 40 MB on
+ * a 152-SM GPU).  Passing less workspace just disables either.
  * Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
                                        size_t* bytes);
@@ -277,6 +284,25 @@ axonn_status_t axonn_set_kernel_config(int config);
  * running configuration 2) it keeps resident at once. */
 axonn_status_t axonn_device_info(int* sms, int* max_pairs);
 int axonn_num_kernel_configs(void);
+
+/* Stream-K tail for later calls in this process: -1 = as tuned, 0 = off,
+ * 1 = on wherever it applies.  It applies to a single-product call that is
+ * given the workspace axonn_fc_workspace_size reports and whose output
+ * tiles do not fill a whole number of rounds of the persistent grid: the
+ * last partial round plus one full round are cut into equal ranges of
+ * 64-deep reduction steps, one per CTA (or CTA pair).  Untuned calls use it
+ * only when the partial round is at most a quarter full; the tuner times
+ * off, that default and always-on, and keeps the fastest.  Each such tile is computed in at most
+ * two pieces.  The piece that holds the tile's first steps adds the other's
+ * fp32 partial (fixed order), so results are deterministic for a given
+ * shape and GPU but may differ in the last bit from a call with it off.
+ * Not part of the source pages: it removes the idle SMs of the last wave.
+ * AXONN_ERR_INVALID_ARG for another mode.  Host-only. */
+axonn_status_t axonn_set_streamk(int mode);
+
+/* Output tiles the last GEMM launch on this thread computed as stream-K
+ * pieces (0: none).  Host-only. */
+int axonn_last_streamk_tiles(void);
 const char* axonn_kernel_config_name(int config);
 int axonn_last_kernel_config(void);
 

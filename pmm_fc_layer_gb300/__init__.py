@@ -33,7 +33,8 @@ EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_s
            "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
            "axonn_last_choice",
            "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
-           "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs", "axonn_device_info",
+           "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs",
+           "axonn_set_streamk", "axonn_last_streamk_tiles", "axonn_device_info",
            "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
            "axonn_version")
 
@@ -114,6 +115,10 @@ def load(path: str | None = None):
         lib.axonn_debug_set_inject.restype = None
         lib.axonn_set_kernel_config.argtypes = [ctypes.c_int]
         lib.axonn_set_kernel_config.restype = ctypes.c_int
+        lib.axonn_set_streamk.argtypes = [ctypes.c_int]
+        lib.axonn_set_streamk.restype = ctypes.c_int
+        lib.axonn_last_streamk_tiles.argtypes = []
+        lib.axonn_last_streamk_tiles.restype = ctypes.c_int
         lib.axonn_num_kernel_configs.restype = ctypes.c_int
         lib.axonn_device_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
         lib.axonn_device_info.restype = ctypes.c_int
@@ -298,6 +303,16 @@ def axonn_debug_set_inject(mode: int):
 def axonn_set_kernel_config(config: int):
     """Force kernel configuration `config` (-1: automatic choice)."""
     _check(load().axonn_set_kernel_config(int(config)))
+
+
+def axonn_set_streamk(mode: int):
+    """Stream-K tail: -1 as tuned (default on), 0 off, 1 on."""
+    _check(load().axonn_set_streamk(int(mode)))
+
+
+def axonn_last_streamk_tiles() -> int:
+    """Stream-K tiles of the last GEMM launch on this thread (0: none)."""
+    return int(load().axonn_last_streamk_tiles())
 
 
 def axonn_device_info():

@@ -379,10 +379,17 @@ constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[
 std::atomic<int> g_forced_config{-1};
 thread_local int t_last_config = -1;
 
+// Stream-K modes: off; on when the partial round is at most a quarter full
+// (the default); on whenever the launch allows it.
+enum StreamKMode : int { kStreamKOff = 0, kStreamKShortTail = 1, kStreamKAlways = 2 };
+
 struct LaunchPlan {
   int config = 1;
   int group_m = 16;
   std::vector<Block> blocks;
+  int streamk = kStreamKOff;
+  void* ws = nullptr;  // workspace for the stream-K partials and counters
+  size_t ws_bytes = 0;
 };
 
 // One way to run a call: kernel configuration, split of the reduction range
@@ -392,7 +399,9 @@ struct TuneChoice {
   int config = -1;
   int split = 1;
   int group_m = 16;
+  int streamk = 1;  // StreamKMode (see configure_streamk)
 };
+std::atomic<int> g_forced_streamk{-1};
 thread_local TuneChoice t_last_choice;
 
 struct TuneEntry {
@@ -467,6 +476,53 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
   return AXONN_OK;
 }
 
+// Stream-K tail of a single-problem launch over `units` persistent CTAs (or
+// CTA pairs): when the tiles do not fill a whole number of rounds, the last
+// partial round and one full round (at least `units` tiles) are cut by
+// reduction steps into equal consecutive ranges, one per unit, so every unit
+// finishes at about the same time.  Units then start their ranges at
+// different reduction offsets, so units working on neighbouring tiles no
+// longer read the same operand panels at the same time.  When a unit's share
+// is close to one tile (a partial round at most a quarter full) the offsets
+// stay close and the tail is faster.  Otherwise the lost L2 reuse can cost
+// more than the idle SMs it saves, so kStreamKShortTail applies it only in
+// the first case.  A tile is cut into at most two pieces;
+// the piece holding its first steps adds the other's fp32 partial, so the
+// order of the sum is fixed by the shape and the unit count.  Workspace: a
+// block of kStreamKFlagBytes for the per-unit counters (zeroed here, in
+// stream order, before the launch) followed by one tile-sized fp32 slot per
+// unit.
+constexpr size_t kStreamKFlagBytes = 1024;  // up to 256 units
+thread_local int t_last_sk_tiles = 0;
+size_t streamk_ws_bytes(const KernelConfig& c, int units) {
+  return kStreamKFlagBytes + static_cast<size_t>(units) * c.bm * c.bn * 4;
+}
+
+template <int MAXP>
+axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int units,
+                                 const LaunchPlan& plan, cudaStream_t stream) {
+  const int T = P.total_tiles;
+  t_last_sk_tiles = 0;
+  if (plan.streamk == kStreamKOff || P.num_problems != 1 || units <= 0 || T <= units ||
+      T % units == 0)
+    return AXONN_OK;
+  if (plan.streamk == kStreamKShortTail && 4 * (T % units) > units) return AXONN_OK;
+  const int nk = P.prob[0].num_k;
+  const int S = T >= 2 * units ? units + T % units : T;
+  if (nk < 2 || static_cast<int64_t>(S) * nk >= (int64_t{1} << 31)) return AXONN_OK;
+  if (static_cast<size_t>(units) * 4 > kStreamKFlagBytes || !plan.ws ||
+      plan.ws_bytes < streamk_ws_bytes(c, units) || (reinterpret_cast<uintptr_t>(plan.ws) & 255u) != 0)
+    return AXONN_OK;
+  const cudaError_t e = cudaMemsetAsync(plan.ws, 0, static_cast<size_t>(units) * 4, stream);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream-K counters: %s", cudaGetErrorString(e));
+  P.sk_tiles = S;
+  t_last_sk_tiles = S;
+  P.sk_slot_floats = c.bm * c.bn;
+  P.sk_flags = static_cast<uint32_t*>(plan.ws);
+  P.sk_partials = reinterpret_cast<float*>(static_cast<char*>(plan.ws) + kStreamKFlagBytes);
+  return AXONN_OK;
+}
+
 template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
 axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
                              cudaStream_t stream) {
@@ -474,6 +530,8 @@ axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const Devi
   axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int grid = P.total_tiles < dev.sms ? P.total_tiles : dev.sms;
+  st = configure_streamk(P, kConfigs[plan.config], grid, plan, stream);
+  if (st != AXONN_OK) return st;
   axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>
       <<<grid, axonn::cta_threads<MH>(), axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes, stream>>>(P);
   cudaError_t e = cudaGetLastError();
@@ -488,6 +546,8 @@ axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const Device
   axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int pairs = P.total_tiles < dev.max_pairs ? P.total_tiles : dev.max_pairs;
+  st = configure_streamk(P, kConfigs[plan.config], pairs, plan, stream);
+  if (st != AXONN_OK) return st;
   axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
       <<<2 * pairs, axonn::cta_threads<MH, MH == 2>(), axonn::PairSmemLayout<BN, STAGES, MH>::kBytes,
          stream>>>(P);
@@ -740,6 +800,8 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     const int forced_cfg = g_forced_config.load();
     if (forced_cfg >= 0) ch.config = forced_cfg;
   }
+  const int forced_sk = g_forced_streamk.load();
+  if (forced_sk >= 0) ch.streamk = forced_sk == 0 ? kStreamKOff : kStreamKAlways;
   if (ch.config < 0 || ch.config >= kNumConfigs) ch.config = choose_config(plan.blocks, *dev);
   if (ch.group_m == 0) ch.group_m = 16;
 
@@ -781,6 +843,11 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   }
   plan.config = ch.config;
   plan.group_m = ch.group_m;
+  if (!vgrid && ch.split == 1) {
+    plan.streamk = ch.streamk;
+    plan.ws = ws;
+    plan.ws_bytes = ws_bytes;
+  }
   t_last_choice = ch;
   // Products whose epilogue sums earlier partials run in a second launch,
   // after every partial they read has been written by the first.
@@ -1178,6 +1245,26 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
       best.us = cand_us[i];
       best.choice = cands[i];
     }
+  // The candidates ran with the default stream-K mode.  Time the best one
+  // in all three modes back to back (so they see the same clock) and keep
+  // the fastest; the modes are the same launch where no tail applies.
+  if (best.us >= 0 && g_forced_streamk.load() < 0) {
+    double mode_us[3] = {-1, -1, -1};
+    for (int m : {kStreamKOff, kStreamKShortTail, kStreamKAlways}) {
+      TuneChoice c = best.choice;
+      c.streamk = m;
+      if (fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) != AXONN_OK ||
+          !time_candidate(c, &mode_us[m]))
+        mode_us[m] = -1;
+    }
+    int pick = best.choice.streamk;
+    for (int m : {kStreamKOff, kStreamKShortTail, kStreamKAlways})
+      if (mode_us[m] >= 0 && (mode_us[pick] < 0 || mode_us[m] < mode_us[pick])) pick = m;
+    if (mode_us[pick] >= 0) {
+      best.choice.streamk = pick;
+      best.us = mode_us[pick];
+    }
+  }
   cudaEventDestroy(e0);
   cudaEventDestroy(e1);
   if (best.us < 0) return fail(AXONN_ERR_CUDA, "no candidate configuration ran");
@@ -1200,9 +1287,10 @@ axonn_status_t axonn_tune_cache_save(const char* path) {
   for (const auto& kv : g_tune) {
     char line[512];
     snprintf(line, sizeof(line),
-             "{\"key\": \"%s\", \"config\": \"%s\", \"split\": %d, \"group_m\": %d, \"us\": %.3f}\n",
+             "{\"key\": \"%s\", \"config\": \"%s\", \"split\": %d, \"group_m\": %d, "
+             "\"streamk\": %d, \"us\": %.3f}\n",
              kv.first.c_str(), kConfigs[kv.second.choice.config].name, kv.second.choice.split,
-             kv.second.choice.group_m, kv.second.us);
+             kv.second.choice.group_m, kv.second.choice.streamk, kv.second.us);
     f << line;
   }
   return f ? ok() : fail(AXONN_ERR_INVALID_ARG, "write to %s failed", path);
@@ -1249,8 +1337,11 @@ axonn_status_t axonn_tune_cache_load(const char* path) {
       if (cfg == kConfigs[c].name) e.choice.config = c;
     e.choice.split = atoi(split.c_str());
     e.choice.group_m = atoi(gm.c_str());
+    std::string sk;
+    if (json_field(line, "streamk", &sk)) e.choice.streamk = atoi(sk.c_str());
     e.us = atof(us.c_str());
-    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m == 0)
+    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m == 0 ||
+        e.choice.streamk < kStreamKOff || e.choice.streamk > kStreamKAlways)
       return fail(AXONN_ERR_INVALID_ARG, "%s:%d: unknown configuration", path, lineno);
     loaded[key] = e;
   }
@@ -1297,6 +1388,11 @@ axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, ui
       if (s.gx * s.gy * s.gz > 1) block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
       if (rows.len() > 0 && cols.len() > 0 && split_eligible(rows.len(), cols.len(), red.len(), *dev))
         *bytes = split_ws_bytes(rows.len(), cols.len(), kMaxSplit);
+      // Products of more than one wave of tiles may run a stream-K tail.
+      const int64_t tiles128 = ((rows.len() + 127) / 128) * ((cols.len() + 127) / 128);
+      if (tiles128 > dev->sms)
+        for (const KernelConfig& c : kConfigs)
+          *bytes = std::max(*bytes, streamk_ws_bytes(c, c.pair ? dev->max_pairs : dev->sms));
     }
   }
   return ok();
@@ -1339,6 +1435,12 @@ axonn_status_t axonn_set_kernel_config(int config) {
 
 int axonn_num_kernel_configs(void) { return kNumConfigs; }
 
+axonn_status_t axonn_set_streamk(int mode) {
+  if (mode < -1 || mode > 1) return fail(AXONN_ERR_INVALID_ARG, "stream-K mode %d not in {-1, 0, 1}", mode);
+  g_forced_streamk.store(mode);
+  return ok();
+}
+
 axonn_status_t axonn_device_info(int* sms, int* max_pairs) {
   DeviceState* d = nullptr;
   axonn_status_t st = device_state(&d);
@@ -1353,6 +1455,8 @@ const char* axonn_kernel_config_name(int config) {
 }
 
 int axonn_last_kernel_config(void) { return t_last_config; }
+
+int axonn_last_streamk_tiles(void) { return t_last_sk_tiles; }
 
 const char* axonn_last_error(void) { return t_last_error.c_str(); }
 

@@ -98,6 +98,67 @@ struct GemmParams {
   int32_t group_m;     // tile rows per rasterisation group
   int32_t inject;      // test-only: 1 = the producer withholds every load
   uint64_t timeout_ns; // bound on any single mbarrier wait
+  // Stream-K tail (single-problem launches only; sk_tiles = 0 disables it).
+  // The last sk_tiles tiles of the tile order are not given whole to CTAs:
+  // their sk_tiles * num_k reduction steps are cut into gridDim equal,
+  // consecutive ranges, one per CTA (or CTA pair).  sk_tiles >= gridDim, so
+  // a range covers at least one tile and each tile is cut into at most two
+  // pieces: a head (steps 0..k1) finished by unit g at the end of its range,
+  // and a tail (k1..num_k) done by unit g+1 at the start of its range.  The
+  // tail is written as an fp32 partial to slot g+1 and unit g+1's epilogue
+  // warps each add one to counter g+1; the head's epilogue waits for the
+  // counter, adds that partial to its own accumulator and stores the tile.
+  int32_t sk_tiles;
+  int32_t sk_slot_floats;  // floats per partial slot (one tile)
+  float* sk_partials;      // gridDim slots (or one per CTA pair)
+  uint32_t* sk_flags;      // gridDim counters, zero at launch
+};
+
+// One unit of a CTA's work: reduction steps [k0, k1) of tile t.
+enum WorkKind : int { kWhole = 0, kHead = 1, kTail = 2 };
+struct WorkItem {
+  int t, k0, k1, kind;
+};
+
+// The work of unit `u` of `units` (a CTA, or a CTA pair): whole tiles
+// u, u + units, ... below the stream-K tiles, then its range of the
+// stream-K steps.  Every role of the unit walks the same sequence.
+// (The host keeps sk_tiles * num_k below 2^31.)
+template <int MAXP>
+struct WorkIter {
+  int t;
+  int s, s_end;  // stream-K steps still to do: [s, s_end)
+  int dp_end, nk, units;
+
+  __device__ __forceinline__ WorkIter(const GemmParams<MAXP>& P, int u, int units_) {
+    units = units_;
+    t = u;
+    dp_end = P.total_tiles - P.sk_tiles;
+    nk = P.prob[0].num_k;
+    const int64_t steps = static_cast<int64_t>(P.sk_tiles) * nk;
+    s = static_cast<int>(steps * u / units);
+    s_end = static_cast<int>(steps * (u + 1) / units);
+  }
+  __device__ __forceinline__ bool next(const GemmParams<MAXP>& P, WorkItem& w) {
+    if (t < dp_end) {
+      w.t = t;
+      w.k0 = 0;
+      w.k1 = -1;  // whole tile: num_k of its problem
+      w.kind = kWhole;
+      t += units;
+      return true;
+    }
+    if (s < s_end) {
+      const int st = s / nk;
+      w.t = dp_end + st;
+      w.k0 = s - st * nk;
+      w.k1 = min(nk, w.k0 + (s_end - s));
+      w.kind = (w.k0 == 0 && w.k1 == nk) ? kWhole : (w.k0 == 0 ? kHead : kTail);
+      s += w.k1 - w.k0;
+      return true;
+    }
+    return false;
+  }
 };
 
 // Device-side error word: 0 = no error.  Layout of a timeout record:
@@ -111,6 +172,7 @@ enum WaitSite : uint32_t {
   kSiteEpiTmemFull = 4,
   kSiteDrainLoads = 5,
   kSiteDrainMma = 6,
+  kSiteStreamK = 7,
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -132,6 +194,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (honor_abort && *abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      record_timeout(site);
+      return false;
+    }
+  }
+}
+
+// Bounded wait until the counter at p reaches target (acquire), with the
+// same limit and abort rules as wait_bounded.
+__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target,
+                                             uint64_t timeout_ns, volatile int* abort_flag,
+                                             uint32_t site) {
+  if (ld_acquire(p) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(128);
+    if (ld_acquire(p) >= target) return true;
+    if (*abort_flag) return false;
     if (global_timer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       record_timeout(site);
@@ -344,6 +425,49 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
   }
 }
 
+// Epilogue of one work item (see WorkIter) by one warp.  Whole tiles go to
+// the output.  A stream-K tail goes, in fp32, to partial slot `unit` (tile-
+// local rows and columns, BN floats a row) and then counts on counter
+// `unit`.  A stream-K head waits for counter `unit + 1` to reach
+// `flag_target` (every epilogue warp of that unit), adds slot `unit + 1` to
+// its accumulator and stores the tile.
+template <int BN, int MAXP>
+__device__ __forceinline__ void epilogue_item(const GemmParams<MAXP>& P, const ProblemDesc& d,
+                                              const WorkItem& w, int unit, int tile_m0, int n0,
+                                              uint32_t t_row, int row, uint32_t tempty,
+                                              bool remote, uint32_t flag_target,
+                                              volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  if (w.kind == kWhole) {
+    drain_accumulator<BN>(d, t_row, row, n0, tempty, lane == 0, remote);
+    return;
+  }
+  ProblemDesc ds = d;
+  ds.fast_bf16 = 0;
+  const int64_t origin = static_cast<int64_t>(tile_m0) * BN + n0;
+  if (w.kind == kTail) {
+    ds.C = P.sk_partials + static_cast<int64_t>(unit) * P.sk_slot_floats - origin;
+    ds.ldc = BN;
+    ds.out_mode = kOutF32;
+    ds.red_count = 0;
+    drain_accumulator<BN>(ds, t_row, row, n0, tempty, lane == 0, remote);
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) red_release_add(&P.sk_flags[unit], 1u);
+    return;
+  }
+  int ok = 1;
+  if (lane == 0)
+    ok = wait_counter(&P.sk_flags[unit + 1], flag_target, P.timeout_ns, abort_flag, kSiteStreamK);
+  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  __syncwarp();
+  ds.red_count = ok ? 1 : 0;
+  ds.red_src = P.sk_partials + static_cast<int64_t>(unit + 1) * P.sk_slot_floats - origin;
+  ds.red_ld = BN;
+  ds.red_stride = 0;
+  drain_accumulator<BN>(ds, t_row, row, n0, tempty, lane == 0, remote);
+}
+
 template <int BN, int BK, int STAGES, int MH = 1>
 struct SmemLayout {
   static constexpr int kAHalfBytes = kBM * BK * 2;
@@ -445,14 +569,17 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       uint32_t phase = 0;
       uint32_t loads = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile(P, t);
+      WorkIter<MAXP> it(P, blockIdx.x, gridDim.x);
+      WorkItem w;
+      while (ok && it.next(P, w)) {
+        const TileCoord tc = decode_tile(P, w.t);
         const ProblemDesc& d = P.prob[tc.p];
         const CUtensorMap* ma = &P.tma[tc.p];
         const CUtensorMap* mb = &P.tmb[tc.p];
         const int m0 = tc.m_blk * kTileM;
         const int n0 = tc.n_blk * BN;
-        for (int k = 0; k < d.num_k; ++k) {
+        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
+        for (int k = w.k0; k < k1; ++k) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -509,16 +636,19 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       uint32_t phase = 0;
       uint32_t acc = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < P.total_tiles; t += gridDim.x) {
-        const TileCoord tc = decode_tile(P, t);
+      WorkIter<MAXP> it(P, blockIdx.x, gridDim.x);
+      WorkItem w;
+      while (ok && it.next(P, w)) {
+        const TileCoord tc = decode_tile(P, w.t);
         const ProblemDesc& d = P.prob[tc.p];
-        if (d.num_k == 0) continue;
+        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
+        if (k1 <= w.k0) continue;
         const uint32_t b = acc % kAccBufs;
         const uint32_t acc_phase = (acc / kAccBufs) & 1u;
         if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kAccCols;
-        for (int k = 0; k < d.num_k; ++k) {
+        for (int k = w.k0; k < k1; ++k) {
           if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
             ok = false;
             break;
@@ -532,7 +662,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
 #pragma unroll
             for (int hh = 0; hh < MH; ++hh) {
               const uint64_t ad = operand_desc<BK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
-              umma_bf16(d_tmem + hh * kHalfCols, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+              umma_bf16(d_tmem + hh * kHalfCols, ad, bd, d.idesc, (k != w.k0 || kk != 0) ? 1u : 0u);
             }
           }
           umma_commit(empty_bar(stage));
@@ -554,12 +684,14 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int hh = (warp - epi_first_warp<MH>()) >> 2;  // row half it drains
     uint32_t acc = 0;
-    for (int t = blockIdx.x; t < P.total_tiles; t += gridDim.x) {
-      const TileCoord tc = decode_tile(P, t);
+    WorkIter<MAXP> it(P, blockIdx.x, gridDim.x);
+    WorkItem w;
+    while (it.next(P, w)) {
+      const TileCoord tc = decode_tile(P, w.t);
       const ProblemDesc& d = P.prob[tc.p];
       const int row = tc.m_blk * kTileM + hh * kBM + q * 32 + lane;
       const int n0 = tc.n_blk * BN;
-      if (d.num_k == 0) {
+      if ((w.k1 < 0 ? d.num_k : w.k1) <= w.k0) {
         if (row < d.M) store_zero_row(d, row, n0, BN);
         continue;
       }
@@ -572,7 +704,8 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      drain_accumulator<BN>(d, t_row, row, n0, tempty_bar(b), lane == 0, false);
+      epilogue_item<BN>(P, d, w, blockIdx.x, tc.m_blk * kTileM, n0, t_row, row, tempty_bar(b),
+                        false, kEpiWarps * MH, abort_flag);
       ++acc;
     }
   }

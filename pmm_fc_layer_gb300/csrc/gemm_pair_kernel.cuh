@@ -114,14 +114,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       uint32_t phase = 0;
       uint32_t loads = 0;
       bool ok = true;
-      for (int t = pair; ok && t < P.total_tiles; t += num_pairs) {
-        const TileCoord tc = decode_tile(P, t);
+      WorkIter<MAXP> it(P, pair, num_pairs);
+      WorkItem w;
+      while (ok && it.next(P, w)) {
+        const TileCoord tc = decode_tile(P, w.t);
         const ProblemDesc& d = P.prob[tc.p];
         const CUtensorMap* ma = &P.tma[tc.p];
         const CUtensorMap* mb = &P.tmb[tc.p];
         const int m0 = tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM;
         const int n0 = tc.n_blk * BN + static_cast<int>(rank) * (BN / 2);
-        for (int k = 0; k < d.num_k; ++k) {
+        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
+        for (int k = w.k0; k < k1; ++k) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
             ok = false;
             break;
@@ -176,16 +179,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       uint32_t phase = 0;
       uint32_t acc = 0;
       bool ok = true;
-      for (int t = pair; ok && t < P.total_tiles; t += num_pairs) {
-        const TileCoord tc = decode_tile(P, t);
+      WorkIter<MAXP> it(P, pair, num_pairs);
+      WorkItem w;
+      while (ok && it.next(P, w)) {
+        const TileCoord tc = decode_tile(P, w.t);
         const ProblemDesc& d = P.prob[tc.p];
-        if (d.num_k == 0) continue;
+        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
+        if (k1 <= w.k0) continue;
         const uint32_t b = acc % kAccBufs;
         const uint32_t acc_phase = (acc / kAccBufs) & 1u;
         if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kAccCols;
-        for (int k = 0; k < d.num_k; ++k) {
+        for (int k = w.k0; k < k1; ++k) {
           if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
             ok = false;
             break;
@@ -199,7 +205,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
 #pragma unroll
             for (int hh = 0; hh < MH; ++hh) {
               const uint64_t ad = operand_desc<kBK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
-              umma_bf16_pair(d_tmem + hh * kHalfCols, ad, bd, d.idesc, (k | kk) != 0 ? 1u : 0u);
+              umma_bf16_pair(d_tmem + hh * kHalfCols, ad, bd, d.idesc,
+                             (k != w.k0 || kk != 0) ? 1u : 0u);
             }
           }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
@@ -221,13 +228,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int hh = (warp - epi_first_warp<MH, kSplit>()) >> 2;  // row half it drains
     uint32_t acc = 0;
-    for (int t = pair; t < P.total_tiles; t += num_pairs) {
-      const TileCoord tc = decode_tile(P, t);
+    WorkIter<MAXP> it(P, pair, num_pairs);
+    WorkItem w;
+    while (it.next(P, w)) {
+      const TileCoord tc = decode_tile(P, w.t);
       const ProblemDesc& d = P.prob[tc.p];
       const int row =
           tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM + hh * 128 + q * 32 + lane;
       const int n0 = tc.n_blk * BN;
-      if (d.num_k == 0) {
+      if ((w.k1 < 0 ? d.num_k : w.k1) <= w.k0) {
         if (row < d.M) store_zero_row(d, row, n0, BN);
         continue;
       }
@@ -240,9 +249,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      drain_accumulator<BN>(d, t_row, row, n0,
-                            leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), lane == 0,
-                            !leader);
+      epilogue_item<BN>(P, d, w, pair, tc.m_blk * kTileM, n0, t_row, row,
+                        leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), !leader,
+                        2 * kEpiWarps * MH, abort_flag);
       ++acc;
     }
   }

@@ -142,18 +142,21 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     fc.axonn_tune_cache_clear()
     entries = [
         {"key": "op0_T8_K8_N8_g1x1x1_at0.0.0_f0_sm152", "config": "pair_256x256", "split": 1,
-         "group_m": 8, "us": 12.5},
+         "group_m": 8, "streamk": 0, "us": 12.5},
         {"key": "op1_T64_K512_N16_g1x1x1_at0.0.0_f0_sm152", "config": "1cta_128x128",
-         "split": 4, "group_m": 16, "us": 3.25},
+         "split": 4, "group_m": 16, "streamk": 2, "us": 3.25},
     ]
+    # a line written before the stream-K field existed loads with it on
+    legacy = {"key": "op2_T8_K8_N8_g1x1x1_at0.0.0_f0_sm152", "config": "pair_512x256", "split": 1,
+              "group_m": -16, "us": 7.0}
     src = tmp_path / "tune.jsonl"
-    src.write_text("".join(json.dumps(e) + "\n" for e in entries))
+    src.write_text("".join(json.dumps(e) + "\n" for e in entries + [legacy]))
     fc.axonn_tune_cache_load(str(src))
-    assert fc.axonn_tune_cache_size() == 2
+    assert fc.axonn_tune_cache_size() == 3
     out = tmp_path / "saved.jsonl"
     fc.axonn_tune_cache_save(str(out))
     saved = sorted((json.loads(l) for l in out.read_text().splitlines()), key=lambda e: e["key"])
-    assert saved == sorted(entries, key=lambda e: e["key"])
+    assert saved == sorted(entries + [dict(legacy, streamk=1)], key=lambda e: e["key"])
     # malformed or unknown entries are rejected and leave the table as it was
     bad = tmp_path / "bad.jsonl"
     bad.write_text('{"key": "x", "config": "no_such_config", "split": 1, "group_m": 8, "us": 1}\n')
@@ -162,11 +165,23 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     bad.write_text('{"key": "x", "split": 1}\n')
     with pytest.raises(fc.AxonnError):
         fc.axonn_tune_cache_load(str(bad))
+    bad.write_text('{"key": "x", "config": "pair_512x256", "split": 1, "group_m": 8, '
+                   '"streamk": 3, "us": 1}\n')
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_tune_cache_load(str(bad))
     with pytest.raises(fc.AxonnError):
         fc.axonn_tune_cache_load(str(tmp_path / "absent.jsonl"))
-    assert fc.axonn_tune_cache_size() == 2
+    assert fc.axonn_tune_cache_size() == 3
     fc.axonn_tune_cache_clear()
     assert fc.axonn_tune_cache_size() == 0
+
+
+def test_set_streamk(fc):
+    for mode in (-1, 0, 1, -1):
+        fc.axonn_set_streamk(mode)
+    for bad in (-2, 2):
+        with pytest.raises(fc.AxonnError):
+            fc.axonn_set_streamk(bad)
 
 
 def test_zsharded_validation(fc):
