@@ -113,22 +113,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       int stage = 0;
       uint32_t phase = 0;
       uint32_t loads = 0;
-      bool ok = true;
-      WorkIter<MAXP> it(P, pair, num_pairs);
-      WorkItem w;
-      while (ok && it.next(P, w)) {
-        const TileCoord tc = decode_tile(P, w.t);
+      for_each_work(P, pair, num_pairs, [&](int t, int k0, int k1, int) -> bool {
+        const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
         const CUtensorMap* ma = &P.tma[tc.p];
         const CUtensorMap* mb = &P.tmb[tc.p];
         const int m0 = tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM;
         const int n0 = tc.n_blk * BN + static_cast<int>(rank) * (BN / 2);
-        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
-        for (int k = w.k0; k < k1; ++k) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty)) {
-            ok = false;
-            break;
-          }
+        const int kend = k1 < 0 ? d.num_k : k1;
+        for (int k = k0; k < kend; ++k) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty))
+            return false;
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const int r0 = k * kBK;
@@ -160,7 +155,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
             phase ^= 1u;
           }
         }
-      }
+        return true;
+      });
       // Drain (even CTA): the full barriers count both CTAs' bytes, so the
       // last phase of each stage completing means every copy has landed.
       if (leader) {
@@ -178,24 +174,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc = 0;
-      bool ok = true;
-      WorkIter<MAXP> it(P, pair, num_pairs);
-      WorkItem w;
-      while (ok && it.next(P, w)) {
-        const TileCoord tc = decode_tile(P, w.t);
+      for_each_work(P, pair, num_pairs, [&](int t, int k0, int k1, int) -> bool {
+        const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
-        const int k1 = w.k1 < 0 ? d.num_k : w.k1;
-        if (k1 <= w.k0) continue;
+        const int kend = k1 < 0 ? d.num_k : k1;
+        if (kend <= k0) return true;
         const uint32_t b = acc % kAccBufs;
         const uint32_t acc_phase = (acc / kAccBufs) & 1u;
-        if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) break;
+        if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kAccCols;
-        for (int k = w.k0; k < k1; ++k) {
-          if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) {
-            ok = false;
-            break;
-          }
+        for (int k = k0; k < kend; ++k) {
+          if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) return false;
           tc_fence_after();
           const uint32_t sa = a_tile(stage);
           const uint32_t sb = b_tile(stage);
@@ -206,7 +196,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
             for (int hh = 0; hh < MH; ++hh) {
               const uint64_t ad = operand_desc<kBK>(sa + hh * L::kAHalfBytes, kk, d.a_mn);
               umma_bf16_pair(d_tmem + hh * kHalfCols, ad, bd, d.idesc,
-                             (k != w.k0 || kk != 0) ? 1u : 0u);
+                             (k != k0 || kk != 0) ? 1u : 0u);
             }
           }
           umma_commit_pair_mc(empty_bar(stage), 0x3);
@@ -215,10 +205,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
             phase ^= 1u;
           }
         }
-        if (!ok) break;
         umma_commit_pair_mc(tfull_bar(b), 0x3);
         ++acc;
-      }
+        return true;
+      });
       umma_commit_pair(mma_done_bar);
       wait_bounded(mma_done_bar, 0, tmo, abort_flag, kSiteDrainMma, false);
     }
@@ -228,32 +218,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int hh = (warp - epi_first_warp<MH, kSplit>()) >> 2;  // row half it drains
     uint32_t acc = 0;
-    WorkIter<MAXP> it(P, pair, num_pairs);
-    WorkItem w;
-    while (it.next(P, w)) {
-      const TileCoord tc = decode_tile(P, w.t);
+    for_each_work(P, pair, num_pairs, [&](int t, int k0, int k1, int kind) -> bool {
+      const TileCoord tc = decode_tile(P, t);
       const ProblemDesc& d = P.prob[tc.p];
       const int row =
           tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM + hh * 128 + q * 32 + lane;
       const int n0 = tc.n_blk * BN;
-      if ((w.k1 < 0 ? d.num_k : w.k1) <= w.k0) {
+      if ((k1 < 0 ? d.num_k : k1) <= k0) {
         if (row < d.M) store_zero_row(d, row, n0, BN);
-        continue;
+        return true;
       }
       const uint32_t b = acc % kAccBufs;
       const uint32_t acc_phase = (acc / kAccBufs) & 1u;
       int ok = 1;
       if (lane == 0) ok = wait_bounded(tfull_bar(b), acc_phase, tmo, abort_flag, kSiteEpiTmemFull);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
+      if (!ok) return false;
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      epilogue_item<BN>(P, d, w, pair, tc.m_blk * kTileM, n0, t_row, row,
+      epilogue_item<BN>(P, d, kind, pair, tc.m_blk * kTileM, n0, t_row, row,
                         leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), !leader,
                         2 * kEpiWarps * MH, abort_flag);
       ++acc;
-    }
+      return true;
+    });
   }
 
   tc_fence_before();
