@@ -498,6 +498,14 @@ size_t streamk_ws_bytes(const KernelConfig& c, int units) {
   return kStreamKFlagBytes + static_cast<size_t>(units) * c.bm * c.bn * 4;
 }
 
+// Zeroes the stream-K counters.  A one-block kernel on the GEMM's own stream
+// rather than cudaMemsetAsync: a memset can be carried out by a copy engine
+// and then queues behind large host<->device copies running on other
+// streams, which held each GEMM back in a copy-overlapped pipeline.
+__global__ void zero_counters_kernel(uint32_t* p, int n) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0u;
+}
+
 template <int MAXP>
 axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int units,
                                  const LaunchPlan& plan, cudaStream_t stream) {
@@ -513,7 +521,8 @@ axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int
   if (static_cast<size_t>(units) * 4 > kStreamKFlagBytes || !plan.ws ||
       plan.ws_bytes < streamk_ws_bytes(c, units) || (reinterpret_cast<uintptr_t>(plan.ws) & 255u) != 0)
     return AXONN_OK;
-  const cudaError_t e = cudaMemsetAsync(plan.ws, 0, static_cast<size_t>(units) * 4, stream);
+  zero_counters_kernel<<<1, 256, 0, stream>>>(static_cast<uint32_t*>(plan.ws), units);
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream-K counters: %s", cudaGetErrorString(e));
   P.sk_tiles = S;
   t_last_sk_tiles = S;
