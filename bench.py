@@ -161,8 +161,11 @@ def device_inputs(wl, layers, dev):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi sampling of SM clock and throttle reasons during a region.
+    Samples are timestamped; only those taken between entering and leaving
+    the `with` block count (the sampler starts before and stops after it, so
+    samples at either edge would see an idle GPU)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
@@ -171,19 +174,22 @@ class ClockSampler:
         self.proc = None
         self.gpu_index = gpu_index
         self.lines = []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu_index)],
+                 "-lms", "100", "-i", str(self.gpu_index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.3)
         except OSError:
             self.proc = None
+        self.t0 = time.time()
         return self
 
     def __exit__(self, *exc):
+        self.t1 = time.time()
         if self.proc is not None:
             time.sleep(0.25)
             self.proc.terminate()
@@ -196,23 +202,27 @@ class ClockSampler:
         return False
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
+        import datetime
+        rows = []
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-            for name, val in zip(self.NAMES, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
+        inside = [r for r in rows if self.t0 is not None and self.t0 <= r[0] <= self.t1]
+        use = inside or rows
+        if not use:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        reasons = {name for r in use for name, val in zip(self.NAMES, r[3])
+                   if val.lower().startswith("active")}
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": sorted(reasons),
+                "samples": len(use),
+                "window": "timed region" if inside else "whole sampler run (no sample fell inside)"}
 
 
 # ------------------------------------------------------------------ CPU oracle
