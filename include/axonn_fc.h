@@ -237,7 +237,7 @@ void axonn_last_choice(int* config, int* split, int* group_m);
  * axis.  Without it, it is nonzero for products that leave most SMs idle
  * (fewer 128x256 tiles than two waves), which may then split their
  * reduction range, and for products of more than one wave of 128x128 tiles,
- * which may run a stream-K tail (see axonn_set_streamk; up to about 40 MB on
+ * which may run a stream-K tail (see axonn_set_streamk; up to about 80 MB on
  * a 152-SM GPU).  Passing less workspace just disables either.
  * Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,

@@ -486,16 +486,16 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
 // is close to one tile (a partial round at most a quarter full) the offsets
 // stay close and the tail is faster.  Otherwise the lost L2 reuse can cost
 // more than the idle SMs it saves, so kStreamKShortTail applies it only in
-// the first case.  A tile is cut into at most two pieces;
-// the piece holding its first steps adds the other's fp32 partial, so the
-// order of the sum is fixed by the shape and the unit count.  Workspace: a
-// block of kStreamKFlagBytes for the per-unit counters (zeroed here, in
-// stream order, before the launch) followed by one tile-sized fp32 slot per
-// unit.
-constexpr size_t kStreamKFlagBytes = 1024;  // up to 256 units
+// the first case.  A tile is cut into at most two pieces; whichever piece
+// finishes second adds the other's fp32 partial to its own accumulator.
+// Two fp32 terms sum alike in either order, so the result does not depend on
+// which finishes second, and no piece waits for another (see epilogue_item).
+// Workspace: a block of kStreamKFlagBytes for the counters (zeroed, in stream
+// order, before the launch) followed by two tile-sized fp32 slots per unit.
+constexpr size_t kStreamKFlagBytes = 16384;  // 16 counters per unit, up to 256 units
 thread_local int t_last_sk_tiles = 0;
 size_t streamk_ws_bytes(const KernelConfig& c, int units) {
-  return kStreamKFlagBytes + static_cast<size_t>(units) * c.bm * c.bn * 4;
+  return kStreamKFlagBytes + 2 * static_cast<size_t>(units) * c.bm * c.bn * 4;
 }
 
 // Zeroes the stream-K counters.  A one-block kernel on the GEMM's own stream
@@ -518,10 +518,11 @@ axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int
   const int nk = P.prob[0].num_k;
   const int S = T >= 2 * units ? units + T % units : T;
   if (nk < 2 || static_cast<int64_t>(S) * nk >= (int64_t{1} << 31)) return AXONN_OK;
-  if (static_cast<size_t>(units) * 4 > kStreamKFlagBytes || !plan.ws ||
+  const int counters = units * axonn::kSkCountersPerUnit;
+  if (static_cast<size_t>(counters) * 4 > kStreamKFlagBytes || !plan.ws ||
       plan.ws_bytes < streamk_ws_bytes(c, units) || (reinterpret_cast<uintptr_t>(plan.ws) & 255u) != 0)
     return AXONN_OK;
-  zero_counters_kernel<<<1, 256, 0, stream>>>(static_cast<uint32_t*>(plan.ws), units);
+  zero_counters_kernel<<<1, 256, 0, stream>>>(static_cast<uint32_t*>(plan.ws), counters);
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream-K counters: %s", cudaGetErrorString(e));
   P.sk_tiles = S;

@@ -103,15 +103,13 @@ struct GemmParams {
   // their sk_tiles * num_k reduction steps are cut into gridDim equal,
   // consecutive ranges, one per CTA (or CTA pair).  sk_tiles >= gridDim, so
   // a range covers at least one tile and each tile is cut into at most two
-  // pieces: a head (steps 0..k1) finished by unit g at the end of its range,
-  // and a tail (k1..num_k) done by unit g+1 at the start of its range.  The
-  // tail is written as an fp32 partial to slot g+1 and unit g+1's epilogue
-  // warps each add one to counter g+1; the head's epilogue waits for the
-  // counter, adds that partial to its own accumulator and stores the tile.
+  // pieces: a head (steps 0..k1) at the end of unit u's range and a tail
+  // (k1..num_k) at the start of unit u+1's.  How the two are summed is in
+  // epilogue_item.
   int32_t sk_tiles;
   int32_t sk_slot_floats;  // floats per partial slot (one tile)
-  float* sk_partials;      // gridDim slots (or one per CTA pair)
-  uint32_t* sk_flags;      // gridDim counters, zero at launch
+  float* sk_partials;      // 2 slots per unit (CTA or CTA pair)
+  uint32_t* sk_flags;      // kSkCountersPerUnit counters per unit, zero at launch
 };
 
 // Kinds of work item: a whole tile, or the head or tail piece of a stream-K
@@ -158,7 +156,6 @@ enum WaitSite : uint32_t {
   kSiteEpiTmemFull = 4,
   kSiteDrainLoads = 5,
   kSiteDrainMma = 6,
-  kSiteStreamK = 7,
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -183,25 +180,6 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     // tensor cores.  The limit and abort checks still run every poll.
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (honor_abort && *abort_flag) return false;
-    if (global_timer_ns() - t0 > timeout_ns) {
-      *abort_flag = 1;
-      record_timeout(site);
-      return false;
-    }
-  }
-}
-
-// Bounded wait until the counter at p reaches target (acquire), with the
-// same limit and abort rules as wait_bounded.
-__device__ __forceinline__ bool wait_counter(const uint32_t* p, uint32_t target,
-                                             uint64_t timeout_ns, volatile int* abort_flag,
-                                             uint32_t site) {
-  if (ld_acquire(p) >= target) return true;
-  const uint64_t t0 = global_timer_ns();
-  while (true) {
-    __nanosleep(128);
-    if (ld_acquire(p) >= target) return true;
-    if (*abort_flag) return false;
     if (global_timer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       record_timeout(site);
@@ -414,47 +392,86 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
   }
 }
 
-// Epilogue of one work item (see for_each_work) by one warp.  Whole tiles go to
-// the output.  A stream-K tail goes, in fp32, to partial slot `unit` (tile-
-// local rows and columns, BN floats a row) and then counts on counter
-// `unit`.  A stream-K head waits for counter `unit + 1` to reach
-// `flag_target` (every epilogue warp of that unit), adds slot `unit + 1` to
-// its accumulator and stores the tile.
+// Counters per unit for the stream-K pieces: one per epilogue warp of the
+// unit (up to 2 CTAs x 8 warps).
+constexpr int kSkCountersPerUnit = 16;
+
+// Epilogue of one work item (see for_each_work) by one warp, which owns 32
+// rows of the tile (its TMEM lane quarter of one row half).  Whole tiles go
+// to the output.  The two pieces of a stream-K tile never wait for each
+// other.  Each piece first stores its rows of the accumulator, in fp32, to
+// its own partial slot: the head in slot 2u+1 of its unit u, the tail in
+// slot 2(u+1) of the next unit.  TMEM stays held.  Then the warp adds one to
+// the counter of its rows (counter index: the head's unit, this warp's
+// place `warp_slot` in the unit).  The warp that finds the other piece
+// already counted adds the other piece's partial to its own accumulator
+// and stores the output rows.  Two fp32 terms sum to the same value in
+// either order, so the output does not depend on which piece comes second.
+// Co-residency of the units is not needed, so launches on other streams
+// cannot stall it.
 template <int BN, int MAXP>
 __device__ __forceinline__ void epilogue_item(const GemmParams<MAXP>& P, const ProblemDesc& d,
-                                              int kind, int unit, int tile_m0, int n0,
-                                              uint32_t t_row, int row, uint32_t tempty,
-                                              bool remote, uint32_t flag_target,
-                                              volatile int* abort_flag) {
+                                              int kind, int unit, int warp_slot, int tile_m0,
+                                              int n0, uint32_t t_row, int row, uint32_t tempty,
+                                              bool remote) {
   const int lane = threadIdx.x & 31;
   if (kind == kWhole) {
     drain_accumulator<BN>(d, t_row, row, n0, tempty, lane == 0, remote);
     return;
   }
-  ProblemDesc ds = d;
-  ds.fast_bf16 = 0;
+  const bool head = kind == kHead;
+  const int head_unit = head ? unit : unit - 1;
   const int64_t origin = static_cast<int64_t>(tile_m0) * BN + n0;
-  if (kind == kTail) {
-    ds.C = P.sk_partials + static_cast<int64_t>(unit) * P.sk_slot_floats - origin;
-    ds.ldc = BN;
-    ds.out_mode = kOutF32;
-    ds.red_count = 0;
-    drain_accumulator<BN>(ds, t_row, row, n0, tempty, lane == 0, remote);
-    __threadfence();
-    __syncwarp();
-    if (lane == 0) red_release_add(&P.sk_flags[unit], 1u);
-    return;
+  float* mine = P.sk_partials + static_cast<int64_t>(2 * unit + (head ? 1 : 0)) * P.sk_slot_floats;
+  const float* other =
+      P.sk_partials + static_cast<int64_t>(head ? 2 * (unit + 1) : 2 * (unit - 1) + 1) * P.sk_slot_floats;
+  // 1. this piece's rows, fp32, to its slot (tile-local, BN floats a row)
+  ProblemDesc dp = d;
+  dp.C = mine - origin;
+  dp.ldc = BN;
+  dp.out_mode = kOutF32;
+  dp.red_count = 0;
+  dp.fast_bf16 = 0;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    const int col0 = n0 + c * 32;
+    if (col0 >= d.N) break;
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(t_row + c * 32, r);
+    tmem_ld_wait();
+    if (row < d.M) store_chunk(dp, row, col0, r);
   }
-  int ok = 1;
-  if (lane == 0)
-    ok = wait_counter(&P.sk_flags[unit + 1], flag_target, P.timeout_ns, abort_flag, kSiteStreamK);
-  ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+  // 2. count this warp's rows as done; the second piece finishes them
+  __threadfence();
   __syncwarp();
-  ds.red_count = ok ? 1 : 0;
-  ds.red_src = P.sk_partials + static_cast<int64_t>(unit + 1) * P.sk_slot_floats - origin;
-  ds.red_ld = BN;
-  ds.red_stride = 0;
-  drain_accumulator<BN>(ds, t_row, row, n0, tempty, lane == 0, remote);
+  uint32_t before = 0;
+  if (lane == 0) before = atomicAdd(&P.sk_flags[head_unit * kSkCountersPerUnit + warp_slot], 1u);
+  before = __shfl_sync(0xFFFFFFFFu, before, 0);
+  __syncwarp();
+  if (before == 1u) {
+    __threadfence();
+    ProblemDesc ds = d;
+    ds.fast_bf16 = 0;
+    ds.red_count = 1;
+    ds.red_src = other - origin;
+    ds.red_ld = BN;
+    ds.red_stride = 0;
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      const int col0 = n0 + c * 32;
+      if (col0 >= d.N) break;
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c * 32, r);
+      tmem_ld_wait();
+      if (row < d.M) store_chunk(ds, row, col0, r);
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) {
+    if (remote) mbar_arrive_cluster(tempty);
+    else mbar_arrive(tempty);
+  }
 }
 
 template <int BN, int BK, int STAGES, int MH = 1>
@@ -681,8 +698,8 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      epilogue_item<BN>(P, d, kind, blockIdx.x, tc.m_blk * kTileM, n0, t_row, row, tempty_bar(b),
-                        false, kEpiWarps * MH, abort_flag);
+      epilogue_item<BN>(P, d, kind, blockIdx.x, warp - epi_first_warp<MH>(), tc.m_blk * kTileM, n0,
+                        t_row, row, tempty_bar(b), false);
       ++acc;
       return true;
     });

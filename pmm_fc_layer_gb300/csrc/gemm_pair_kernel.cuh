@@ -237,9 +237,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      epilogue_item<BN>(P, d, kind, pair, tc.m_blk * kTileM, n0, t_row, row,
-                        leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), !leader,
-                        2 * kEpiWarps * MH, abort_flag);
+      epilogue_item<BN>(P, d, kind, pair,
+                        static_cast<int>(rank) * kEpiWarps * MH + (warp - epi_first_warp<MH, kSplit>()),
+                        tc.m_blk * kTileM, n0, t_row, row,
+                        leader ? tempty_bar(b) : mapa_shared(tempty_bar(b), 0), !leader);
       ++acc;
       return true;
     });

@@ -203,3 +203,42 @@ def test_streamk_repeat_and_graph(cuda_lib):
     finally:
         cuda_lib.axonn_set_kernel_config(-1)
         cuda_lib.axonn_set_streamk(-1)
+
+
+def test_streamk_concurrent_streams(cuda_lib):
+    """Two stream-K products on two streams at once.  The two pieces of a
+    tile never wait for each other (the second to finish completes the
+    tile), so a launch does not need all of its CTAs resident together and
+    concurrent launches cannot stall each other."""
+    import torch
+    import fc_inputs
+    fc = cuda_lib
+    jobs = []
+    for op, seed in (("fwd", 66), ("dgrad", 67)):
+        T, K, N = SHAPES[op]
+        pn, qn = operand_names(op)
+        P = make_operand(pn, T, K, N, False, seed=seed, kind="int")
+        Q = make_operand(qn, T, K, N, False, seed=seed, kind="int")
+        want = oracle.bf16_rne(oracle.fc(op, P, Q)[0])
+        M, Nn = fc.out_shape(op, T, K, N)
+        out = torch.zeros((M, Nn), dtype=torch.bfloat16, device="cuda")
+        shape = fc.Shape(T, K, N)
+        ws = torch.empty(fc.axonn_fc_workspace_size(op, shape, 0), dtype=torch.uint8, device="cuda")
+        jobs.append((op, fc_inputs.as_torch_bf16(P, "cuda"), fc_inputs.as_torch_bf16(Q, "cuda"),
+                     out, shape, ws, want, torch.cuda.Stream()))
+    fc.axonn_set_kernel_config(5)
+    fc.axonn_set_streamk(1)
+    try:
+        torch.cuda.synchronize()
+        for _ in range(4):
+            for op, Pd, Qd, out, shape, ws, _, s in jobs:
+                fc.call(op, Pd, Qd, out, shape, 0, ws, stream=s)
+                assert fc.axonn_last_streamk_tiles() > 0
+        torch.cuda.synchronize()
+        for *_, s in jobs:
+            fc.axonn_sync_status(s)
+    finally:
+        fc.axonn_set_kernel_config(-1)
+        fc.axonn_set_streamk(-1)
+    for op, _, _, out, _, _, want, _ in jobs:
+        assert np.array_equal(host_bits(out), want), op
