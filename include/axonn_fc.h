@@ -292,10 +292,12 @@ int axonn_num_kernel_configs(void);
  * last partial round plus one full round are cut into equal ranges of
  * 64-deep reduction steps, one per CTA (or CTA pair).  Untuned calls use it
  * only when the partial round is at most a quarter full; the tuner times
- * off, that default and always-on, and keeps the fastest.  Each such tile is computed in at most
- * two pieces.  The piece that holds the tile's first steps adds the other's
- * fp32 partial (fixed order), so results are deterministic for a given
- * shape and GPU but may differ in the last bit from a call with it off.
+ * off, that default and always-on, and keeps the fastest.  Each such tile
+ * is computed in at most two pieces; the second to finish adds the other's
+ * fp32 partial (two terms, the same sum in either order), so results are
+ * deterministic for a given shape and GPU but may differ in the last bit
+ * from a call with it off.  No CTA waits for another, so concurrent
+ * launches cannot stall each other.
  * Not part of the source pages: it removes the idle SMs of the last wave.
  * AXONN_ERR_INVALID_ARG for another mode.  Host-only. */
 axonn_status_t axonn_set_streamk(int mode);
