@@ -90,14 +90,14 @@ DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 # workload (dram__bytes_read.sum + dram__bytes_write.sum over the 12 launches
 # of one tuned step; summary and command in profiles/).  It is reported only
 # while the kernel sources hash to the value the capture was taken with.
-TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "e0a31eaba0d7e796",
-           "bytes_per_step": (21970.5 + 2560.5) * 1e6, "launches_per_step": 12}
+TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "7d8adb47cd68c249",
+           "bytes_per_step": (22642.6 + 2701.6) * 1e6, "launches_per_step": 12}
 
 
 def kernel_sources_hash():
     import hashlib
     h = hashlib.sha256()
-    for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "ptx.cuh"):
+    for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "ptx.cuh", "kernel_instances.cuh"):
         with open(os.path.join(ROOT, "pmm_fc_layer_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -574,23 +574,30 @@ def run_ours(args):
         torch.cuda.synchronize()
         fc.axonn_sync_status(stream)
         e2e_ms = max_over_ranks(t0.elapsed_time(t1), dev)
-        # The same host<->device copies with no GEMMs: both directions at
-        # once, as in the pipeline.  Their time bounds the end-to-end rate.
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(h2d_stream)
-        d2h_stream.wait_event(c0)
-        for _ in range(e2e_steps):
-            for n in lnames:
-                with torch.cuda.stream(h2d_stream):
-                    for k, hb in hin[n].items():
-                        dbuf[n][k].copy_(hb, non_blocking=True)
-                with torch.cuda.stream(d2h_stream):
-                    for k, hb in hout[n].items():
-                        hb.copy_(dbuf[n][k], non_blocking=True)
-        h2d_stream.wait_stream(d2h_stream)
-        c1.record(h2d_stream)
-        torch.cuda.synchronize()
-        copies_ms = max_over_ranks(c0.elapsed_time(c1), dev)
+        # The same host<->device copies with no GEMMs, both directions at
+        # once as in the pipeline; their time bounds the end-to-end rate.
+        # Best of three passes of up to 3 steps (the link rate varies from
+        # pass to pass).
+        c_steps = min(3, e2e_steps)
+        best = None
+        for _ in range(3):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record(h2d_stream)
+            d2h_stream.wait_event(c0)
+            for _ in range(c_steps):
+                for n in lnames:
+                    with torch.cuda.stream(h2d_stream):
+                        for k, hb in hin[n].items():
+                            dbuf[n][k].copy_(hb, non_blocking=True)
+                    with torch.cuda.stream(d2h_stream):
+                        for k, hb in hout[n].items():
+                            hb.copy_(dbuf[n][k], non_blocking=True)
+            h2d_stream.wait_stream(d2h_stream)
+            c1.record(h2d_stream)
+            torch.cuda.synchronize()
+            ms = c0.elapsed_time(c1) / c_steps
+            best = ms if best is None else min(best, ms)
+        copies_ms = max_over_ranks(best, dev) * e2e_steps
 
     # Dense bf16 peak at the SM clock sampled during the timed region:
     # SMs x 8192 FLOP per clock per SM (tcgen05 kind::f16) x clock.
@@ -632,9 +639,12 @@ def run_ours(args):
                      "copies_only_ms_per_step": round(copies_ms / e2e_steps, 3),
                      "host_link_gbs": round((h2d_bytes + d2h_bytes) * e2e_steps
                                             / (copies_ms * 1e6), 1),
-                     "link_bound_value": round(world * flops_per_step * e2e_steps
-                                               / (max(copies_ms, elapsed_ms * e2e_steps
-                                                      / args.steps) * 1e9), 2)}
+                     # null when the copies alone measured slower than the
+                     # whole overlapped pipeline (a noisy copy measurement)
+                     "link_bound_value": (round(world * flops_per_step * e2e_steps
+                                                / (max(copies_ms, elapsed_ms * e2e_steps
+                                                       / args.steps) * 1e9), 2)
+                                          if copies_ms <= e2e_ms else None)}
                     if e2e_steps else None),
             "gpu_launches": launches,
             "tuned": not args.no_tune,

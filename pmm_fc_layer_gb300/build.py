@@ -42,17 +42,35 @@ def up_to_date() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile every .cu under csrc/ into one shared library; returns its path."""
+    """Compile every .cu under csrc/ (in parallel, one object each) and link
+    them into one shared library; returns its path."""
     if not force and up_to_date():
         return LIB_PATH
-    os.makedirs(os.path.dirname(LIB_PATH), exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC,
-           *_sources(), "-o", tmp]
-    if verbose:
-        print(" ".join(cmd))
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB_PATH)
+    out_dir = os.path.dirname(LIB_PATH)
+    os.makedirs(out_dir, exist_ok=True)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in _sources():
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc(), *NVCC_FLAGS, *extra_flags, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd))
+        procs.append(subprocess.Popen(cmd))
+        objs.append(obj)
+    failed = [p.args[-3] for p in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, f"nvcc -c {' '.join(failed)}")
+        tmp = LIB_PATH + tag
+        link = [nvcc(), *NVCC_FLAGS, *objs, "-o", tmp]
+        if verbose:
+            print(" ".join(link))
+        subprocess.check_call(link)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB_PATH
 
 

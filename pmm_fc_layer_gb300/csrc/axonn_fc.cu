@@ -20,7 +20,7 @@
 
 #include "axonn_fc.h"
 #include "gemm_kernel.cuh"
-#include "gemm_pair_kernel.cuh"
+#include "kernel_launch.h"
 
 namespace {
 
@@ -28,6 +28,10 @@ using axonn::GemmParams;
 using axonn::ProblemDesc;
 
 constexpr int kMaxProblems = 64;  // largest virtual grid Gx*Gy*Gz
+// The kernel parameter block holds a tensor-map pair per problem, so a
+// launch with few problems uses a smaller instantiation (less to copy per
+// launch): 1 problem, up to kFewProblems, or up to kMaxProblems.
+constexpr int kFewProblems = 8;
 
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_timeout_ns{4000000000ULL};
@@ -70,56 +74,11 @@ struct DeviceState {
   bool attrs_set = false;
 };
 
-constexpr int kPairStages = 6;   // 256 x 256 pair tiles, 32 KB stages
-constexpr int kPair2Stages = 4;  // 512 x 256 pair tiles, 48 KB stages
 // Per-device state lives in a fixed table so that pointers handed out stay
 // valid while other threads initialise other devices.
 constexpr int kMaxDevices = 64;
 std::mutex g_dev_mu;
 DeviceState g_devs[kMaxDevices];
-
-template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
-cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes);
-}
-
-template <int BN, int STAGES, int MAXP, int MH>
-cudaError_t set_pair_smem_attr() {
-  return cudaFuncSetAttribute(axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              axonn::PairSmemLayout<BN, STAGES, MH>::kBytes);
-}
-
-// The 12-warp kernels move registers between warpgroups (setmaxnreg); the
-// split adds up to exactly the launch allocation of kRegsAtLaunch per thread.
-// A build whose kernels were allocated fewer registers would make the
-// increase wait forever, so such a kernel is refused before any launch.
-template <typename K>
-cudaError_t check_split_regs(K kernel, bool* ok) {
-  cudaFuncAttributes a = {};
-  cudaError_t e = cudaFuncGetAttributes(&a, reinterpret_cast<const void*>(kernel));
-  if (e == cudaSuccess && a.numRegs != axonn::kRegsAtLaunch) *ok = false;
-  return e;
-}
-
-// Clusters of 2 that can be resident at once (SM pairs inside a GPC).
-int max_active_pairs(int sms) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * sms, 1, 1);
-  cfg.blockDim = dim3(axonn::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = axonn::PairSmemLayout<256, kPairStages, 1>::kBytes;
-  int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(
-      &n, reinterpret_cast<const void*>(&axonn::fc_gemm_tcgen05_pair_kernel<256, kPairStages, 1, 1>),
-      &cfg);
-  if (e != cudaSuccess || n <= 0) {
-    (void)cudaGetLastError();
-    n = sms / 2;
-  }
-  return n;
-}
 
 // Host threads that never touched the runtime have no current context, and
 // the driver call that encodes tensor maps needs one: make the current
@@ -147,39 +106,23 @@ axonn_status_t device_state(DeviceState** out) {
                   dev, major, minor);
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
-    cudaError_t es[] = {set_smem_attr<128, 64, 6, 1>(), set_smem_attr<128, 64, 6, 8>(),
-                        set_smem_attr<128, 64, 6, kMaxProblems>(),
-                        set_smem_attr<256, 64, 4, 1>(), set_smem_attr<256, 64, 4, 8>(),
-                        set_smem_attr<256, 64, 4, kMaxProblems>(),
-                        set_smem_attr<256, 64, 3, 1, 2>(), set_smem_attr<256, 64, 3, 8, 2>(),
-                        set_smem_attr<256, 64, 3, kMaxProblems, 2>(),
-                        set_smem_attr<192, 64, 5, 1>(), set_smem_attr<192, 64, 5, 8>(),
-                        set_smem_attr<192, 64, 5, kMaxProblems>(),
-                        set_smem_attr<192, 64, 4, 1, 2>(), set_smem_attr<192, 64, 4, 8, 2>(),
-                        set_smem_attr<192, 64, 4, kMaxProblems, 2>(),
-                        set_pair_smem_attr<256, kPairStages, 1, 1>(),
-                        set_pair_smem_attr<256, kPairStages, 8, 1>(),
-                        set_pair_smem_attr<256, kPairStages, kMaxProblems, 1>(),
-                        set_pair_smem_attr<256, kPair2Stages, 1, 2>(),
-                        set_pair_smem_attr<256, kPair2Stages, 8, 2>(),
-                        set_pair_smem_attr<256, kPair2Stages, kMaxProblems, 2>()};
+    bool split_ok = true;
+    const cudaError_t es[] = {axonn::kernels_init<1>(&split_ok),
+                              axonn::kernels_init<kFewProblems>(&split_ok),
+                              axonn::kernels_init<kMaxProblems>(&split_ok)};
     for (cudaError_t x : es)
       if (x != cudaSuccess)
-        return fail(AXONN_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(x));
-    bool split_ok = true;
-    cudaError_t rs[] = {
-        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, 1, 2>, &split_ok),
-        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, 8, 2>, &split_ok),
-        check_split_regs(axonn::fc_gemm_tcgen05_pair_kernel<256, kPair2Stages, kMaxProblems, 2>,
-                         &split_ok)};
-    for (cudaError_t x : rs)
-      if (x != cudaSuccess)
-        return fail(AXONN_ERR_CUDA, "cudaFuncGetAttributes: %s", cudaGetErrorString(x));
+        return fail(AXONN_ERR_CUDA, "kernel attributes: %s", cudaGetErrorString(x));
     if (!split_ok)
       return fail(AXONN_ERR_UNSUPPORTED,
                   "a 12-warp GEMM kernel was not built with %d registers per thread",
                   axonn::kRegsAtLaunch);
-    d.max_pairs = max_active_pairs(d.sms);
+    int clusters = 0;
+    if (axonn::pair_clusters_resident(d.sms, &clusters) != cudaSuccess || clusters <= 0) {
+      (void)cudaGetLastError();
+      clusters = d.sms / 2;
+    }
+    d.max_pairs = clusters;
     d.attrs_set = true;
   }
   *out = &d;
@@ -376,6 +319,7 @@ constexpr KernelConfig kConfigs[] = {
 // (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
 constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12, 1.2};
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
+static_assert(kNumConfigs == axonn::kKernelConfigs, "configuration table and kernel instantiations");
 std::atomic<int> g_forced_config{-1};
 thread_local int t_last_config = -1;
 
@@ -533,56 +477,22 @@ axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int
   return AXONN_OK;
 }
 
-template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
-axonn_status_t launch_single(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
-                             cudaStream_t stream) {
-  GemmParams<MAXP> P;
-  axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
-  if (st != AXONN_OK || P.num_problems == 0) return st;
-  const int grid = P.total_tiles < dev.sms ? P.total_tiles : dev.sms;
-  st = configure_streamk(P, kConfigs[plan.config], grid, plan, stream);
-  if (st != AXONN_OK) return st;
-  axonn::fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>
-      <<<grid, axonn::cta_threads<MH>(), axonn::SmemLayout<BN, BK, STAGES, MH>::kBytes, stream>>>(P);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
-  return AXONN_OK;
-}
-
-template <int BN, int STAGES, int MAXP, int MH>
-axonn_status_t launch_pair(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
-                           cudaStream_t stream) {
-  GemmParams<MAXP> P;
-  axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[plan.config], plan.group_m);
-  if (st != AXONN_OK || P.num_problems == 0) return st;
-  const int pairs = P.total_tiles < dev.max_pairs ? P.total_tiles : dev.max_pairs;
-  st = configure_streamk(P, kConfigs[plan.config], pairs, plan, stream);
-  if (st != AXONN_OK) return st;
-  axonn::fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
-      <<<2 * pairs, axonn::cta_threads<MH, MH == 2>(), axonn::PairSmemLayout<BN, STAGES, MH>::kBytes,
-         stream>>>(P);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM pair launch: %s", cudaGetErrorString(e));
-  return AXONN_OK;
-}
-
-// The kernel parameter block holds a tensor-map pair per problem, so a
-// launch with few problems uses a smaller instantiation (less to copy per
-// launch): 1 problem, up to kFewProblems, or up to kMaxProblems.
-constexpr int kFewProblems = 8;
-
+// One launch of configuration `config` over the plan's blocks: the
+// persistent grid is one unit (CTA, or CTA pair) per resident slot, or one
+// per tile when there are fewer tiles.
 template <int P1>
 axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
                           const DeviceState& dev, cudaStream_t stream) {
-  switch (config) {
-    case 0: return launch_single<128, 64, 6, P1>(v, plan, dev, stream);
-    case 1: return launch_single<256, 64, 4, P1>(v, plan, dev, stream);
-    case 3: return launch_single<256, 64, 3, P1, 2>(v, plan, dev, stream);
-    case 4: return launch_single<192, 64, 5, P1>(v, plan, dev, stream);
-    case 5: return launch_single<192, 64, 4, P1, 2>(v, plan, dev, stream);
-    case 6: return launch_pair<256, kPair2Stages, P1, 2>(v, plan, dev, stream);
-    default: return launch_pair<256, kPairStages, P1, 1>(v, plan, dev, stream);
-  }
+  GemmParams<P1> P;
+  axonn_status_t st = fill_params(P, v, plan.blocks, kConfigs[config], plan.group_m);
+  if (st != AXONN_OK || P.num_problems == 0) return st;
+  const int slots = kConfigs[config].pair ? dev.max_pairs : dev.sms;
+  const int units = P.total_tiles < slots ? P.total_tiles : slots;
+  st = configure_streamk(P, kConfigs[config], units, plan, stream);
+  if (st != AXONN_OK) return st;
+  const cudaError_t e = axonn::kernels_launch<P1>(config, P, units, stream);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
+  return AXONN_OK;
 }
 
 axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, const DeviceState& dev,
@@ -1419,14 +1329,14 @@ axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail) {
   if (detail) *detail = 0;
   cudaError_t e = cudaStreamSynchronize(stream);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
-  unsigned long long word = 0;
-  e = cudaMemcpyFromSymbolAsync(&word, axonn::g_status_word, sizeof(word), 0, cudaMemcpyDeviceToHost, stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  // One error word per kernel translation unit; report the first set.
+  unsigned long long word = 0, w1 = 0, w8 = 0, w64 = 0;
+  e = axonn::kernels_take_status<1>(&w1, stream);
+  if (e == cudaSuccess) e = axonn::kernels_take_status<kFewProblems>(&w8, stream);
+  if (e == cudaSuccess) e = axonn::kernels_take_status<kMaxProblems>(&w64, stream);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  word = w1 ? w1 : (w8 ? w8 : w64);
   if (word == 0) return ok();
-  const unsigned long long zero = 0;
-  e = cudaMemcpyToSymbolAsync(axonn::g_status_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
-  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
   if (detail) *detail = word;
   return fail(AXONN_ERR_TIMEOUT, "device wait expired: CTA %llu, site %llu", (word >> 8) & 0xFFFFFFull,
               word & 0xFFull);

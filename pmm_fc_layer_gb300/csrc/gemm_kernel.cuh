@@ -146,7 +146,9 @@ __device__ __forceinline__ void for_each_work(const GemmParams<MAXP>& P, int u, 
 }
 
 // Device-side error word: 0 = no error.  Layout of a timeout record:
-// bits 32..39 = 0x7E, bits 8..31 = CTA index, bits 0..7 = wait site.
+// bits 32..39 = 0x7E, bits 8..31 = CTA index, bits 0..7 = wait site.  Each
+// translation unit that instantiates kernels has its own copy (no
+// relocatable device code); the host reads them through kernels_take_status.
 __device__ unsigned long long g_status_word;
 
 enum WaitSite : uint32_t {

@@ -1,0 +1,103 @@
+// Definitions behind kernel_launch.h, instantiated once per MAXP by the
+// kernels_p*.cu translation units.
+#pragma once
+#include "gemm_pair_kernel.cuh"
+#include "kernel_launch.h"
+
+namespace axonn {
+
+constexpr int kPairStages = 6;   // 256 x 256 pair tiles, 32 KB stages
+constexpr int kPair2Stages = 4;  // 512 x 256 pair tiles, 48 KB stages
+
+template <int BN, int BK, int STAGES, int MAXP, int MH>
+struct Single {
+  static cudaError_t init() {
+    return cudaFuncSetAttribute(fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                SmemLayout<BN, BK, STAGES, MH>::kBytes);
+  }
+  static cudaError_t launch(const GemmParams<MAXP>& P, int ctas, cudaStream_t s) {
+    fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>
+        <<<ctas, cta_threads<MH>(), SmemLayout<BN, BK, STAGES, MH>::kBytes, s>>>(P);
+    return cudaGetLastError();
+  }
+};
+
+template <int BN, int STAGES, int MAXP, int MH>
+struct Pair {
+  static cudaError_t init() {
+    return cudaFuncSetAttribute(fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                PairSmemLayout<BN, STAGES, MH>::kBytes);
+  }
+  // The 12-warp (register split) variant must have exactly the launch
+  // allocation its split adds up to: fewer registers per thread would make
+  // the epilogue's setmaxnreg increase wait forever.
+  static cudaError_t check_regs(bool* ok) {
+    if (MH != 2) return cudaSuccess;
+    cudaFuncAttributes a = {};
+    const cudaError_t e = cudaFuncGetAttributes(
+        &a, reinterpret_cast<const void*>(fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>));
+    if (e == cudaSuccess && a.numRegs != kRegsAtLaunch) *ok = false;
+    return e;
+  }
+  static cudaError_t launch(const GemmParams<MAXP>& P, int pairs, cudaStream_t s) {
+    fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
+        <<<2 * pairs, cta_threads<MH, MH == 2>(), PairSmemLayout<BN, STAGES, MH>::kBytes, s>>>(P);
+    return cudaGetLastError();
+  }
+};
+
+template <int MAXP>
+using C0 = Single<128, 64, 6, MAXP, 1>;
+template <int MAXP>
+using C1 = Single<256, 64, 4, MAXP, 1>;
+template <int MAXP>
+using C2 = Pair<256, kPairStages, MAXP, 1>;
+template <int MAXP>
+using C3 = Single<256, 64, 3, MAXP, 2>;
+template <int MAXP>
+using C4 = Single<192, 64, 5, MAXP, 1>;
+template <int MAXP>
+using C5 = Single<192, 64, 4, MAXP, 2>;
+template <int MAXP>
+using C6 = Pair<256, kPair2Stages, MAXP, 2>;
+
+template <int MAXP>
+cudaError_t kernels_init(bool* split_ok) {
+  const cudaError_t es[] = {C0<MAXP>::init(), C1<MAXP>::init(), C2<MAXP>::init(),
+                            C3<MAXP>::init(), C4<MAXP>::init(), C5<MAXP>::init(),
+                            C6<MAXP>::init(), C6<MAXP>::check_regs(split_ok)};
+  for (cudaError_t e : es)
+    if (e != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+template <int MAXP>
+cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, cudaStream_t s) {
+  switch (config) {
+    case 0: return C0<MAXP>::launch(P, units, s);
+    case 1: return C1<MAXP>::launch(P, units, s);
+    case 2: return C2<MAXP>::launch(P, units, s);
+    case 3: return C3<MAXP>::launch(P, units, s);
+    case 4: return C4<MAXP>::launch(P, units, s);
+    case 5: return C5<MAXP>::launch(P, units, s);
+    case 6: return C6<MAXP>::launch(P, units, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <int MAXP>
+cudaError_t kernels_take_status(unsigned long long* word, cudaStream_t stream) {
+  *word = 0;
+  cudaError_t e = cudaMemcpyFromSymbolAsync(word, g_status_word, sizeof(*word), 0,
+                                            cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess || *word == 0) return e;
+  const unsigned long long zero = 0;
+  e = cudaMemcpyToSymbolAsync(g_status_word, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e;
+}
+
+}  // namespace axonn
