@@ -32,7 +32,6 @@ namespace axonn {
 
 constexpr int kBM = 128;       // rows of one UMMA (cta_group::1)
 constexpr int kBK = 64;        // reduction depth per stage of the CTA-pair kernel
-constexpr int kThreads = 192;  // 6 warps: producer, MMA issuer, 4 epilogue
 constexpr int kEpiWarps = 4;
 
 // A CTA may own MH row halves of 128 (an MH*128 x BN tile).  Warp roles:
