@@ -90,8 +90,8 @@ DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 # workload (dram__bytes_read.sum + dram__bytes_write.sum over the 12 launches
 # of one tuned step; summary and command in profiles/).  It is reported only
 # while the kernel sources hash to the value the capture was taken with.
-TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "890a7995f617088f",
-           "bytes_per_step": (22338.3 + 2647.2) * 1e6, "launches_per_step": 12}
+TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "2907ff51f8c8408e",
+           "bytes_per_step": (25399.0 + 2778.7) * 1e6, "launches_per_step": 12}
 
 
 def kernel_sources_hash():
@@ -265,8 +265,10 @@ def cpu_baseline(data, glist, gpu_rows=None):
     return out
 
 
-def config_block(wl, name, world):
+def config_block(wl, name, world, output=None):
     cfg = {"workload": f"{name}: {wl['desc']}"}
+    if output:
+        cfg["output"] = output
     if wl.get("batch"):
         cfg.update(global_batch=wl["batch"] * world, seq_len=wl["seq"])
     cfg["grid"] = "x".join(str(g) for g in wl.get("grid", (1, 1, 1)))
@@ -353,6 +355,11 @@ def run_ours(args):
     wl = WORKLOADS[args.workload]
     grid = wl.get("grid", (1, 1, 1))
     flags = fc.VGRID if grid != (1, 1, 1) else 0
+    if args.accum_f32:
+        flags |= fc.ACCUM_F32
+    if args.order_free:
+        flags |= fc.REDUCE_ADD
+    out_dtype = torch.float32 if args.accum_f32 else torch.bfloat16
     only = tuple(args.only.split(":")) if args.only else None
     layers = [l for l in wl["layers"] if only is None or l[0] == only[0]]
     glist = [g for g in gemms(layers) if only is None or (g[0], g[1]) == only]
@@ -365,9 +372,9 @@ def run_ours(args):
         dbuf = {name: {k: fc_inputs.as_torch_bf16(v, dev) for k, v in data[name].items()}
                 for name in data}
     for name, T, K, N in layers:
-        dbuf[name]["Y"] = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
-        dbuf[name]["dX"] = torch.empty((T, K), dtype=torch.bfloat16, device=dev)
-        dbuf[name]["dW"] = torch.empty((K, N), dtype=torch.bfloat16, device=dev)
+        dbuf[name]["Y"] = torch.zeros((T, N), dtype=out_dtype, device=dev)
+        dbuf[name]["dX"] = torch.zeros((T, K), dtype=out_dtype, device=dev)
+        dbuf[name]["dW"] = torch.zeros((K, N), dtype=out_dtype, device=dev)
 
     plan = []
     ws_need = 0
@@ -376,13 +383,16 @@ def run_ours(args):
         ws_need = max(ws_need, fc.axonn_fc_workspace_size(op, shape, flags))
         plan.append(dict(name=name, op=op, flops=2.0 * m * n * r, mnr=(m, n, r),
                          P=dbuf[name][pn], Q=dbuf[name][qn], C=dbuf[name][cn], shape=shape,
-                         bytes=2.0 * (m * r + r * n + m * n)))
+                         bytes=2.0 * (m * r + r * n) + (8.0 if args.accum_f32 else 2.0) * m * n))
     ws = torch.empty(ws_need, dtype=torch.uint8, device=dev) if ws_need else None
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if wl.get("flush") else None
     stream = torch.cuda.Stream(device=dev)
     used = [None] * len(plan)
+    # the fixed-order virtual-grid sum is a second launch per GEMM whose
+    # reduced grid axis has more than one block; the order-free one is not
     reduce_launches = sum(1 for g in glist
-                          if flags and {"fwd": grid[0], "dgrad": grid[1], "wgrad": grid[2]}[g[1]] > 1)
+                          if (flags & fc.VGRID) and not (flags & fc.REDUCE_ADD)
+                          and {"fwd": grid[0], "dgrad": grid[1], "wgrad": grid[2]}[g[1]] > 1)
 
     sk_tiles = [0] * len(plan)
 
@@ -507,7 +517,7 @@ def run_ours(args):
 
     # end to end: host (pinned) -> device copies, the GEMMs, device -> host
     h2d_bytes = d2h_bytes = 0
-    io_bytes = sum(t.numel() * 2 for d in dbuf.values() for t in d.values())
+    io_bytes = sum(t.numel() * t.element_size() for d in dbuf.values() for t in d.values())
     e2e_steps = 0
     if not (args.no_e2e or only is not None or io_bytes > (24 << 30)):
         e2e_steps = max(1, min(args.steps, 10))
@@ -518,9 +528,9 @@ def run_ours(args):
         for k, hb in hin[name].items():
             hb.copy_(dbuf[name][k])
             h2d_bytes += hb.numel() * 2
-        hout[name] = {k: torch.empty(dbuf[name][k].shape, dtype=torch.bfloat16, pin_memory=True)
+        hout[name] = {k: torch.empty(dbuf[name][k].shape, dtype=out_dtype, pin_memory=True)
                       for k in ("Y", "dX", "dW")}
-        d2h_bytes += sum(hb.numel() * 2 for hb in hout[name].values())
+        d2h_bytes += sum(hb.numel() * hb.element_size() for hb in hout[name].values())
 
     # The host-buffer step is pipelined by layer on three streams: inputs of
     # layer l+1 go up while layer l's GEMMs run and layer l-1's outputs come
@@ -612,7 +622,13 @@ def run_ours(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": DATA if not wl.get("scale") else
             DATA.replace("activations/grads N(0,1), weights N(0,0.02)", "all operands N(0,1)*0.05"),
-            "config": config_block(wl, args.workload, world),
+            "config": config_block(
+                wl, args.workload, world,
+                output=None if not args.accum_f32 else
+                "fp32, every step adds its product into it (C += A.B)" + (
+                    "; grid partials added by atomics in one launch (order-free)"
+                    if args.order_free else "; grid partials summed in fixed order"
+                    if grid != (1, 1, 1) else "")),
             "per_gemm": per,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                          "peak": peaks["sustained"], "unit": "TFLOP/s",
@@ -620,7 +636,10 @@ def run_ours(args):
                          "frac_of_burst": round(achieved / peaks["burst"], 4),
                          "peak_source": f"{peaks['source']} (sustained; burst {peaks['burst']})",
                          "kernel": "fc_gemm_tcgen05_kernel" + (
-                             " (+ vgrid_reduce_kernel inside each timed call)" if flags else ""),
+                             " (virtual grid: blocks added into the output by atomics, one "
+                             "launch per GEMM)" if flags & fc.REDUCE_ADD else
+                             " (virtual grid: two launches per GEMM, the partials summed in "
+                             "the second one's epilogue)" if flags & fc.VGRID else ""),
                          "traffic": (TRAFFIC["bytes_per_step"] / TRAFFIC["launches_per_step"]
                                      if args.workload == TRAFFIC["workload"] and only is None
                                      and kernel_sources_hash() == TRAFFIC["kernel_sources"]
@@ -657,6 +676,9 @@ def run_ours(args):
         }
         if only is not None:
             line["profile_case"] = f"{only[0]}:{only[1]} only"
+        elif data is not None and not args.no_cpu_baseline and args.accum_f32:
+            # accumulated outputs hold the sum of every step: no row check
+            line["cpu_baseline"] = cpu_baseline(data, glist)
         elif data is not None and not args.no_cpu_baseline:
             # the GPU's first output rows of every GEMM, as computed in the timed steps
             gpu_rows = {gi: g["C"][:CPU_STRIPE_ROWS].to(torch.float64).cpu().numpy()
@@ -773,11 +795,20 @@ def main():
     ap.add_argument("--tune-cache", default=None, metavar="PATH",
                     help="load tuned choices from PATH if it exists (no tuning), else tune "
                          "and save them there")
+    ap.add_argument("--accum-f32", action="store_true",
+                    help="fp32 outputs that every step adds into (the main-gradient form)")
+    ap.add_argument("--order-free", action="store_true",
+                    help="virtual grid with --accum-f32: blocks added into the output by "
+                         "atomics in one launch, instead of the fixed-order sum")
     ap.add_argument("--only", default=None, metavar="LAYER:OP",
                     help="time one GEMM (e.g. out:fwd) for profiling; not a bench line")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.order_free and not args.accum_f32:
+        ap.error("--order-free needs --accum-f32")
+    if args.order_free and "grid" not in WORKLOADS.get(args.workload, {}):
+        ap.error("--order-free needs a virtual-grid workload")
     if args.impl == "reference":
         return run_reference(args)
     if args.workload == "zsharded_h6144_2x2x2":

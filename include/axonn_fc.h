@@ -27,10 +27,18 @@
  * of G gets floor(U/G) units plus one if b < U mod G, blocks are contiguous
  * in order, and the last block is clipped at D (see axonn_block_range).
  *
- * Virtual grid (AXONN_VGRID).  All G_x*G_y*G_z block products run in one
- * launch on this GPU; the partials of the reduced axis are written in fp32
- * to the caller's workspace and summed in fixed order 0..G-1 by a second
- * kernel, which stands in for the all-reduce / reduce-scatter of the grid.
+ * Virtual grid (AXONN_VGRID).  All G_x*G_y*G_z block products run on this
+ * GPU, and an on-device sum over the reduced axis (G = G_x for fwd, G_y for
+ * dgrad, G_z for wgrad) stands in for the grid's all-reduce /
+ * reduce-scatter.  By default the sum has a fixed order: one launch writes
+ * the partials 0..G-2 in fp32 to the caller's workspace, and a second
+ * computes partial G-1, whose epilogue adds partials 0..G-1 in that order
+ * and writes the output, so results are the same on every run.  With
+ * AXONN_REDUCE_ADD (fp32 accumulating output only) all blocks run in one
+ * launch and each adds its tile into the output with fp32 atomic adds: no
+ * workspace, no second launch, and a summation order that can change from
+ * run to run (every order stays within the same error bound; integer-valued
+ * sums below 2^24 are exact in any order).
  *
  * Conventions for every entry point below.
  *  - Pointers are DEVICE pointers; the caller owns every buffer and the
@@ -95,6 +103,8 @@ typedef struct {
 #define AXONN_FULL_OPERANDS 0x10u /* block mode: pointers are full matrices */
 #define AXONN_OUT_F32 0x20u       /* output is fp32, overwritten */
 #define AXONN_ZSHARDED 0x40u      /* axonn_fc_workspace_size of axonn_fc_wgrad_zsharded */
+#define AXONN_REDUCE_ADD 0x80u    /* with AXONN_VGRID | AXONN_ACCUM_F32: partials added
+                                     into the output by atomics, one launch, no workspace */
 
 /*
  * Forward product Y = X . W of the layer, of block (x,y,z), or of the whole
@@ -109,7 +119,7 @@ typedef struct {
  *   with it they address the full matrices and the block is located by its
  *   offsets, its partial written at Y[Tz, Ny].
  *   ws / ws_bytes: device workspace, needed with AXONN_VGRID when G_x > 1
- *   (size from axonn_fc_workspace_size).  Otherwise optional: a full-size
+ *   and AXONN_REDUCE_ADD is not given (size from axonn_fc_workspace_size).  Otherwise optional: a full-size
  *   one enables the reduction split of small products and the stream-K
  *   tail of large ones; NULL / 0 runs without them.
  */
@@ -205,8 +215,9 @@ axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void*
  * records the fastest for later calls with the same op, sizes, grid, block
  * and flags on a GPU with the same SM count.  Arguments are those of the
  * op's entry point (op is an axonn_op_t); the caller's output is
- * overwritten (with AXONN_ACCUM_F32 the runs overwrite instead of adding,
- * so tune on a scratch output).  Not for use during stream capture.  Any
+ * overwritten (with AXONN_ACCUM_F32 the runs overwrite instead of adding;
+ * with AXONN_REDUCE_ADD as well they add, once per run: tune on a scratch
+ * output).  Not for use during stream capture.  Any
  * of the result pointers may be NULL.
  */
 axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int64_t ldp,
@@ -234,7 +245,7 @@ void axonn_last_choice(int* config, int* split, int* group_m);
 
 /* Workspace bytes an op needs with these flags (0 when none).  `op` is an
  * axonn_op_t.  With AXONN_VGRID it is the fp32 partials of the reduced grid
- * axis.  Without it, it is nonzero for products that leave most SMs idle
+ * axis (0 with AXONN_REDUCE_ADD).  Without it, it is nonzero for products that leave most SMs idle
  * (fewer 128x256 tiles than two waves), which may then split their
  * reduction range, and for products of more than one wave of 128x128 tiles,
  * which may run a stream-K tail (see axonn_set_streamk; up to about 80 MB on

@@ -23,6 +23,7 @@ VGRID = 0x8
 FULL_OPERANDS = 0x10
 OUT_F32 = 0x20
 ZSHARDED = 0x40
+REDUCE_ADD = 0x80
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]

@@ -189,7 +189,8 @@ void full_dims(int op, const axonn_fc_shape_t& s, int64_t* M, int64_t* N, int64_
 }
 
 constexpr uint32_t kKnownFlags = AXONN_A_T | AXONN_B_T | AXONN_ACCUM_F32 | AXONN_VGRID |
-                                 AXONN_FULL_OPERANDS | AXONN_OUT_F32 | AXONN_ZSHARDED;
+                                 AXONN_FULL_OPERANDS | AXONN_OUT_F32 | AXONN_ZSHARDED |
+                                 AXONN_REDUCE_ADD;
 
 axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
   if (op < AXONN_OP_FWD || op > AXONN_OP_WGRAD) return fail(AXONN_ERR_INVALID_ARG, "bad op %d", op);
@@ -197,6 +198,8 @@ axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
   if (flags & ~kKnownFlags) return fail(AXONN_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags & ~kKnownFlags);
   if ((flags & AXONN_ACCUM_F32) && (flags & AXONN_OUT_F32))
     return fail(AXONN_ERR_INVALID_ARG, "AXONN_ACCUM_F32 and AXONN_OUT_F32 are exclusive");
+  if ((flags & AXONN_REDUCE_ADD) && (flags & (AXONN_VGRID | AXONN_ACCUM_F32)) != (AXONN_VGRID | AXONN_ACCUM_F32))
+    return fail(AXONN_ERR_INVALID_ARG, "AXONN_REDUCE_ADD needs AXONN_VGRID and AXONN_ACCUM_F32");
   if (s->T < 0 || s->K < 0 || s->N < 0) return fail(AXONN_ERR_INVALID_ARG, "negative extent");
   const int64_t lim = (int64_t{1} << 31) - 256;
   if (s->T > lim || s->K > lim || s->N > lim) return fail(AXONN_ERR_UNSUPPORTED, "extent above 2^31");
@@ -213,7 +216,7 @@ axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
 }
 
 size_t vgrid_ws_bytes(int op, const axonn_fc_shape_t& s, uint32_t flags) {
-  if (!(flags & AXONN_VGRID)) return 0;
+  if (!(flags & AXONN_VGRID) || (flags & AXONN_REDUCE_ADD)) return 0;
   const int G = reduce_extent(op, s);
   if (G <= 1) return 0;
   int64_t M, N, R;
@@ -627,8 +630,12 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   }
   if (hM == 0 || hN == 0) return ok();
 
+  // With AXONN_REDUCE_ADD every block adds its product into the fp32 output
+  // with atomic adds, all in one launch: no partials, no workspace, and a
+  // summation order that varies from run to run.
+  const bool red_add = (flags & AXONN_REDUCE_ADD) != 0;
   const int G = reduce_extent(op, s);
-  const bool partials = vgrid && G > 1;
+  const bool partials = vgrid && G > 1 && !red_add;
   int64_t ldpart = 0;
   if (partials) {
     const size_t need = vgrid_ws_bytes(op, s, flags);
@@ -680,7 +687,7 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
           } else {
             b.C = v.C + celt * (br.s * ldc + bc.s);
             b.ldc = ldc;
-            b.out_mode = user_mode;
+            b.out_mode = red_add ? axonn::kOutF32Red : user_mode;
           }
           plan.blocks.push_back(b);
         }
@@ -1051,9 +1058,12 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   if (st != AXONN_OK) return st;
   const axonn_fc_shape_t& s = *shape;
   // Tuning runs the product many times: an accumulating call is timed as an
-  // overwriting one (the caller's output is overwritten either way).
+  // overwriting one (the caller's output is overwritten either way), except
+  // with AXONN_REDUCE_ADD, whose atomic epilogue only adds: those runs add
+  // into the output again and again.
   const uint32_t run_flags =
-      (flags & AXONN_ACCUM_F32) ? ((flags & ~AXONN_ACCUM_F32) | AXONN_OUT_F32) : flags;
+      (flags & AXONN_ACCUM_F32) && !(flags & AXONN_REDUCE_ADD)
+          ? ((flags & ~AXONN_ACCUM_F32) | AXONN_OUT_F32) : flags;
   int64_t M, N, R;
   full_dims(op, s, &M, &N, &R);
   Range rows{0, M}, red{0, R}, cols{0, N};

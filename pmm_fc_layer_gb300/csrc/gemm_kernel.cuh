@@ -65,8 +65,11 @@ __device__ __forceinline__ void grow_registers() {
   if constexpr (MH == 2 && SPLIT) setmaxnreg_inc<kRegsEpilogue>();
 }
 
-// Output modes of the epilogue.
-enum OutMode : int32_t { kOutBF16 = 0, kOutF32 = 1, kOutF32Accum = 2 };
+// Output modes of the epilogue.  kOutF32Red adds the tile into an fp32
+// output with atomic adds, for products of which several write the same
+// output rows in one launch (the grid's partial products summed in no fixed
+// order).
+enum OutMode : int32_t { kOutBF16 = 0, kOutF32 = 1, kOutF32Accum = 2, kOutF32Red = 3 };
 
 struct ProblemDesc {
   void* C;            // output base (element (0,0) of this problem)
@@ -304,7 +307,20 @@ __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int c
   } else {
     float* out = reinterpret_cast<float*>(d.C) + row * d.ldc + col0;
     const bool acc = d.out_mode == kOutF32Accum;
-    if (ncols == 32 && !acc && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+    if (d.out_mode == kOutF32Red) {
+      // 16-byte vector reductions (row stride and column offset keep every
+      // 4-column group 16-byte aligned).  They return nothing, so the warp
+      // issues them and moves on; the L2 performs the adds.
+      if (ncols == 32) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+          red_add_v4_f32(out + 4 * v, r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncols) red_add_f32(out + j, r[j]);
+      }
+    } else if (ncols == 32 && !acc && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) st_global_v8(out + 8 * v, &r[8 * v]);
     } else if (ncols == 32) {

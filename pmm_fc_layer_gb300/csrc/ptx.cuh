@@ -112,6 +112,18 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
                : "memory");
 }
 
+// fp32 adds into global memory that return nothing (reductions, performed
+// at the L2): four consecutive floats, 16-byte aligned, or one float.
+__device__ __forceinline__ void red_add_v4_f32(float* p, uint32_t a, uint32_t b, uint32_t c,
+                                               uint32_t d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(a)),
+               "f"(__uint_as_float(b)), "f"(__uint_as_float(c)), "f"(__uint_as_float(d))
+               : "memory");
+}
+__device__ __forceinline__ void red_add_f32(float* p, uint32_t a) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(__uint_as_float(a)) : "memory");
+}
+
 // 3-D tiled bulk load (coordinates innermost first).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, uint32_t bar,
                                             int32_t c0, int32_t c1, int32_t c2) {

@@ -106,6 +106,11 @@ FAKE = 0x10000000  # never dereferenced: every case below fails validation
     (dict(shape=(64, 64, 64), C=FAKE + 4), 2),
     (dict(shape=(64, 64, 64), P=0), 1),
     (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x8), 4),
+    # the order-free sum needs the virtual grid and an accumulating fp32 output
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80 | 0x8), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80 | 0x4), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80 | 0x8 | 0x20), 1),
 ])
 def test_validation_errors(fc, case, expect):
     T, K, N = case["shape"]
@@ -124,6 +129,24 @@ def test_no_device_is_an_error_not_a_fallback(fc):
         pytest.skip("a GPU is present")
     st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, fc.Shape(64, 64, 64), 0)
     assert st in (fc.ERR_CUDA, fc.ERR_UNSUPPORTED)
+
+
+def test_reduce_add_needs_no_workspace(fc):
+    """The order-free virtual grid adds every block into the output: no
+    partials, so no workspace, and a call without one passes validation
+    (here it then fails for want of a GPU, not of workspace)."""
+    s = fc.Shape(64, 64, 64, (2, 2, 2))
+    f = fc.VGRID | fc.ACCUM_F32
+    for op in ("fwd", "dgrad", "wgrad"):
+        assert fc.axonn_fc_workspace_size(op, s, f) == 2 * 64 * 64 * 4
+        assert fc.axonn_fc_workspace_size(op, s, f | fc.REDUCE_ADD) == 0
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, s, f | fc.REDUCE_ADD)
+    assert st in (fc.ERR_CUDA, fc.ERR_UNSUPPORTED), fc.axonn_last_error()
+    st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, s, f)
+    assert st == fc.ERR_WORKSPACE
 
 
 def test_binding_refuses_missing_library(tmp_path):
