@@ -285,6 +285,10 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
+    import oracle
+    # Rank 0 runs alone on the host: every core, also where the launcher set
+    # OMP_NUM_THREADS=1 for each of its processes.
+    oracle.set_threads(os.cpu_count() or 1)
     wl = WORKLOADS[args.workload]
     if wl.get("device_inputs"):
         layers = wl["layers"][:: max(1, len(wl["layers"]) // 8)]
@@ -676,10 +680,10 @@ def run_ours(args):
         }
         if only is not None:
             line["profile_case"] = f"{only[0]}:{only[1]} only"
-        elif data is not None and not args.no_cpu_baseline and args.accum_f32:
+        elif data is not None and not args.no_cpu_baseline and world == 1 and args.accum_f32:
             # accumulated outputs hold the sum of every step: no row check
             line["cpu_baseline"] = cpu_baseline(data, glist)
-        elif data is not None and not args.no_cpu_baseline:
+        elif data is not None and not args.no_cpu_baseline and world == 1:
             # the GPU's first output rows of every GEMM, as computed in the timed steps
             gpu_rows = {gi: g["C"][:CPU_STRIPE_ROWS].to(torch.float64).cpu().numpy()
                         for gi, g in enumerate(plan)}

@@ -87,6 +87,8 @@ def _load():
                       lib.oracle_bf16_to_f64, lib.oracle_f64_to_bf16):
                 f.restype = None
             lib.oracle_max_threads.restype = ci
+            lib.oracle_set_threads.argtypes = [ci]
+            lib.oracle_set_threads.restype = ci
             _lib = lib
     return _lib
 
@@ -94,6 +96,12 @@ def _load():
 def max_threads() -> int:
     """OpenMP threads the oracle's loops use."""
     return int(_load().oracle_max_threads())
+
+
+def set_threads(n: int) -> int:
+    """Use `n` OpenMP threads in the oracle's loops from now on (calling
+    thread); returns the count in effect."""
+    return int(_load().oracle_set_threads(int(n)))
 
 
 # --------------------------------------------------------------------------

@@ -146,3 +146,16 @@ int oracle_max_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads for the calling thread's later parallel loops (n >= 1); returns
+ * the count now in effect.  A launcher that sets OMP_NUM_THREADS=1 for each
+ * of several processes leaves one process that wants every core. */
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+  extern void omp_set_num_threads(int);
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+  return oracle_max_threads();
+}

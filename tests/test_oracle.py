@@ -229,3 +229,20 @@ def test_wgrad_zsharded_is_the_vgrid_block_cut_in_shards(grid, xy):
     assert np.array_equal(oracle.gather_shards(Cs), full[Kx[0]:Kx[1], Ny[0]:Ny[1]])
     assert np.array_equal(oracle.gather_shards(Ss), Sfull[Kx[0]:Kx[1], Ny[0]:Ny[1]])
     assert len(Cs) == grid[2]
+
+
+def test_thread_count_setter_keeps_results():
+    """The oracle's thread count is a setting, not arithmetic: one thread and
+    all threads give the same bits."""
+    A = fc_inputs.normal_bf16((37, 29), 5, 1)
+    B = fc_inputs.normal_bf16((29, 41), 5, 2)
+    before = oracle.max_threads()
+    try:
+        assert oracle.set_threads(1) == 1
+        C1, S1 = oracle.gemm(A, False, B, False)
+        n = os.cpu_count() or 1
+        assert oracle.set_threads(n) == n
+        Cn, Sn = oracle.gemm(A, False, B, False)
+    finally:
+        oracle.set_threads(before)
+    assert np.array_equal(C1, Cn) and np.array_equal(S1, Sn)
