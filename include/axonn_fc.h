@@ -35,10 +35,12 @@
  * computes partial G-1, whose epilogue adds partials 0..G-1 in that order
  * and writes the output, so results are the same on every run.  With
  * AXONN_REDUCE_ADD (fp32 accumulating output only) all blocks run in one
- * launch and each adds its tile into the output with fp32 atomic adds: no
- * workspace, no second launch, and a summation order that can change from
- * run to run (every order stays within the same error bound; integer-valued
- * sums below 2^24 are exact in any order).
+ * launch and each adds its tile into the output with fp32 reduction adds
+ * (PTX red.global.add: rounded to nearest even, subnormal inputs and
+ * results flushed to zero): no workspace, no second launch, and a
+ * summation order that can change from run to run (every order stays
+ * within the same error bound; integer-valued sums below 2^24 are exact in
+ * any order).
  *
  * Conventions for every entry point below.
  *  - Pointers are DEVICE pointers; the caller owns every buffer and the
