@@ -81,7 +81,7 @@ typedef enum {
   AXONN_OK = 0,
   AXONN_ERR_INVALID_ARG = 1,  /* bad size, grid, coordinate, flag or pointer */
   AXONN_ERR_ALIGNMENT = 2,    /* pointer or leading dimension misaligned */
-  AXONN_ERR_UNSUPPORTED = 3,  /* valid request this build cannot run */
+  AXONN_ERR_UNSUPPORTED = 3,  /* valid request the library cannot run */
   AXONN_ERR_WORKSPACE = 4,    /* workspace missing or too small */
   AXONN_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed */
   AXONN_ERR_TIMEOUT = 6       /* a bounded device-side wait expired */
