@@ -90,8 +90,8 @@ DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 # workload (dram__bytes_read.sum + dram__bytes_write.sum over the 12 launches
 # of one tuned step; summary and command in profiles/).  It is reported only
 # while the kernel sources hash to the value the capture was taken with.
-TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "2907ff51f8c8408e",
-           "bytes_per_step": (25399.0 + 2778.7) * 1e6, "launches_per_step": 12}
+TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "b3d3f66be45e8d80",
+           "bytes_per_step": (20398.4 + 2697.9) * 1e6, "launches_per_step": 12}
 
 
 def kernel_sources_hash():
@@ -571,23 +571,29 @@ def run_ours(args):
         first["step"] = False
 
     e2e_ms = copies_ms = 0.0
+    e2e_pass_ms = []
     if e2e_steps:
-        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e2e_step()
         torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        t0.record(h2d_stream)
-        stream.wait_event(t0)
-        d2h_stream.wait_event(t0)
-        for _ in range(e2e_steps):
-            e2e_step()
-        h2d_stream.wait_stream(d2h_stream)
-        h2d_stream.wait_stream(stream)
-        t1.record(h2d_stream)
-        torch.cuda.synchronize()
+        # Two timed passes of e2e_steps steps; the faster one is reported and
+        # both are listed.  The steps are issued from the host as they go,
+        # so one stall of the host thread shows as a slow pass.
+        for _ in range(2):
+            if world > 1:
+                dist.barrier()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(h2d_stream)
+            stream.wait_event(t0)
+            d2h_stream.wait_event(t0)
+            for _ in range(e2e_steps):
+                e2e_step()
+            h2d_stream.wait_stream(d2h_stream)
+            h2d_stream.wait_stream(stream)
+            t1.record(h2d_stream)
+            torch.cuda.synchronize()
+            e2e_pass_ms.append(t0.elapsed_time(t1))
         fc.axonn_sync_status(stream)
-        e2e_ms = max_over_ranks(t0.elapsed_time(t1), dev)
+        e2e_ms = max_over_ranks(min(e2e_pass_ms), dev)
         # The same host<->device copies with no GEMMs, both directions at
         # once as in the pipeline; their time bounds the end-to-end rate.
         # Best of three passes of up to 3 steps (the link rate varies from
@@ -659,6 +665,8 @@ def run_ours(args):
                      "unit": UNIT, "h2d_bytes_per_step": h2d_bytes,
                      "d2h_bytes_per_step": d2h_bytes, "steps": e2e_steps,
                      "pipelining": "per-layer H2D / GEMM / D2H on three streams",
+                     "passes_ms_per_step": [round(x / e2e_steps, 3) for x in e2e_pass_ms],
+                     "pass_rule": "the faster of two timed passes",
                      "copies_only_ms_per_step": round(copies_ms / e2e_steps, 3),
                      "host_link_gbs": round((h2d_bytes + d2h_bytes) * e2e_steps
                                             / (copies_ms * 1e6), 1),

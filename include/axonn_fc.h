@@ -100,7 +100,9 @@ typedef struct {
 /* Flags (bitwise or). */
 #define AXONN_A_T 0x1u            /* first operand stored transposed */
 #define AXONN_B_T 0x2u            /* second operand stored transposed */
-#define AXONN_ACCUM_F32 0x4u      /* output is fp32 and the result is added */
+#define AXONN_ACCUM_F32 0x4u      /* output is fp32 and the result is added (one fp32
+                                     reduction add per element: round to nearest even,
+                                     subnormals flushed to zero) */
 #define AXONN_VGRID 0x8u          /* all blocks + on-device partial sum */
 #define AXONN_FULL_OPERANDS 0x10u /* block mode: pointers are full matrices */
 #define AXONN_OUT_F32 0x20u       /* output is fp32, overwritten */

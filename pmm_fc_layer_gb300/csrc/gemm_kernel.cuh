@@ -306,11 +306,14 @@ __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int c
     store_bf16_32(d, row, col0, pk);
   } else {
     float* out = reinterpret_cast<float*>(d.C) + row * d.ldc + col0;
-    const bool acc = d.out_mode == kOutF32Accum;
-    if (d.out_mode == kOutF32Red) {
+    if (d.out_mode == kOutF32Red || d.out_mode == kOutF32Accum) {
       // 16-byte vector reductions (row stride and column offset keep every
       // 4-column group 16-byte aligned).  They return nothing, so the warp
-      // issues them and moves on; the L2 performs the adds.
+      // issues them and moves on, and the L2 performs the adds: an
+      // accumulating tile never waits for the old output.  With one writer
+      // per element (kOutF32Accum) the result is the single rounded sum of
+      // the old value and the tile's, as a load-add-store would give (up to
+      // the reduction's flush of subnormals to zero).
       if (ncols == 32) {
 #pragma unroll
         for (int v = 0; v < 8; ++v)
@@ -320,27 +323,19 @@ __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int c
         for (int j = 0; j < 32; ++j)
           if (j < ncols) red_add_f32(out + j, r[j]);
       }
-    } else if (ncols == 32 && !acc && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
+    } else if (ncols == 32 && (reinterpret_cast<uintptr_t>(out) & 31u) == 0) {
 #pragma unroll
       for (int v = 0; v < 4; ++v) st_global_v8(out + 8 * v, &r[8 * v]);
     } else if (ncols == 32) {
 #pragma unroll
-      for (int v = 0; v < 8; ++v) {
-        float4 x = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                               __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-        if (acc) {
-          const float4 o = reinterpret_cast<const float4*>(out)[v];
-          x.x += o.x;
-          x.y += o.y;
-          x.z += o.z;
-          x.w += o.w;
-        }
-        reinterpret_cast<float4*>(out)[v] = x;
-      }
+      for (int v = 0; v < 8; ++v)
+        reinterpret_cast<float4*>(out)[v] =
+            make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                        __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (j < ncols) out[j] = __uint_as_float(r[j]) + (acc ? out[j] : 0.0f);
+        if (j < ncols) out[j] = __uint_as_float(r[j]);
     }
   }
 }
@@ -348,6 +343,8 @@ __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int c
 // Row of a tile whose reduction range is empty: the product is zero (plus
 // any partials to add).
 __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, int n0, int BN) {
+  // nothing to add into an accumulating output: leave it as it is
+  if ((d.out_mode == kOutF32Accum || d.out_mode == kOutF32Red) && d.red_count == 0) return;
   for (int col0 = n0; col0 < min(d.N, n0 + BN); col0 += 32) {
     uint32_t r[32];
 #pragma unroll

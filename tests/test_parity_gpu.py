@@ -172,6 +172,22 @@ def test_empty_reduction_writes_zeros(cuda_lib):
     assert torch.count_nonzero(out).item() == 0
 
 
+def test_empty_reduction_leaves_accumulated_output_unchanged(cuda_lib):
+    """K = 0 with an accumulating fp32 output adds nothing: every bit stays,
+    a subnormal and a negative zero included."""
+    import torch
+    T, N = 64, 40
+    out = torch.randn((T, N), generator=torch.Generator().manual_seed(9)).cuda()
+    out[0, 0] = 1e-40            # subnormal in fp32
+    out[1, 1] = -0.0
+    before = out.clone()
+    Xd = torch.empty((T, 8), dtype=torch.bfloat16, device="cuda")
+    Wd = torch.empty((8, N), dtype=torch.bfloat16, device="cuda")[:0]
+    cuda_lib.axonn_fc_fwd(Xd, Wd, out, cuda_lib.Shape(T, 0, N), cuda_lib.ACCUM_F32, ldx=8, ldw=40)
+    cuda_lib.axonn_sync_status()
+    assert torch.equal(out.view(torch.int32), before.view(torch.int32))
+
+
 def test_empty_output_is_noop(cuda_lib):
     import torch
     out = torch.full((4, 8), 5.0, dtype=torch.bfloat16, device="cuda")
