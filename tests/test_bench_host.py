@@ -1,0 +1,122 @@
+"""Host logic of the benchmark, on CPU: the reference arm's JSON line, the
+argument checks, the peak and clock bookkeeping, and the FLOP accounting
+that every reported rate divides."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(args, env=None, timeout=300):
+    e = dict(os.environ)
+    e.update(env or {})
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), *args], cwd=ROOT,
+                          env=e, capture_output=True, text=True, timeout=timeout)
+
+
+def test_reference_arm_prints_one_contract_line():
+    p = _run(["--impl", "reference", "--workload", "single_layer_t256", "--steps", "2",
+              "--warmup", "3"])
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference"
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert (d["steps"], d["warmup"], d["n_gpus"]) == (2, 3, 1)
+    assert d["higher_is_better"] is True and d["value"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
+    assert cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
+    assert d["config"]["workload"].startswith("single_layer_t256")
+
+
+def test_reference_arm_other_ranks_do_no_work():
+    p = _run(["--impl", "reference", "--workload", "single_layer_t256", "--steps", "2",
+              "--warmup", "3"], env={"RANK": "1", "WORLD_SIZE": "2"})
+    assert p.returncode == 0 and p.stdout.strip() == ""
+
+
+@pytest.mark.parametrize("args,msg", [
+    (["--warmup", "2"], "--warmup must be at least 3"),
+    (["--order-free"], "--order-free needs --accum-f32"),
+    (["--order-free", "--accum-f32"], "--order-free needs a virtual-grid workload"),
+])
+def test_argument_checks(args, msg):
+    p = _run(args)
+    assert p.returncode == 2 and msg in p.stderr
+
+
+def test_peaks_fallback_and_measured(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.read_peaks() == {"burst": 1900.0, "sustained": 1700.0, "hbm_gbs": 6800.0,
+                                  "source": "fallback"}
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1950.5}))
+    p = bench.read_peaks()
+    assert p["source"] == "measured" and p["burst"] == p["sustained"] == 1950.5
+    (tmp_path / "MEASURED_PEAKS.json").write_text(
+        json.dumps({"bf16_tflops": 1950.5, "bf16_tflops_sustained": 1720.0, "hbm_gbs": 7100}))
+    p = bench.read_peaks()
+    assert (p["burst"], p["sustained"], p["hbm_gbs"]) == (1950.5, 1720.0, 7100.0)
+    (tmp_path / "MEASURED_PEAKS.json").write_text("{not json")
+    assert bench.read_peaks()["source"] == "fallback"
+
+
+def test_clock_summary_keeps_the_timed_window():
+    import datetime
+    cs = bench.ClockSampler(0)
+    base = datetime.datetime(2026, 1, 2, 3, 4, 5)
+
+    def row(dt_s, mhz, cap):
+        ts = (base + datetime.timedelta(seconds=dt_s)).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+        return (f"{ts}, 0, {mhz}, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, "
+                f"{'Active' if cap else 'Not Active'}")
+
+    cs.lines = [row(0.0, 2070, False), row(1.0, 1500, True), row(1.1, 1520, True),
+                row(1.2, 1510, False), row(3.0, 2070, False), "garbage"]
+    cs.t0 = (base + datetime.timedelta(seconds=0.5)).timestamp()
+    cs.t1 = (base + datetime.timedelta(seconds=2.0)).timestamp()
+    s = cs.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1510 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["window"] == "timed region"
+    cs.t0 = cs.t1 = (base + datetime.timedelta(seconds=10)).timestamp()
+    assert bench.ClockSampler.summary(cs)["window"].startswith("whole sampler run")
+
+
+def test_gemm_flops_of_the_gpt_block():
+    """12 products; 2*M*N*R summed equals 3 ops x 2*T*K*N per layer, 22.27
+    TFLOP for H = 6144, T = 8192 (qkv, out, up, down)."""
+    wl = bench.WORKLOADS["gpt_h6144_t8192"]
+    g = bench.gemms(wl["layers"])
+    assert len(g) == 12
+    for name, op, T, K, N, M, Nc, R, _ in g:
+        assert (M, Nc, R) == {"fwd": (T, N, K), "dgrad": (T, K, N), "wgrad": (K, N, T)}[op]
+    flops = sum(2.0 * m * n * r for *_, m, n, r, _ in g)
+    closed = sum(3 * 2.0 * T * K * N for _, T, K, N in wl["layers"])
+    assert flops == closed
+    assert round(flops / 1e12, 2) == 22.27
+
+
+def test_config_block_labels():
+    c = bench.config_block(bench.WORKLOADS["gpt_h6144_t8192"], "gpt_h6144_t8192", 1)
+    assert c["l2"].startswith("operands exceed") and c["grid"] == "1x1x1"
+    assert (c["global_batch"], c["seq_len"], c["parallelism"]) == (4, 2048, "single GPU")
+    c = bench.config_block(bench.WORKLOADS["single_layer_t256"], "single_layer_t256", 2,
+                           output="fp32")
+    assert c["l2"].startswith("L2 flushed") and c["parallelism"] == "replicas x2"
+    assert c["output"] == "fp32" and c["global_batch"] == 2
+    c = bench.config_block(bench.WORKLOADS["gpt_h6144_t8192_vgrid_2x2x2"], "v", 1)
+    assert c["grid"] == "2x2x2"
+    assert bench.config_block(bench.WORKLOADS["layout_sweep"], "s", 1)["l2"].startswith("mixed")
