@@ -3,13 +3,12 @@
  *
  * What it computes.  The three matrix products of a fully-connected layer's
  * training step, either on the whole layer or on one local block of
- * Agarwal's 3D parallel matrix multiplication ("Parallelization of a matrix
- * multiply in an FC layer with Agarwal's 3D parallel matrix multiplication
- * algorithm ... G_x, G_y and G_z ... the three dimensions of the virtual grid
- * topology" -- Figure 1 caption, "Democratizing AI: Open-source Scalable LLM
- * Training on GPU-based Supercomputers"; the 4D grid G_data x G_x x G_y x G_z
- * with collectives is described under "What carries the argument" in the
- * pith.science review of arXiv 2502.08145):
+ * Agarwal's 3D parallel matrix multiplication.  Figure 1 of "Democratizing
+ * AI: Open-source Scalable LLM Training on GPU-based Supercomputers" shows
+ * one FC layer's matmul split this way over a virtual grid whose three
+ * extents are G_x, G_y and G_z; the pith.science review of arXiv
+ * 2502.08145 ("What carries the argument") places that grid inside a 4D
+ * one, G_data x G_x x G_y x G_z, joined by collectives:
  *
  *   forward          Y[T x N]  = X[T x K] . W[K x N]
  *   data gradient    dX[T x K] = dY[T x N] . W^T
@@ -150,9 +149,9 @@ axonn_status_t axonn_fc_wgrad(const void* X, const void* dY, void* dW, int64_t l
  * Z-sharded weights of the 3D grid.  Each rank (x, y, z) keeps only shard z
  * of its weight block W_{x,y}; the grid all-gathers the block over the Z
  * group before using it and reduce-scatters the weight-gradient partials
- * over the Z group into shards ("the weight matrix sharded along the Z axis
- * ... all-gather, reduce-scatter, and all-reduce collectives moving data" --
- * "What carries the argument", review of arXiv 2502.08145).  Shards are row
+ * over the Z group into shards (the review of arXiv 2502.08145, "What
+ * carries the argument", has the weights split over the Z axis and data
+ * moved by all-gather, reduce-scatter and all-reduce).  Shards are row
  * blocks of W_{x,y} cut by the grid's split rule (units of 8 rows, leading
  * shards take the extra unit; see axonn_block_range).
  *

@@ -7,11 +7,10 @@ thing both sides share is the seeded input generator in ``fc_inputs``.
 
 What it follows
 ---------------
-* The operation: "Parallelization of a matrix multiply in an FC layer with
-  Agarwal's 3D parallel matrix multiplication algorithm ... on eight GPUs
-  organized in a 2x2x2 topology" -- Figure 1 caption, "Democratizing AI:
-  Open-source Scalable LLM Training on GPU-based Supercomputers"
-  (sciencestack.ai page).  An FC layer's training step is three products:
+* The operation: Figure 1 of "Democratizing AI: Open-source Scalable LLM
+  Training on GPU-based Supercomputers" (sciencestack.ai page) splits the
+  matmul of one FC layer over eight GPUs in a 2x2x2 grid, by Agarwal's 3D
+  parallel matrix multiplication.  An FC layer's training step is three products:
   forward Y = X.W, data gradient dX = dY.W^T, weight gradient dW = X^T.dY.
 * The grid: GPUs form G_data x G_x x G_y x G_z; inside a data-parallel group
   the 3D scheme shards the matmul and moves data with all-gather,

@@ -5,9 +5,8 @@
  * this library.  It shares no code, header or constant with the GPU path.
  *
  * What it computes: the plain matrix product C = A . B that an FC layer's
- * forward and backward passes reduce to ("Parallelization of a matrix
- * multiply in an FC layer", Figure 1 caption of "Democratizing AI:
- * Open-source Scalable LLM Training on GPU-based Supercomputers").  Agarwal's
+ * forward and backward passes reduce to (Figure 1 caption of "Democratizing
+ * AI: Open-source Scalable LLM Training on GPU-based Supercomputers").  Agarwal's
  * 3D decomposition only reassigns which block of this sum each GPU computes,
  * so the exact result is the definition
  *     C[i][j] = sum_r A[i][r] * B[r][j]

@@ -1,11 +1,11 @@
 """Communication performance model of the 4D grid -- a CPU planning tool.
 
 Purpose: rank grid configurations G_data x G_x x G_y x G_z for a set of FC
-layers before running them, as the pages' performance model does ("The
-performance model (Section V-B) predicts communication times from analytical
-ring-collective formulas ... plus independently profiled bandwidths" and
-ranks 9 of the 10 fastest configurations correctly -- circularity check and
-Figure 2 caption of the pith.science review of arXiv 2502.08145).  The
+layers before running them, as the pages' performance model does.  The
+pith.science review of arXiv 2502.08145 (its circularity check, and the
+Figure 2 caption) says that model takes ring-collective formulas and
+separately measured bandwidths to predict communication time, and that it
+put 9 of the 10 fastest configurations in the right places.  The
 pages state its assumptions but not its equations, so this module writes the
 plainest model those assumptions fix; its parity with the pages' Equations
 1-7 cannot be checked (parity unpinned):
