@@ -37,7 +37,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["higher_is_better"] is True and d["value"] > 0
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
-    assert cb["sample"]
+    assert "whole" in cb["sample"]      # a 1.6 GFLOP step is computed in full
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
     assert d["config"]["workload"].startswith("single_layer_t256")
@@ -107,6 +107,13 @@ def test_gemm_flops_of_the_gpt_block():
     closed = sum(3 * 2.0 * T * K * N for _, T, K, N in wl["layers"])
     assert flops == closed
     assert round(flops / 1e12, 2) == 22.27
+
+
+def test_cpu_rows_whole_small_steps_stripe_large_ones():
+    small = bench.gemms(bench.WORKLOADS["single_layer_t256"]["layers"])
+    assert bench.cpu_rows(small) == 512          # every row of every GEMM
+    for w in ("gpt_h6144_t8192", "large_h16384_t4096", "layout_sweep"):
+        assert bench.cpu_rows(bench.gemms(bench.WORKLOADS[w]["layers"])) == bench.CPU_STRIPE_ROWS
 
 
 def test_config_block_labels():
