@@ -19,9 +19,10 @@ plainest model those assumptions fix; its parity with the pages' Equations
 * Intra-node bandwidths are measured per process-group size and looked up.
 
 Rank layout (not given on the pages; the plainest reading): ranks are
-numbered with x fastest, then y, then z, then the data-parallel index, so a
-group along an axis with stride s and size g stays inside one node when
-s * g divides the GPUs per node.
+numbered with x fastest, then y, then z, then the data-parallel index.  A
+group along an axis uses the intra-node bandwidth when every group along
+that axis lies inside one node (for power-of-two grids: when stride x size
+divides the GPUs per node).
 
 Per FC layer [K -> N] with T tokens per data-parallel group, block (x,y,z)
 holds X[T/Gz x K/Gx], W[K/Gx x N/Gy], dY[T/Gz x N/Gy]:
@@ -81,11 +82,28 @@ def axis_size(grid, axis: str) -> int:
     return {"x": gx, "y": gy, "z": gz, "data": gd}[axis]
 
 
-def group_bandwidth(grid, axis: str, m: Machine) -> float:
+def groups_within_nodes(grid, axis: str, gpus_per_node: int) -> bool:
+    """Whether every process group along `axis` lies inside one node.  The
+    group of first rank b holds b, b + s, ..., b + (g-1) s (stride s, size g),
+    and its first ranks are i + s g j with i < s.  b mod P (P = GPUs per
+    node) repeats with period at most P in both i and j, so P x P candidates
+    decide it."""
     size, stride = axis_size(grid, axis), axis_stride(grid, axis)
-    span = size * stride
-    if span <= m.gpus_per_node and m.gpus_per_node % span == 0:
-        return m.intra(size)
+    if size == 1:
+        return True
+    n = grid[0] * grid[1] * grid[2] * grid[3]
+    block = stride * size
+    P = gpus_per_node
+    for j in range(min(n // block, P)):
+        for i in range(min(stride, P)):
+            if (i + block * j) % P + (size - 1) * stride >= P:
+                return False
+    return True
+
+
+def group_bandwidth(grid, axis: str, m: Machine) -> float:
+    if groups_within_nodes(grid, axis, m.gpus_per_node):
+        return m.intra(axis_size(grid, axis))
     return float(m.inter_node_gbs)
 
 

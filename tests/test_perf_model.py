@@ -62,3 +62,83 @@ def test_rank_configs_enumerates_and_orders():
     # with a slow network the fastest grid keeps its 3D groups inside a node
     best = ranked[0][1]
     assert best[1] * best[2] * best[3] <= 8
+
+
+def _ring(p, chunks, mode):
+    """A literal ring on p ranks, each holding p chunks (numpy arrays).
+    reduce_scatter: after p-1 steps rank r holds the sum of chunk (r+1) % p.
+    all_gather: rank r starts with its own chunk (r+1) % p and ends with all.
+    Returns (per-rank data, bytes each rank sent)."""
+    import numpy as np
+    data = [[None if c is None else np.array(c, dtype=np.float64) for c in row] for row in chunks]
+    sent = [0] * p
+    for step in range(p - 1):
+        msgs = []
+        for r in range(p):
+            if mode == "reduce_scatter":
+                idx = (r - step) % p
+            else:
+                idx = (r + 1 - step) % p
+            msgs.append(((r + 1) % p, idx, data[r][idx].copy()))
+            sent[r] += data[r][idx].nbytes
+        for dst, idx, buf in msgs:
+            data[dst][idx] = data[dst][idx] + buf if mode == "reduce_scatter" else buf
+    return data, sent
+
+
+@pytest.mark.parametrize("p", [2, 3, 4, 8])
+def test_ring_cost_matches_a_simulated_ring(p):
+    """Assumption 1 pinned by simulation, not by the formula: a ring
+    reduce-scatter and all-gather of S bytes each send (p-1)/p * S bytes per
+    rank, and the all-reduce (one then the other) 2 (p-1)/p * S; the
+    simulated ring also yields the right sums."""
+    import numpy as np
+    rng = np.random.default_rng(p)
+    n = 6                                        # elements per chunk
+    x = rng.integers(-9, 9, size=(p, p, n)).astype(np.float64)   # rank, chunk, element
+    S = p * n * 8                                # bytes of one rank's tensor
+    rs, sent_rs = _ring(p, [[x[r, c] for c in range(p)] for r in range(p)], "reduce_scatter")
+    total = x.sum(axis=0)
+    for r in range(p):
+        assert np.array_equal(rs[r][(r + 1) % p], total[(r + 1) % p])
+    ag_in = [[rs[r][c] if c == (r + 1) % p else None for c in range(p)] for r in range(p)]
+    ag, sent_ag = _ring(p, ag_in, "all_gather")
+    for r in range(p):
+        assert np.array_equal(np.stack(ag[r]), total)          # all-reduce done
+    gbs = 1.0                                                  # 1 GB/s: seconds = bytes / 1e9
+    assert max(sent_rs) / 1e9 == pytest.approx(pm.ring_time("reduce_scatter", S, p, gbs))
+    assert max(sent_ag) / 1e9 == pytest.approx(pm.ring_time("all_gather", S, p, gbs))
+    assert (max(sent_rs) + max(sent_ag)) / 1e9 == pytest.approx(
+        pm.ring_time("all_reduce", S, p, gbs))
+
+
+@pytest.mark.parametrize("grid", [(2, 2, 2, 2), (1, 2, 4, 2), (4, 1, 1, 4), (1, 8, 1, 2),
+                                  (2, 1, 8, 1), (1, 1, 1, 16), (1, 3, 2, 1), (2, 3, 1, 1),
+                                  (1, 1, 3, 4), (3, 2, 2, 1), (1, 5, 1, 3), (1, 6, 2, 2)])
+def test_group_placement_by_enumeration(grid):
+    """Ranks numbered x fastest, then y, z, data; a group along an axis is the
+    ranks that share every other coordinate.  Enumerate the groups and check
+    that the model's choice of intra- or inter-node bandwidth is intra
+    exactly when every group lies within one node of 8."""
+    gd, gx, gy, gz = grid
+    ext = {"x": gx, "y": gy, "z": gz, "data": gd}
+    coords = {}
+    r = 0
+    for d in range(gd):
+        for z in range(gz):
+            for y in range(gy):
+                for x in range(gx):
+                    coords[r] = {"x": x, "y": y, "z": z, "data": d}
+                    r += 1
+    for axis in ("x", "y", "z", "data"):
+        groups = {}
+        for rank, c in coords.items():
+            key = tuple(v for a, v in sorted(c.items()) if a != axis)
+            groups.setdefault(key, []).append(rank)
+        assert all(len(g) == ext[axis] for g in groups.values())
+        one_node = all(len({rank // M.gpus_per_node for rank in g}) == 1
+                       for g in groups.values())
+        assert pm.groups_within_nodes(grid, axis, M.gpus_per_node) == one_node
+        if ext[axis] > 1:                        # a one-rank group moves nothing
+            bw = pm.group_bandwidth(grid, axis, M)
+            assert bw == (M.intra(ext[axis]) if one_node else M.inter_node_gbs)
