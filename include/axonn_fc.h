@@ -62,8 +62,8 @@
  *    guarded by locks.  The kernel-configuration override and the wait
  *    timeout are process-wide.
  *  - Empty outputs (an extent of 0) return AXONN_OK and touch nothing; an
- *    empty reduction range writes zeros (leaves C unchanged with
- *    AXONN_ACCUM_F32).
+ *    empty reduction range writes zeros (leaves C bit for bit unchanged
+ *    with AXONN_ACCUM_F32).
  */
 #ifndef AXONN_FC_H_
 #define AXONN_FC_H_
@@ -106,8 +106,9 @@ typedef struct {
 #define AXONN_FULL_OPERANDS 0x10u /* block mode: pointers are full matrices */
 #define AXONN_OUT_F32 0x20u       /* output is fp32, overwritten */
 #define AXONN_ZSHARDED 0x40u      /* axonn_fc_workspace_size of axonn_fc_wgrad_zsharded */
-#define AXONN_REDUCE_ADD 0x80u    /* with AXONN_VGRID | AXONN_ACCUM_F32: partials added
-                                     into the output by atomics, one launch, no workspace */
+#define AXONN_REDUCE_ADD 0x80u    /* with AXONN_VGRID | AXONN_ACCUM_F32: every block added
+                                     into the output by fp32 reduction adds, in no fixed
+                                     order; one launch, no workspace */
 
 /*
  * Forward product Y = X . W of the layer, of block (x,y,z), or of the whole
@@ -122,9 +123,10 @@ typedef struct {
  *   with it they address the full matrices and the block is located by its
  *   offsets, its partial written at Y[Tz, Ny].
  *   ws / ws_bytes: device workspace, needed with AXONN_VGRID when G_x > 1
- *   and AXONN_REDUCE_ADD is not given (size from axonn_fc_workspace_size).  Otherwise optional: a full-size
- *   one enables the reduction split of small products and the stream-K
- *   tail of large ones; NULL / 0 runs without them.
+ *   and AXONN_REDUCE_ADD is not given (size from
+ *   axonn_fc_workspace_size).  Otherwise optional: a full-size one enables
+ *   the reduction split of small products and the stream-K tail of large
+ *   ones; NULL / 0 runs without them.
  */
 axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw,
                             int64_t ldy, const axonn_fc_shape_t* shape, uint32_t flags,
