@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cstdarg>
+#include <cerrno>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -1246,6 +1247,26 @@ bool json_field(const std::string& line, const char* name, std::string* out) {
 }
 }  // namespace
 
+}  // extern "C"
+
+namespace {
+// A whole decimal integer in [lo, hi] (no trailing characters).
+bool parse_int(const std::string& text, long lo, long hi, int* out) {
+  if (text.empty()) return false;
+  char* end = nullptr;
+  errno = 0;
+  const long v = strtol(text.c_str(), &end, 10);
+  if (errno != 0 || end == text.c_str() || *end != '\0' || v < lo || v > hi) return false;
+  *out = static_cast<int>(v);
+  return true;
+}
+// Rasterisation groups the kernels take: at most 64 tile rows or columns
+// (the tuner writes 8 and 16); larger values would overflow the tile walk.
+constexpr long kMaxGroup = 64;
+}  // namespace
+
+extern "C" {
+
 axonn_status_t axonn_tune_cache_load(const char* path) {
   if (!path) return fail(AXONN_ERR_INVALID_ARG, "path is NULL");
   std::ifstream f(path);
@@ -1265,14 +1286,13 @@ axonn_status_t axonn_tune_cache_load(const char* path) {
     e.choice.config = -1;
     for (int c = 0; c < kNumConfigs; ++c)
       if (cfg == kConfigs[c].name) e.choice.config = c;
-    e.choice.split = atoi(split.c_str());
-    e.choice.group_m = atoi(gm.c_str());
     std::string sk;
-    if (json_field(line, "streamk", &sk)) e.choice.streamk = atoi(sk.c_str());
-    e.us = atof(us.c_str());
-    if (e.choice.config < 0 || e.choice.split < 1 || e.choice.split > kMaxSplit || e.choice.group_m == 0 ||
-        e.choice.streamk < kStreamKOff || e.choice.streamk > kStreamKAlways)
+    const bool has_sk = json_field(line, "streamk", &sk);
+    if (e.choice.config < 0 || !parse_int(split, 1, kMaxSplit, &e.choice.split) ||
+        !parse_int(gm, -kMaxGroup, kMaxGroup, &e.choice.group_m) || e.choice.group_m == 0 ||
+        (has_sk && !parse_int(sk, kStreamKOff, kStreamKAlways, &e.choice.streamk)))
       return fail(AXONN_ERR_INVALID_ARG, "%s:%d: unknown configuration", path, lineno);
+    e.us = atof(us.c_str());
     loaded[key] = e;
   }
   std::lock_guard<std::mutex> lk(g_tune_mu);

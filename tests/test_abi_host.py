@@ -192,6 +192,27 @@ def test_tune_cache_roundtrip(fc, tmp_path):
                    '"streamk": 3, "us": 1}\n')
     with pytest.raises(fc.AxonnError):
         fc.axonn_tune_cache_load(str(bad))
+    # integers are whole and in range: rasterisation groups of at most 64
+    # (a larger one would overflow the kernel's tile walk), splits 1..8
+    for field in ('"group_m": 100000', '"group_m": -65', '"group_m": 0', '"group_m": "8x"',
+                  '"group_m": 8.5', '"split": 0', '"split": 9', '"split": 99999999999999999999',
+                  '"streamk": -1', '"streamk": "1 "'):
+        entry = {"key": "x", "config": "pair_512x256", "split": 1, "group_m": 8, "streamk": 1,
+                 "us": 1}
+        name = field.split(":")[0].strip('"')
+        line = json.dumps(entry).replace(f'"{name}": {json.dumps(entry[name])}', field)
+        assert field in line
+        bad.write_text(line + "\n")
+        with pytest.raises(fc.AxonnError):
+            fc.axonn_tune_cache_load(str(bad))
+    ok_line = {"key": "y", "config": "pair_512x256", "split": 8, "group_m": -64, "streamk": 2,
+               "us": 1}
+    good = tmp_path / "edge.jsonl"
+    good.write_text(json.dumps(ok_line) + "\n")
+    fc.axonn_tune_cache_load(str(good))
+    assert fc.axonn_tune_cache_size() == 4
+    fc.axonn_tune_cache_clear()
+    fc.axonn_tune_cache_load(str(src))
     with pytest.raises(fc.AxonnError):
         fc.axonn_tune_cache_load(str(tmp_path / "absent.jsonl"))
     assert fc.axonn_tune_cache_size() == 3
