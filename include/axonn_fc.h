@@ -234,8 +234,10 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
 /* The tuning table as text, one JSON object per line:
  *   {"key": "...", "config": "<name>", "split": S, "group_m": G,
  *    "streamk": 0 | 1 | 2, "us": t}
- * (streamk: off, on for a partial round at most a quarter full, on wherever
- * it applies; a line without it loads as 1).
+ * (S a whole number 1..8; G a whole number in -64..-1 or 1..64, tile rows
+ * per rasterisation group, negative for tile columns; streamk: off, on for
+ * a partial round at most a quarter full, on wherever it applies; a line
+ * without it loads as 1).
  * save writes every entry; load merges a file's entries into the table
  * (AXONN_ERR_INVALID_ARG on an unreadable file or a malformed line, leaving
  * the table unchanged).  Host-only. */
