@@ -246,3 +246,29 @@ def test_thread_count_setter_keeps_results():
     finally:
         oracle.set_threads(before)
     assert np.array_equal(C1, Cn) and np.array_equal(S1, Sn)
+
+
+@pytest.mark.parametrize("T,K,N", [(1, 1, 1), (5, 7, 3), (16, 9, 12)])
+def test_op_equivalences_through_transposed_copies(T, K, N):
+    """dgrad(dY, W) = fwd(dY, W^T) and wgrad(X, dY) = fwd(X^T, dY), with the
+    transposes made as explicit copies (the other addressing path); and
+    each op with its operands stored transposed (flags) equals the op on the
+    plain layout."""
+    X = fc_inputs.normal_bf16((T, K), 21, 1)
+    W = fc_inputs.normal_bf16((K, N), 21, 2)
+    dY = fc_inputs.normal_bf16((T, N), 21, 3)
+    Wt = np.ascontiguousarray(W.T)
+    Xt = np.ascontiguousarray(X.T)
+    dYt = np.ascontiguousarray(dY.T)
+    dx, sdx = oracle.fc("dgrad", dY, W)
+    dx2, sdx2 = oracle.fc("fwd", dY, Wt)
+    assert np.array_equal(dx, dx2) and np.array_equal(sdx, sdx2)
+    dw, sdw = oracle.fc("wgrad", X, dY)
+    dw2, sdw2 = oracle.fc("fwd", Xt, dY)
+    assert np.array_equal(dw, dw2) and np.array_equal(sdw, sdw2)
+    for op, P, Q, Pt, Qt in (("fwd", X, W, Xt, Wt), ("dgrad", dY, W, dYt, Wt),
+                             ("wgrad", X, dY, Xt, dYt)):
+        ref, _ = oracle.fc(op, P, Q)
+        for p_t, q_t in ((True, False), (False, True), (True, True)):
+            got, _ = oracle.fc(op, Pt if p_t else P, Qt if q_t else Q, p_t, q_t)
+            assert np.array_equal(got, ref), (op, p_t, q_t)
