@@ -337,6 +337,20 @@ def run_reference(args):
     return 0
 
 
+def torch_product(op, P, Q, C):
+    """The op through torch.matmul (cuBLAS on a GPU), written into C: the
+    context leg's products.  P, Q are the op's stored operands (X, W for
+    fwd; dY, W for dgrad; X, dY for wgrad), untransposed."""
+    import torch
+    if op == "fwd":
+        torch.matmul(P, Q, out=C)
+    elif op == "dgrad":
+        torch.matmul(P, Q.t(), out=C)
+    else:
+        torch.matmul(P.t(), Q, out=C)
+    return C
+
+
 def max_over_ranks(value, device):
     """The largest `value` over all ranks of the default process group (the
     slowest rank's time); `value` itself when there is no group."""
@@ -536,6 +550,36 @@ def run_ours(args):
     else:
         achieved = flops_per_step * args.steps / (elapsed_ms * 1e9)
 
+    # Context only, off the product path: the same products through
+    # torch.matmul (cuBLAS), full layers, bf16 outputs, timed the same way.
+    torch_mm = None
+    if args.torch_matmul and not args.accum_f32:
+        def torch_gemm(g):
+            torch_product(g["op"], g["P"], g["Q"], g["C"])
+        full = [g for g in plan if tuple(g["C"].shape) == tuple(g["mnr"][:2])]
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                for g in full:
+                    torch_gemm(g)
+            tev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in full]
+            per_ms = [0.0] * len(full)
+            for _ in range(args.steps):
+                for gi, g in enumerate(full):
+                    tev[gi][0].record(stream)
+                    torch_gemm(g)
+                    tev[gi][1].record(stream)
+                torch.cuda.synchronize()
+                for gi in range(len(full)):
+                    per_ms[gi] += tev[gi][0].elapsed_time(tev[gi][1])
+        torch.cuda.synchronize()
+        tflops = [g["flops"] / (ms / args.steps) / 1e9 for g, ms in zip(full, per_ms)]
+        torch_mm = {"value": round(sum(g["flops"] for g in full) * args.steps
+                                   / (sum(per_ms) * 1e9), 2) if full else None,
+                    "unit": UNIT, "library": "cuBLAS through torch.matmul",
+                    "per_gemm_tflops": [round(t, 1) for t in tflops],
+                    "timing": "CUDA events around each eager call, summed over the steps",
+                    "note": "context only; not the product path"}
+
     # end to end: host (pinned) -> device copies, the GEMMs, device -> host
     h2d_bytes = d2h_bytes = 0
     io_bytes = sum(t.numel() * t.element_size() for d in dbuf.values() for t in d.values())
@@ -702,6 +746,7 @@ def run_ours(args):
             "device": {"sms": sms, "resident_cta_pairs": max_pairs,
                        "kernel_configs": sorted({p["config"] for p in per})},
             "clocks": clk,
+            **({"torch_matmul": torch_mm} if torch_mm is not None else {}),
         }
         if only is not None:
             line["profile_case"] = f"{only[0]}:{only[1]} only"
@@ -831,6 +876,9 @@ def main():
     ap.add_argument("--order-free", action="store_true",
                     help="virtual grid with --accum-f32: blocks added into the output by "
                          "atomics in one launch, instead of the fixed-order sum")
+    ap.add_argument("--torch-matmul", action="store_true",
+                    help="also time the same products through torch.matmul (cuBLAS), as "
+                         "context off the product path")
     ap.add_argument("--only", default=None, metavar="LAYER:OP",
                     help="time one GEMM (e.g. out:fwd) for profiling; not a bench line")
     args = ap.parse_args()

@@ -127,3 +127,23 @@ def test_config_block_labels():
     c = bench.config_block(bench.WORKLOADS["gpt_h6144_t8192_vgrid_2x2x2"], "v", 1)
     assert c["grid"] == "2x2x2"
     assert bench.config_block(bench.WORKLOADS["layout_sweep"], "s", 1)["l2"].startswith("mixed")
+
+
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_torch_context_products_are_the_ops(op):
+    """The cuBLAS context leg computes the same three products (checked here
+    with torch's CPU matmul against the oracle, within the parity bound)."""
+    import numpy as np
+    import torch
+    import fc_inputs
+    import oracle
+    T, K, N = 24, 40, 16
+    X = fc_inputs.normal_bf16((T, K), 3, 1)
+    W = fc_inputs.normal_bf16((K, N), 3, 2, sigma=0.02)
+    dY = fc_inputs.normal_bf16((T, N), 3, 3)
+    P, Q = {"fwd": (X, W), "dgrad": (dY, W), "wgrad": (X, dY)}[op]
+    M, Nn = oracle.out_shape(op, T, K, N)
+    C = torch.empty((M, Nn), dtype=torch.bfloat16)
+    bench.torch_product(op, fc_inputs.as_torch_bf16(P), fc_inputs.as_torch_bf16(Q), C)
+    ref, S = oracle.fc(op, P, Q)
+    assert float(oracle.error_ratio(C.to(torch.float64).numpy(), ref, S).max()) <= 1.0
