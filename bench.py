@@ -706,8 +706,10 @@ def run_ours(args):
                          "frac": round(achieved / peaks["sustained"], 4),
                          "frac_of_burst": round(achieved / peaks["burst"], 4),
                          "peak_source": f"{peaks['source']} (sustained; burst {peaks['burst']})",
-                         "kernel": "fc_gemm_tcgen05_kernel" + (
-                             " (virtual grid: blocks added into the output by atomics, one "
+                         "kernel": ("fc_gemm_tcgen05_kernel / fc_gemm_tcgen05_pair_kernel, "
+                                    "every GEMM launch of the step in the configurations "
+                                    "listed under device.kernel_configs") + (
+                             " (virtual grid: blocks added into the output by reduction adds, one "
                              "launch per GEMM)" if flags & fc.REDUCE_ADD else
                              " (virtual grid: two launches per GEMM, the partials summed in "
                              "the second one's epilogue)" if flags & fc.VGRID else ""),
