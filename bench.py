@@ -252,6 +252,61 @@ def oracle_stripes(data, glist, which, rows, gpu_rows=None):
     return flops, secs, min(oracle.max_threads(), rows), worst
 
 
+def check_bands(M, N, rng, row_band=32, col_band=64):
+    """Rows and columns of the whole-output check: rows 0 and M-1 plus one
+    seeded random row in every `row_band`-row band, columns 0 and N-1 plus
+    one random column in every `col_band`-column band.  Their cross product
+    puts an entry in every 32 x 64 cell of the output, so every output tile
+    of every kernel configuration (at least 128 x 128) is checked on the rows
+    of each of its epilogue warps (32 rows each), stream-K tiles included."""
+    import numpy as np
+    rows = [0, M - 1] + [b + int(rng.integers(0, min(row_band, M - b)))
+                         for b in range(0, M, row_band)]
+    cols = [0, N - 1] + [b + int(rng.integers(0, min(col_band, N - b)))
+                         for b in range(0, N, col_band)]
+    return np.unique(np.array(rows, np.int64)), np.unique(np.array(cols, np.int64))
+
+
+def _rows_of(view, t, idx):
+    """Stored copy of logical rows `idx` of an operand stored transposed if t."""
+    import numpy as np
+    return np.ascontiguousarray(view[:, idx] if t else view[idx, :])
+
+
+def _cols_of(view, t, idx):
+    """Stored copy of logical columns `idx` of an operand stored transposed if t."""
+    import numpy as np
+    return np.ascontiguousarray(view[idx, :] if t else view[:, idx])
+
+
+def whole_output_check(data, glist, outputs, seed=7):
+    """The GPU's outputs of the timed steps against the fp64 oracle over the
+    whole output of every GEMM: full rows 0 and M-1, full columns 0 and
+    N-1, and the cross product of one random row per 32-row band with one
+    random column per 64-column band (see check_bands).  `outputs` maps a
+    GEMM index to a function (rows, cols) -> float64 array of the GPU's
+    output there.  Returns the worst |C - C_ref| / (1e-2 |A|.|B| + 1e-5)
+    and the number of entries checked."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(seed)
+    worst, entries = 0.0, 0
+    for gi, (name, op, T, K, N, m, n, r, (pn, qn, _)) in enumerate(glist):
+        A, a_t, B, b_t = oracle.operands(op, data[name][pn], data[name][qn], False, False)
+        I, J = check_bands(m, n, rng)
+        full_i = np.array(sorted({0, m - 1}), np.int64)
+        full_j = np.array(sorted({0, n - 1}), np.int64)
+        all_j, all_i = np.arange(n, dtype=np.int64), np.arange(m, dtype=np.int64)
+        for ri, cj, Ablk, Bblk in ((I, J, _rows_of(A, a_t, I), _cols_of(B, b_t, J)),
+                                   (full_i, all_j, _rows_of(A, a_t, full_i), B),
+                                   (all_i, full_j, A, _cols_of(B, b_t, full_j))):
+            C, S = oracle.gemm(Ablk, a_t, Bblk, b_t)
+            got = outputs[gi](ri, cj)
+            worst = max(worst, float(oracle.error_ratio(got, C, S).max()))
+            entries += C.size
+    return worst, entries
+
+
 def cpu_rows(glist):
     """Output rows per GEMM that the CPU oracle computes: every row when the
     whole step is small (a few seconds on the host), else a stripe."""
@@ -762,6 +817,27 @@ def run_ours(args):
             gpu_rows = {gi: g["C"][:rows].to(torch.float64).cpu().numpy()
                         for gi, g in enumerate(plan)}
             line["cpu_baseline"] = cpu_baseline(data, glist, gpu_rows, rows)
+            # and the whole output of every GEMM, sampled, as the tuned step
+            # left it (every tile of every configuration, stream-K tiles
+            # included)
+            def gpu_at(gi):
+                C = plan[gi]["C"]
+
+                def f(ri, cj):
+                    ii = torch.from_numpy(ri).to(C.device)
+                    jj = torch.from_numpy(cj).to(C.device)
+                    return C.index_select(0, ii).index_select(1, jj).to(torch.float64).cpu().numpy()
+                return f
+            t0 = time.perf_counter()
+            worst, entries = whole_output_check(data, glist, {gi: gpu_at(gi) for gi in range(len(plan))})
+            line["cpu_baseline"]["whole_output_check"] = {
+                "max_error_ratio": worst, "entries": entries,
+                "seconds": round(time.perf_counter() - t0, 1),
+                "streamk_tiles_in_step": sum(sk_tiles),
+                "what": ("sampled over the whole output of every GEMM, stream-K tiles included: "
+                         "full rows 0 and M-1, full columns 0 and N-1, and one random row per "
+                         "32-row band x one random column per 64-column band (an entry in every "
+                         "32 x 64 cell); bound |C - C_ref| <= 1e-2 * (|A|.|B|) + 1e-5")}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

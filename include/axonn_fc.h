@@ -192,8 +192,8 @@ axonn_status_t axonn_fc_wgrad_zsharded(const void* X, const void* dY, void* cons
  *   flags     as for the entry points; AXONN_VGRID is implied
  * The fp32 partials live in a fixed 64 MiB scratch array inside the
  * library, which every GPU that loads the library holds until the process
- * exits.  A product whose partials need more (G * M * ceil8(N) * 4 bytes,
- * G the reduced grid extent) returns AXONN_ERR_WORKSPACE with a message;
+ * exits.  A product whose partials need more ((G-1) * M * ceil8(N) * 4
+ * bytes, G the reduced grid extent, M x N the output) returns AXONN_ERR_WORKSPACE with a message;
  * products whose reduced axis has one block need no scratch.  The first call
  * on each device looks up the scratch's device address (once, with that
  * device current); make that first call before any stream capture.  Every
@@ -264,6 +264,17 @@ axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, ui
 /* Rows [*start, *stop) of block b when a dimension D is cut into G blocks by
  * the 8-element-unit rule above.  Host-only, no GPU needed. */
 axonn_status_t axonn_block_range(int64_t D, int32_t G, int32_t b, int64_t* start, int64_t* stop);
+
+/* Logical ranges of block (shape->x, shape->y, shape->z) of op `op` (an
+ * axonn_op_t), as the product entry points resolve them: rows[2] = its
+ * output rows, red[2] = its reduced range, cols[2] = its output columns,
+ * each [start, stop) in the full matrices (forward: Tz, Kx, Ny; data
+ * gradient: Tz, Ny, Kx; weight gradient: Kx, Tz, Ny -- the block products
+ * of Figure 1 of the sciencestack.ai page under the reading T by G_z, K by
+ * G_x, N by G_y).  AXONN_ERR_INVALID_ARG for a bad op, shape or
+ * coordinate or a NULL output.  Host-only, no GPU needed. */
+axonn_status_t axonn_fc_block_extents(int op, const axonn_fc_shape_t* shape, int64_t* rows,
+                                      int64_t* red, int64_t* cols);
 
 /* Waits for `stream`, then reports (and clears) a device-side timeout
  * recorded by any kernel of this library on the current device since the

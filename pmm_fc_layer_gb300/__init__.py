@@ -33,7 +33,7 @@ EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_s
            "axonn_fc_workspace_size", "axonn_fc_tune", "axonn_tune_cache_save",
            "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
            "axonn_last_choice",
-           "axonn_block_range", "axonn_sync_status", "axonn_set_wait_timeout_ns",
+           "axonn_block_range", "axonn_fc_block_extents", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs",
            "axonn_set_streamk", "axonn_last_streamk_tiles", "axonn_device_info",
            "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
@@ -108,6 +108,10 @@ def load(path: str | None = None):
         lib.axonn_fc_workspace_size.restype = ctypes.c_int
         lib.axonn_block_range.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
         lib.axonn_block_range.restype = ctypes.c_int
+        lib.axonn_fc_block_extents.argtypes = [ctypes.c_int, ctypes.POINTER(Shape),
+                                               ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                               ctypes.POINTER(i64)]
+        lib.axonn_fc_block_extents.restype = ctypes.c_int
         lib.axonn_sync_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint64)]
         lib.axonn_sync_status.restype = ctypes.c_int
         lib.axonn_set_wait_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -282,6 +286,15 @@ def axonn_block_range(D: int, G: int, b: int):
     s, e = ctypes.c_int64(0), ctypes.c_int64(0)
     _check(load().axonn_block_range(D, G, b, ctypes.byref(s), ctypes.byref(e)))
     return s.value, e.value
+
+
+def axonn_fc_block_extents(op, shape: Shape):
+    """((rows), (red), (cols)) of block (shape.x, shape.y, shape.z) of `op`,
+    each a [start, stop) pair in the full matrices."""
+    op = OPS.get(op, op)
+    r, k, c = (ctypes.c_int64 * 2)(), (ctypes.c_int64 * 2)(), (ctypes.c_int64 * 2)()
+    _check(load().axonn_fc_block_extents(int(op), ctypes.byref(shape), r, k, c))
+    return (r[0], r[1]), (k[0], k[1]), (c[0], c[1])
 
 
 def axonn_sync_status(stream=None, raise_on_error: bool = True):

@@ -223,7 +223,9 @@ size_t vgrid_ws_bytes(int op, const axonn_fc_shape_t& s, uint32_t flags) {
   int64_t M, N, R;
   full_dims(op, s, &M, &N, &R);
   const int64_t ldp = (N + 7) / 8 * 8;
-  return static_cast<size_t>(G) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * 4u;
+  // Partials 0..G-2 go to the workspace; the last block's epilogue adds
+  // them to its own accumulator and writes the output.
+  return static_cast<size_t>(G - 1) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * 4u;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -1352,6 +1354,19 @@ axonn_status_t axonn_block_range(int64_t D, int32_t G, int32_t b, int64_t* start
   if (!start || !stop) return fail(AXONN_ERR_INVALID_ARG, "NULL output");
   if (D < 0 || G < 1 || b < 0 || b >= G) return fail(AXONN_ERR_INVALID_ARG, "bad D/G/b");
   split_range(D, G, b, start, stop);
+  return ok();
+}
+
+axonn_status_t axonn_fc_block_extents(int op, const axonn_fc_shape_t* shape, int64_t* rows,
+                                      int64_t* red, int64_t* cols) {
+  if (!rows || !red || !cols) return fail(AXONN_ERR_INVALID_ARG, "NULL output");
+  axonn_status_t st = check_shape(op, shape, 0);
+  if (st != AXONN_OK) return st;
+  Range r, k, c;
+  block_ranges(op, *shape, shape->x, shape->y, shape->z, &r, &k, &c);
+  rows[0] = r.s; rows[1] = r.e;
+  red[0] = k.s; red[1] = k.e;
+  cols[0] = c.s; cols[1] = c.e;
   return ok();
 }
 

@@ -61,6 +61,21 @@ def test_block_range_matches_oracle_rule(fc, D, G):
         assert fc.axonn_block_range(D, G, b) == oracle.split_range(D, G, b)
 
 
+def test_block_extents_hand_table(fc):
+    """The library's own block resolution (which grid axis cuts which
+    dimension, and each op's rows / reduced range / columns) against the
+    hand-worked table in tests/golden/, on the CPU."""
+    import json
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "fc_hand_examples.json")))
+    for case in g["block_extents"]["cases"]:
+        shape = fc.Shape(*case["TKN"], tuple(case["grid"]), tuple(case["coords"]))
+        for op in ("fwd", "dgrad", "wgrad"):
+            got = fc.axonn_fc_block_extents(op, shape)
+            assert [list(r) for r in got] == case[op], (case["TKN"], op)
+    with pytest.raises(fc.AxonnError):
+        fc.axonn_fc_block_extents("fwd", fc.Shape(64, 64, 64, (2, 1, 1), (2, 0, 0)))
+
+
 def test_block_range_errors(fc):
     with pytest.raises(fc.AxonnError):
         fc.axonn_block_range(10, 0, 0)
@@ -71,14 +86,14 @@ def test_block_range_errors(fc):
 def test_workspace_size(fc):
     s = fc.Shape(8192, 6144, 24576, (2, 2, 2))
     assert fc.axonn_fc_workspace_size("fwd", s, 0) == 0
-    assert fc.axonn_fc_workspace_size("fwd", s, fc.VGRID) == 2 * 8192 * 24576 * 4
-    assert fc.axonn_fc_workspace_size("dgrad", s, fc.VGRID) == 2 * 8192 * 6144 * 4
-    assert fc.axonn_fc_workspace_size("wgrad", s, fc.VGRID) == 2 * 6144 * 24576 * 4
+    assert fc.axonn_fc_workspace_size("fwd", s, fc.VGRID) == 1 * 8192 * 24576 * 4
+    assert fc.axonn_fc_workspace_size("dgrad", s, fc.VGRID) == 1 * 8192 * 6144 * 4
+    assert fc.axonn_fc_workspace_size("wgrad", s, fc.VGRID) == 1 * 6144 * 24576 * 4
     s4 = fc.Shape(4096, 16384, 18432, (1, 4, 4))
     assert fc.axonn_fc_workspace_size("fwd", s4, fc.VGRID) == 0      # G_x = 1
-    assert fc.axonn_fc_workspace_size("dgrad", s4, fc.VGRID) == 4 * 4096 * 16384 * 4
+    assert fc.axonn_fc_workspace_size("dgrad", s4, fc.VGRID) == 3 * 4096 * 16384 * 4
     odd = fc.Shape(100, 60, 1001, (1, 1, 3))
-    assert fc.axonn_fc_workspace_size("wgrad", odd, fc.VGRID) == 3 * 60 * 1008 * 4
+    assert fc.axonn_fc_workspace_size("wgrad", odd, fc.VGRID) == 2 * 60 * 1008 * 4
 
 
 def _status(fc, fn, *args):
@@ -138,7 +153,7 @@ def test_reduce_add_needs_no_workspace(fc):
     s = fc.Shape(64, 64, 64, (2, 2, 2))
     f = fc.VGRID | fc.ACCUM_F32
     for op in ("fwd", "dgrad", "wgrad"):
-        assert fc.axonn_fc_workspace_size(op, s, f) == 2 * 64 * 64 * 4
+        assert fc.axonn_fc_workspace_size(op, s, f) == 1 * 64 * 64 * 4
         assert fc.axonn_fc_workspace_size(op, s, f | fc.REDUCE_ADD) == 0
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():

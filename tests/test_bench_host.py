@@ -147,3 +147,52 @@ def test_torch_context_products_are_the_ops(op):
     bench.torch_product(op, fc_inputs.as_torch_bf16(P), fc_inputs.as_torch_bf16(Q), C)
     ref, S = oracle.fc(op, P, Q)
     assert float(oracle.error_ratio(C.to(torch.float64).numpy(), ref, S).max()) <= 1.0
+
+
+@pytest.mark.parametrize("M,N", [(256, 2048), (8192, 6144), (300, 1000), (1, 1), (33, 65)])
+def test_check_bands_cover_every_cell(M, N):
+    """The whole-output check's rows and columns put an entry in every 32 x
+    64 cell of the output (so in every epilogue warp's rows of every tile)
+    and include the first and last row and column."""
+    import numpy as np
+    I, J = bench.check_bands(M, N, np.random.default_rng(1))
+    assert I.min() == 0 and I.max() == M - 1 and J.min() == 0 and J.max() == N - 1
+    assert set(range(0, M, 32)) == {32 * (i // 32) for i in I}
+    assert set(range(0, N, 64)) == {64 * (j // 64) for j in J}
+
+
+@pytest.mark.parametrize("planted", [None, "cell", "last_row", "last_col"])
+def test_whole_output_check_finds_a_wrong_entry(planted):
+    """Fed the oracle's own full product (transposed storages included), the
+    check reports ratios of bf16 rounding alone (at most 2^-9 |C| against
+    1e-2 S, so below 0.2); with one entry moved well outside the
+    bound (in a random 32 x 64 cell, in the last row, or in the last
+    column), it reports a ratio above 1."""
+    import numpy as np
+    import fc_inputs
+    import oracle
+    layers = [("a", 96, 130, 200)]
+    wl = {"layers": layers, "seed": 5}
+    data = bench.host_inputs(wl, layers)
+    glist = bench.gemms(layers)
+    rng = np.random.default_rng(3)
+    full = {}
+    for gi, (name, op, T, K, N, m, n, r, (pn, qn, _)) in enumerate(glist):
+        C, S = oracle.fc(op, data[name][pn], data[name][qn])
+        got = oracle.bf16_to_f64(oracle.bf16_rne(C))
+        if planted and gi == 1:
+            i, j = {"cell": (int(rng.integers(1, m - 1)), int(rng.integers(1, n - 1))),
+                    "last_row": (m - 1, int(rng.integers(0, n))),
+                    "last_col": (int(rng.integers(0, m)), n - 1)}[planted]
+            # a wrong entry in every 32 x 64 cell of the row band and column
+            # band of (i, j): the check samples one row per band
+            got[32 * (i // 32): 32 * (i // 32) + 32, 64 * (j // 64): 64 * (j // 64) + 64] += \
+                1.0 + 0.1 * S[32 * (i // 32): 32 * (i // 32) + 32, 64 * (j // 64): 64 * (j // 64) + 64]
+        full[gi] = got
+    outputs = {gi: (lambda g: (lambda ri, cj: g[np.ix_(ri, cj)]))(full[gi]) for gi in full}
+    worst, entries = bench.whole_output_check(data, glist, outputs)
+    assert entries > 0
+    if planted:
+        assert worst > 1.0
+    else:
+        assert worst < 0.2

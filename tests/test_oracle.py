@@ -272,3 +272,66 @@ def test_op_equivalences_through_transposed_copies(T, K, N):
         for p_t, q_t in ((True, False), (False, True), (True, True)):
             got, _ = oracle.fc(op, Pt if p_t else P, Qt if q_t else Q, p_t, q_t)
             assert np.array_equal(got, ref), (op, p_t, q_t)
+
+
+def _block_pin_mismatches(block_extents):
+    """Cases of the hand-worked block-extent table that `block_extents`
+    gets wrong (empty when every op of every case matches)."""
+    g = json.load(open(GOLDEN))["block_extents"]
+    bad = []
+    for case in g["cases"]:
+        T, K, N = case["TKN"]
+        for op in oracle.OPS:
+            want = tuple(tuple(r) for r in case[op])
+            try:
+                got = tuple(tuple(r) for r in block_extents(op, T, K, N, tuple(case["grid"]),
+                                                            tuple(case["coords"])))
+            except AssertionError:
+                got = None
+            if got != want:
+                bad.append((case["TKN"], case["grid"], case["coords"], op, got, want))
+    return bad
+
+
+def test_block_extents_hand_table():
+    """Which grid axis cuts which dimension (T by G_z, K by G_x, N by G_y) and
+    each op's (output rows, reduced range, output cols), pinned by hand on
+    asymmetric grids: any permutation of the axes fails here, where the
+    block-sum invariant (which holds for every permutation) cannot tell."""
+    assert _block_pin_mismatches(oracle.block_extents) == []
+
+
+def _swap_axes(which):
+    real = oracle.block_extents
+
+    def wrong(op, T, K, N, grid, coords):
+        gx, gy, gz = grid
+        x, y, z = coords
+        if which == "xy":
+            return real(op, T, K, N, (gy, gx, gz), (y, x, z))
+        if which == "xz":
+            return real(op, T, K, N, (gz, gy, gx), (z, y, x))
+        # dgrad reducing over the output columns' axis instead of N's
+        rows, red, cols = real(op, T, K, N, grid, coords)
+        return (rows, cols, red) if op == "dgrad" else (rows, red, cols)
+    return wrong
+
+
+@pytest.mark.parametrize("which", ["xy", "xz", "dgrad_roles"])
+def test_planted_block_axis_mistake_is_caught(which):
+    """A grid whose G_x and G_y (or G_x and G_z) trade places, or a data
+    gradient with its reduced and output ranges exchanged, fails the hand
+    table; the block-sum invariant alone would pass all three."""
+    wrong = _swap_axes(which)
+    assert _block_pin_mismatches(wrong)
+    if which != "dgrad_roles":
+        T, K, N, grid = 41, 50, 36, (3, 1, 2)
+        X = fc_inputs.small_int_bf16((T, K), seed=9, tid=1, h=2)
+        W = fc_inputs.small_int_bf16((K, N), seed=9, tid=2, h=2)
+        real = oracle.block_extents
+        try:
+            oracle.block_extents = wrong
+            vg, _ = oracle.fc_vgrid("fwd", X, W, False, False, T, K, N, (2, 2, 2))
+        finally:
+            oracle.block_extents = real
+        assert np.array_equal(vg, oracle.fc_fwd(X, W)[0])   # the invariant cannot tell

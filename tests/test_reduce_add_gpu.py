@@ -143,12 +143,12 @@ def test_reduce_add_repeat_and_graph(cuda_lib):
 
 
 def test_reduce_add_static_entry_point_needs_no_scratch(cuda_lib):
-    """A product whose fixed-order partials (2 x 4096 x 4096 fp32 = 128 MiB)
-    exceed the built-in 64 MiB scratch: refused without AXONN_REDUCE_ADD,
-    exact with it."""
+    """A product whose fixed-order partial (one slot of 4096 x 8192 fp32 =
+    128 MiB on a 2x1x1 grid) exceeds the built-in 64 MiB scratch: refused
+    without AXONN_REDUCE_ADD, exact with it."""
     import torch
     fc = cuda_lib
-    T, K, N = 4096, 64, 4096
+    T, K, N = 4096, 64, 8192
     grid = (2, 1, 1)
     X = make_operand("X", T, K, N, False, seed=75, kind="int")
     W = make_operand("W", T, K, N, False, seed=75, kind="int")
