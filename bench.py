@@ -449,6 +449,8 @@ def run_ours(args):
         flags |= fc.ACCUM_F32
     if args.order_free:
         flags |= fc.REDUCE_ADD
+    if args.vgrid_partials:
+        flags |= fc.VGRID_PARTIALS
     out_dtype = torch.float32 if args.accum_f32 else torch.bfloat16
     only = tuple(args.only.split(":")) if args.only else None
     layers = [l for l in wl["layers"] if only is None or l[0] == only[0]]
@@ -478,10 +480,11 @@ def run_ours(args):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev) if wl.get("flush") else None
     stream = torch.cuda.Stream(device=dev)
     used = [None] * len(plan)
-    # the fixed-order virtual-grid sum is a second launch per GEMM whose
-    # reduced grid axis has more than one block; the order-free one is not
+    # the two-launch virtual-grid sum is a second launch per GEMM whose
+    # reduced grid axis has more than one block; the chained and the
+    # order-free ones are not
     reduce_launches = sum(1 for g in glist
-                          if (flags & fc.VGRID) and not (flags & fc.REDUCE_ADD)
+                          if (flags & fc.VGRID) and (flags & fc.VGRID_PARTIALS)
                           and {"fwd": grid[0], "dgrad": grid[1], "wgrad": grid[2]}[g[1]] > 1)
 
     sk_tiles = [0] * len(plan)
@@ -767,7 +770,9 @@ def run_ours(args):
                              " (virtual grid: blocks added into the output by reduction adds, one "
                              "launch per GEMM)" if flags & fc.REDUCE_ADD else
                              " (virtual grid: two launches per GEMM, the partials summed in "
-                             "the second one's epilogue)" if flags & fc.VGRID else ""),
+                             "the second one's epilogue)" if flags & fc.VGRID_PARTIALS else
+                             " (virtual grid: one launch per GEMM, each tile's block products "
+                             "chained into one accumulator)" if flags & fc.VGRID else ""),
                          "traffic": (TRAFFIC["bytes_per_step"] / TRAFFIC["launches_per_step"]
                                      if args.workload == TRAFFIC["workload"] and only is None
                                      and kernel_sources_hash() == TRAFFIC["kernel_sources"]
@@ -954,6 +959,9 @@ def main():
     ap.add_argument("--order-free", action="store_true",
                     help="virtual grid with --accum-f32: blocks added into the output by "
                          "atomics in one launch, instead of the fixed-order sum")
+    ap.add_argument("--vgrid-partials", action="store_true",
+                    help="virtual grid in its two-launch form: fp32 partials in a workspace, "
+                         "summed in the last block's epilogue (default: chained)")
     ap.add_argument("--torch-matmul", action="store_true",
                     help="also time the same products through torch.matmul (cuBLAS), as "
                          "context off the product path")

@@ -29,17 +29,25 @@
  * Virtual grid (AXONN_VGRID).  All G_x*G_y*G_z block products run on this
  * GPU, and an on-device sum over the reduced axis (G = G_x for fwd, G_y for
  * dgrad, G_z for wgrad) stands in for the grid's all-reduce /
- * reduce-scatter.  By default the sum has a fixed order: one launch writes
- * the partials 0..G-2 in fp32 to the caller's workspace, and a second
- * computes partial G-1, whose epilogue adds partials 0..G-1 in that order
- * and writes the output, so results are the same on every run.  With
- * AXONN_REDUCE_ADD (fp32 accumulating output only) all blocks run in one
- * launch and each adds its tile into the output with fp32 reduction adds
- * (PTX red.global.add: rounded to nearest even, subnormal inputs and
- * results flushed to zero): no workspace, no second launch, and a
- * summation order that can change from run to run (every order stays
- * within the same error bound; integer-valued sums below 2^24 are exact in
- * any order).
+ * reduce-scatter.  Three forms:
+ *  - default (chained): each output tile runs the G block products of its
+ *    output block one after another, in order g = 0..G-1, into one fp32
+ *    accumulator on the tensor cores, each block product read from its own
+ *    block (its own tensor maps, zero-filled at the block's edges).  One
+ *    launch, no workspace, no partial in memory; results are the same on
+ *    every run.
+ *  - AXONN_VGRID_PARTIALS: one launch writes the partials 0..G-2 in fp32 to
+ *    the caller's workspace, and a second computes partial G-1, whose
+ *    epilogue adds partials 0..G-1 in that order and writes the output
+ *    (the partials as the grid's ranks would hold them); results are the
+ *    same on every run, and may differ from the chained form in the last
+ *    bits (another summation order).
+ *  - AXONN_REDUCE_ADD (fp32 accumulating output only): all blocks run in
+ *    one launch and each adds its tile into the output with fp32 reduction
+ *    adds (PTX red.global.add: rounded to nearest even, subnormal inputs
+ *    and results flushed to zero): no workspace, and a summation order that
+ *    can change from run to run (every order stays within the same error
+ *    bound; integer-valued sums below 2^24 are exact in any order).
  *
  * Conventions for every entry point below.
  *  - Pointers are DEVICE pointers; the caller owns every buffer and the
@@ -109,6 +117,9 @@ typedef struct {
 #define AXONN_REDUCE_ADD 0x80u    /* with AXONN_VGRID | AXONN_ACCUM_F32: every block added
                                      into the output by fp32 reduction adds, in no fixed
                                      order; one launch, no workspace */
+#define AXONN_VGRID_PARTIALS 0x100u /* with AXONN_VGRID: the two-launch form, fp32 partials
+                                     of blocks 0..G-2 in the workspace, summed in order in
+                                     the last block's epilogue */
 
 /*
  * Forward product Y = X . W of the layer, of block (x,y,z), or of the whole
@@ -122,8 +133,8 @@ typedef struct {
  *   (X_blk [Tz x Kx], W_blk [Kx x Ny], Y_blk [Tz x Ny], each with its ld);
  *   with it they address the full matrices and the block is located by its
  *   offsets, its partial written at Y[Tz, Ny].
- *   ws / ws_bytes: device workspace, needed with AXONN_VGRID when G_x > 1
- *   and AXONN_REDUCE_ADD is not given (size from
+ *   ws / ws_bytes: device workspace, needed with AXONN_VGRID |
+ *   AXONN_VGRID_PARTIALS when G_x > 1 (size from
  *   axonn_fc_workspace_size).  Otherwise optional: a full-size one enables
  *   the reduction split of small products and the stream-K tail of large
  *   ones; NULL / 0 runs without them.
@@ -190,11 +201,13 @@ axonn_status_t axonn_fc_wgrad_zsharded(const void* X, const void* dY, void* cons
  * code that must not allocate once it is running.
  *   op        axonn_op_t; P, Q, C and ld* as for that op's entry point
  *   flags     as for the entry points; AXONN_VGRID is implied
- * The fp32 partials live in a fixed 64 MiB scratch array inside the
- * library, which every GPU that loads the library holds until the process
- * exits.  A product whose partials need more ((G-1) * M * ceil8(N) * 4
- * bytes, G the reduced grid extent, M x N the output) returns AXONN_ERR_WORKSPACE with a message;
- * products whose reduced axis has one block need no scratch.  The first call
+ * The fp32 partials of the two-launch form (AXONN_VGRID_PARTIALS) live in
+ * a fixed 64 MiB scratch array inside the library, which every GPU that
+ * loads the library holds until the process exits.  A product whose
+ * partials need more ((G-1) * M * ceil8(N) * 4 bytes, G the reduced grid
+ * extent, M x N the output) returns AXONN_ERR_WORKSPACE with a message.
+ * The default chained form, AXONN_REDUCE_ADD and products whose reduced
+ * axis has one block need no scratch.  The first call
  * on each device looks up the scratch's device address (once, with that
  * device current); make that first call before any stream capture.  Every
  * call uses the same scratch and the kernels overwrite every partial they
@@ -251,12 +264,14 @@ int axonn_tune_cache_size(void);
 void axonn_last_choice(int* config, int* split, int* group_m);
 
 /* Workspace bytes an op needs with these flags (0 when none).  `op` is an
- * axonn_op_t.  With AXONN_VGRID it is the fp32 partials of the reduced grid
- * axis (0 with AXONN_REDUCE_ADD).  Without it, it is nonzero for products that leave most SMs idle
- * (fewer 128x256 tiles than two waves), which may then split their
- * reduction range, and for products of more than one wave of 128x128 tiles,
- * which may run a stream-K tail (see axonn_set_streamk; up to about 80 MB on
- * a 152-SM GPU).  Passing less workspace just disables either.
+ * axonn_op_t.  With AXONN_VGRID | AXONN_VGRID_PARTIALS it is the fp32
+ * partials 0..G-2 of the reduced grid axis ((G-1) * M * ceil8(N) * 4); the
+ * other virtual-grid forms need none.  Without AXONN_VGRID it is nonzero
+ * for products that leave most SMs idle (fewer 128x256 tiles than two
+ * waves), which may then split their reduction range, and for products of
+ * more than one wave of 128x128 tiles, which may run a stream-K tail (see
+ * axonn_set_streamk; up to about 80 MB on a 152-SM GPU).  Passing less
+ * workspace just disables either.
  * Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
                                        size_t* bytes);

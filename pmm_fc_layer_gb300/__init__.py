@@ -24,6 +24,7 @@ FULL_OPERANDS = 0x10
 OUT_F32 = 0x20
 ZSHARDED = 0x40
 REDUCE_ADD = 0x80
+VGRID_PARTIALS = 0x100
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ERR_TIMEOUT = range(7)
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]

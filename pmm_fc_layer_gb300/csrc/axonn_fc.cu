@@ -191,7 +191,7 @@ void full_dims(int op, const axonn_fc_shape_t& s, int64_t* M, int64_t* N, int64_
 
 constexpr uint32_t kKnownFlags = AXONN_A_T | AXONN_B_T | AXONN_ACCUM_F32 | AXONN_VGRID |
                                  AXONN_FULL_OPERANDS | AXONN_OUT_F32 | AXONN_ZSHARDED |
-                                 AXONN_REDUCE_ADD;
+                                 AXONN_REDUCE_ADD | AXONN_VGRID_PARTIALS;
 
 axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
   if (op < AXONN_OP_FWD || op > AXONN_OP_WGRAD) return fail(AXONN_ERR_INVALID_ARG, "bad op %d", op);
@@ -201,6 +201,10 @@ axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
     return fail(AXONN_ERR_INVALID_ARG, "AXONN_ACCUM_F32 and AXONN_OUT_F32 are exclusive");
   if ((flags & AXONN_REDUCE_ADD) && (flags & (AXONN_VGRID | AXONN_ACCUM_F32)) != (AXONN_VGRID | AXONN_ACCUM_F32))
     return fail(AXONN_ERR_INVALID_ARG, "AXONN_REDUCE_ADD needs AXONN_VGRID and AXONN_ACCUM_F32");
+  if ((flags & AXONN_VGRID_PARTIALS) && !(flags & AXONN_VGRID))
+    return fail(AXONN_ERR_INVALID_ARG, "AXONN_VGRID_PARTIALS needs AXONN_VGRID");
+  if ((flags & AXONN_VGRID_PARTIALS) && (flags & AXONN_REDUCE_ADD))
+    return fail(AXONN_ERR_INVALID_ARG, "AXONN_VGRID_PARTIALS and AXONN_REDUCE_ADD are exclusive");
   if (s->T < 0 || s->K < 0 || s->N < 0) return fail(AXONN_ERR_INVALID_ARG, "negative extent");
   const int64_t lim = (int64_t{1} << 31) - 256;
   if (s->T > lim || s->K > lim || s->N > lim) return fail(AXONN_ERR_UNSUPPORTED, "extent above 2^31");
@@ -217,7 +221,7 @@ axonn_status_t check_shape(int op, const axonn_fc_shape_t* s, uint32_t flags) {
 }
 
 size_t vgrid_ws_bytes(int op, const axonn_fc_shape_t& s, uint32_t flags) {
-  if (!(flags & AXONN_VGRID) || (flags & AXONN_REDUCE_ADD)) return 0;
+  if (!(flags & AXONN_VGRID) || !(flags & AXONN_VGRID_PARTIALS)) return 0;
   const int G = reduce_extent(op, s);
   if (G <= 1) return 0;
   int64_t M, N, R;
@@ -297,6 +301,10 @@ struct Block {
   int64_t ldc;
   int64_t M, N, R;
   int out_mode;
+  // Chains: the head of a run of `chain` consecutive blocks (same output,
+  // same M x N) whose products all add into one accumulator, in order; the
+  // members after the head have chain = 0.  An ordinary block has chain = 1.
+  int chain = 1;
   int phase = 1;               // 0: writes an fp32 partial that a phase-1 block reads
   int red_count = 0;           // partials to add in the epilogue (last partial only)
   const float* red_src = nullptr;
@@ -374,10 +382,19 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
   const uint32_t a_rows = 128;
   const uint32_t cta_rows = c.pair ? c.bm / 2 : c.bm;
   const uint32_t b_cols = c.pair ? c.bn / 2 : c.bn;
+  const uint32_t bk = static_cast<uint32_t>(c.bk);
   int64_t tiles = 0;
-  int np = 0;
-  for (const Block& b : blocks) {
-    if (b.M == 0 || b.N == 0) continue;
+  int np = 0, nmaps = 0;
+  for (size_t bi = 0; bi < blocks.size();) {
+    const Block& b = blocks[bi];
+    const size_t members = static_cast<size_t>(b.chain > 0 ? b.chain : 1);
+    if (b.chain <= 0 || bi + members > blocks.size())
+      return fail(AXONN_ERR_INVALID_ARG, "malformed chain of block products");
+    const size_t next = bi + members;
+    if (b.M == 0 || b.N == 0) {
+      bi = next;
+      continue;
+    }
     if (np >= MAXP) return fail(AXONN_ERR_UNSUPPORTED, "too many block products");
     if (tiles + ((b.M + c.bm - 1) / c.bm) * ((b.N + c.bn - 1) / c.bn) > (int64_t{1} << 30))
       return fail(AXONN_ERR_UNSUPPORTED, "more than 2^30 output tiles in one launch");
@@ -386,11 +403,9 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.ldc = b.ldc;
     d.M = static_cast<int32_t>(b.M);
     d.N = static_cast<int32_t>(b.N);
-    d.R = static_cast<int32_t>(b.R);
     d.tiles_m = static_cast<int32_t>((b.M + c.bm - 1) / c.bm);
     d.tiles_n = static_cast<int32_t>((b.N + c.bn - 1) / c.bn);
     d.tile_start = static_cast<int32_t>(tiles);
-    d.num_k = static_cast<int32_t>((b.R + c.bk - 1) / c.bk);
     d.a_mn = v.a_mn;
     d.b_mn = v.b_mn;
     d.idesc = make_idesc(c.mma_m, c.bn, v.a_mn, v.b_mn);
@@ -401,24 +416,49 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.red_ld = b.red_ld;
     d.fast_bf16 = b.out_mode == axonn::kOutBF16 && b.red_count == 0 &&
                   reinterpret_cast<uintptr_t>(b.C) % 32 == 0 && b.ldc % 16 == 0;
-    if (b.R > 0) {
+    d.a_3d = v.a_mn && b.M % 64 == 0;
+    d.b_3d = v.b_mn && b.N % 64 == 0;
+    // One tensor-map pair per member with a non-empty reduction, each with
+    // the member's own extents (loads past them read zeros).
+    d.map0 = nmaps;
+    d.chain = 0;
+    int64_t steps = 0, red = 0;
+    for (size_t g = bi; g < next; ++g) {
+      const Block& m = blocks[g];
+      if (m.M != b.M || m.N != b.N || (g > bi && m.chain != 0))
+        return fail(AXONN_ERR_INVALID_ARG, "chain members differ in output extent");
+      if (m.R == 0) continue;
+      if (nmaps >= MAXP) return fail(AXONN_ERR_UNSUPPORTED, "too many block products");
       axonn_status_t s;
-      const uint32_t bk = static_cast<uint32_t>(c.bk);
-      d.a_3d = v.a_mn && b.M % 64 == 0;
-      d.b_3d = v.b_mn && b.N % 64 == 0;
-      if (d.a_3d) s = encode_mn_3d(&P.tma[np], b.A, b.M, b.R, v.lda, bk, cta_rows / 64);
-      else if (v.a_mn) s = encode_2d(&P.tma[np], b.A, b.M, b.R, v.lda, 64, bk);
-      else s = encode_2d(&P.tma[np], b.A, b.R, b.M, v.lda, bk, a_rows);
+      CUtensorMap* ta = &P.tma[nmaps];
+      CUtensorMap* tb = &P.tmb[nmaps];
+      if (d.a_3d) s = encode_mn_3d(ta, m.A, m.M, m.R, v.lda, bk, cta_rows / 64);
+      else if (v.a_mn) s = encode_2d(ta, m.A, m.M, m.R, v.lda, 64, bk);
+      else s = encode_2d(ta, m.A, m.R, m.M, v.lda, bk, a_rows);
       if (s != AXONN_OK) return s;
-      if (d.b_3d) s = encode_mn_3d(&P.tmb[np], b.B, b.N, b.R, v.ldb, bk, b_cols / 64);
-      else if (v.b_mn) s = encode_2d(&P.tmb[np], b.B, b.N, b.R, v.ldb, 64, bk);
-      else s = encode_2d(&P.tmb[np], b.B, b.R, b.N, v.ldb, bk, b_cols);
+      if (d.b_3d) s = encode_mn_3d(tb, m.B, m.N, m.R, v.ldb, bk, b_cols / 64);
+      else if (v.b_mn) s = encode_2d(tb, m.B, m.N, m.R, v.ldb, 64, bk);
+      else s = encode_2d(tb, m.B, m.R, m.N, v.ldb, bk, b_cols);
       if (s != AXONN_OK) return s;
+      P.map_nk[nmaps] = static_cast<int32_t>((m.R + c.bk - 1) / c.bk);
+      steps += P.map_nk[nmaps];
+      red += m.R;
+      ++d.chain;
+      ++nmaps;
     }
+    if (steps >= (int64_t{1} << 30)) return fail(AXONN_ERR_UNSUPPORTED, "reduction too long");
+    if (d.chain == 0) {  // empty reduction: no loads, the epilogue writes zeros
+      d.chain = 1;
+      d.map0 = 0;
+    }
+    d.num_k = static_cast<int32_t>(steps);
+    d.R = static_cast<int32_t>(std::min<int64_t>(red, INT32_MAX));
     tiles += d.tiles_m * d.tiles_n;
     ++np;
+    bi = next;
   }
   P.num_problems = np;
+  P.num_maps = nmaps;
   P.total_tiles = static_cast<int32_t>(tiles);
   P.group_m = group_m;
   P.inject = g_inject.load();
@@ -515,8 +555,8 @@ axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, const DeviceS
 // units the GPU runs at once; the rounding up is the wave-quantisation loss.
 double config_cost(const std::vector<Block>& blocks, const KernelConfig& c, const DeviceState& dev) {
   int64_t tiles = 0;
-  for (const Block& b : blocks)
-    if (b.M > 0 && b.N > 0) tiles += ((b.M + c.bm - 1) / c.bm) * ((b.N + c.bn - 1) / c.bn);
+  for (const Block& b : blocks)  // chain members after the head share its tiles
+    if (b.chain > 0 && b.M > 0 && b.N > 0) tiles += ((b.M + c.bm - 1) / c.bm) * ((b.N + c.bn - 1) / c.bn);
   const int64_t slots = c.pair ? dev.max_pairs : dev.sms;
   const int64_t waves = (tiles + slots - 1) / slots;
   // One wave costs the tile's area over the configuration's speed.
@@ -633,12 +673,18 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   }
   if (hM == 0 || hN == 0) return ok();
 
-  // With AXONN_REDUCE_ADD every block adds its product into the fp32 output
-  // with atomic adds, all in one launch: no partials, no workspace, and a
-  // summation order that varies from run to run.
+  // The virtual grid's sum over the reduced axis, three ways:
+  //  - chained (default): the G block products of each output tile run one
+  //    after another into one TMEM accumulator (fixed order g = 0..G-1),
+  //    one launch, no workspace;
+  //  - AXONN_VGRID_PARTIALS: blocks 0..G-2 write fp32 partials to the
+  //    workspace and the last block's epilogue adds them in order;
+  //  - AXONN_REDUCE_ADD: every block adds its product into the fp32 output
+  //    with reduction adds, in one launch, in no fixed order.
   const bool red_add = (flags & AXONN_REDUCE_ADD) != 0;
   const int G = reduce_extent(op, s);
-  const bool partials = vgrid && G > 1 && !red_add;
+  const bool partials = vgrid && G > 1 && (flags & AXONN_VGRID_PARTIALS);
+  const bool chained = vgrid && G > 1 && !partials && !red_add;
   int64_t ldpart = 0;
   if (partials) {
     const size_t need = vgrid_ws_bytes(op, s, flags);
@@ -661,7 +707,30 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   const size_t celt = out_f32 ? 4 : 2;
 
   LaunchPlan plan;
-  if (vgrid) {
+  if (chained) {
+    // Output blocks (o1, o2) in turn, each followed by its G block products
+    // in order along the reduced axis.
+    const int n1 = op == AXONN_OP_WGRAD ? s.gx : s.gz;
+    const int n2 = op == AXONN_OP_DGRAD ? s.gx : s.gy;
+    for (int o1 = 0; o1 < n1; ++o1)
+      for (int o2 = 0; o2 < n2; ++o2)
+        for (int g = 0; g < G; ++g) {
+          const int x = op == AXONN_OP_FWD ? g : (op == AXONN_OP_DGRAD ? o2 : o1);
+          const int y = op == AXONN_OP_DGRAD ? g : o2;
+          const int z = op == AXONN_OP_WGRAD ? g : o1;
+          Range br, bred, bc;
+          block_ranges(op, s, x, y, z, &br, &bred, &bc);
+          Block b;
+          b.A = a_at(br.s, bred.s);
+          b.B = b_at(bred.s, bc.s);
+          b.M = br.len(); b.N = bc.len(); b.R = bred.len();
+          b.C = v.C + celt * (br.s * ldc + bc.s);
+          b.ldc = ldc;
+          b.out_mode = user_mode;
+          b.chain = g == 0 ? G : 0;
+          plan.blocks.push_back(b);
+        }
+  } else if (vgrid) {
     for (int x = 0; x < s.gx; ++x)
       for (int y = 0; y < s.gy; ++y)
         for (int z = 0; z < s.gz; ++z) {

@@ -88,14 +88,22 @@ struct ProblemDesc {
   int64_t red_ld;         // row stride of a partial, elements
   int32_t a_3d, b_3d;     // MN-major operand whose tile comes in one 3-D box
   int32_t fast_bf16;      // bf16 output, no partials, every row 32-byte aligned
+  // The reduction of every tile runs through `chain` block products in
+  // order, tensor-map pairs map0 .. map0+chain-1 (map_nk[] steps each), all
+  // into one accumulator: the virtual grid's sum over the reduced axis kept
+  // in TMEM.  chain = 1 for a single product.  num_k is the chain's total.
+  int32_t chain;
+  int32_t map0;
 };
 
 template <int MAXP>
 struct GemmParams {
-  CUtensorMap tma[MAXP];  // A operand of each problem
-  CUtensorMap tmb[MAXP];  // B operand of each problem
+  CUtensorMap tma[MAXP];  // A operand of each block product (map index)
+  CUtensorMap tmb[MAXP];  // B operand of each block product
+  int32_t map_nk[MAXP];   // 64-deep reduction steps of each block product
   ProblemDesc prob[MAXP];
   int32_t num_problems;
+  int32_t num_maps;
   int32_t total_tiles;
   int32_t group_m;     // tile rows per rasterisation group
   int32_t inject;      // test-only: 1 = the producer withholds every load
@@ -195,6 +203,37 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
 struct TileCoord {
   int p, m_blk, n_blk;
 };
+
+// Where reduction step k of a problem falls in its chain of block products:
+// member g, step kl of that member's nk steps.
+struct ChainPos {
+  int g, kl, nk;
+};
+
+template <int MAXP>
+__device__ __forceinline__ ChainPos chain_start(const GemmParams<MAXP>& P, const ProblemDesc& d,
+                                                int k) {
+  ChainPos c{0, k, P.map_nk[d.map0]};
+#pragma unroll 1
+  while (c.g + 1 < d.chain && c.kl >= c.nk) {
+    c.kl -= c.nk;
+    ++c.g;
+    c.nk = P.map_nk[d.map0 + c.g];
+  }
+  return c;
+}
+
+// Moves to the next reduction step; true when it starts the next member
+// (whose tensor maps the producer then loads from).
+template <int MAXP>
+__device__ __forceinline__ bool chain_next(const GemmParams<MAXP>& P, const ProblemDesc& d,
+                                           ChainPos& c) {
+  if (++c.kl < c.nk || c.g + 1 >= d.chain) return false;
+  ++c.g;
+  c.kl = 0;
+  c.nk = P.map_nk[d.map0 + c.g];
+  return true;
+}
 
 template <int MAXP>
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams<MAXP>& P, int t) {
@@ -567,7 +606,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int p = 0; p < P.num_problems; ++p) {
+    for (int p = 0; p < P.num_maps; ++p) {
       prefetch_tmap(&P.tma[p]);
       prefetch_tmap(&P.tmb[p]);
     }
@@ -591,8 +630,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       for_each_work(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
-        const CUtensorMap* ma = &P.tma[tc.p];
-        const CUtensorMap* mb = &P.tmb[tc.p];
+        ChainPos cp = chain_start(P, d, k0);
+        const CUtensorMap* ma = &P.tma[d.map0 + cp.g];
+        const CUtensorMap* mb = &P.tmb[d.map0 + cp.g];
         const int m0 = tc.m_blk * kTileM;
         const int n0 = tc.n_blk * BN;
         const int kend = k1 < 0 ? d.num_k : k1;
@@ -601,7 +641,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
             return false;
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, L::kStageBytes);
-          const int r0 = k * BK;
+          const int r0 = cp.kl * BK;
           // An MN-major tile is (rows or columns / 64) chunks of BK rows of
           // 128 B; with a 3-D tensor map {64, R, MN/64} one box brings all of
           // them (fewer TMA operations per stage), else one box per chunk.
@@ -627,6 +667,10 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
               tma_load_2d(b_tile(stage) + h * (BK * 128), mb, fb, n0 + 64 * h, r0);
           } else {
             tma_load_2d(b_tile(stage), mb, fb, r0, n0);
+          }
+          if (chain_next(P, d, cp)) {
+            ma = &P.tma[d.map0 + cp.g];
+            mb = &P.tmb[d.map0 + cp.g];
           }
           ++loads;
           if (++stage == STAGES) {

@@ -90,7 +90,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
     fence_mbarrier_init();
   }
   if (warp == 0 && lane == 0) {
-    for (int p = 0; p < P.num_problems; ++p) {
+    for (int p = 0; p < P.num_maps; ++p) {
       prefetch_tmap(&P.tma[p]);
       prefetch_tmap(&P.tmb[p]);
     }
@@ -116,8 +116,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       for_each_work(P, pair, num_pairs, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
-        const CUtensorMap* ma = &P.tma[tc.p];
-        const CUtensorMap* mb = &P.tmb[tc.p];
+        ChainPos cp = chain_start(P, d, k0);
+        const CUtensorMap* ma = &P.tma[d.map0 + cp.g];
+        const CUtensorMap* mb = &P.tmb[d.map0 + cp.g];
         const int m0 = tc.m_blk * kTileM + static_cast<int>(rank) * kCtaM;
         const int n0 = tc.n_blk * BN + static_cast<int>(rank) * (BN / 2);
         const int kend = k1 < 0 ? d.num_k : k1;
@@ -126,7 +127,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
             return false;
           if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * L::kStageBytes);
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
-          const int r0 = k * kBK;
+          const int r0 = cp.kl * kBK;
           if (d.a_3d) {
             tma_load_3d_pair(a_tile(stage), ma, fb, 0, r0, m0 / 64);
           } else
@@ -148,6 +149,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
               tma_load_2d_pair(b_tile(stage) + h * (kBK * 128), mb, fb, n0 + 64 * h, r0);
           } else {
             tma_load_2d_pair(b_tile(stage), mb, fb, r0, n0);
+          }
+          if (chain_next(P, d, cp)) {
+            ma = &P.tma[d.map0 + cp.g];
+            mb = &P.tmb[d.map0 + cp.g];
           }
           ++loads;
           if (++stage == STAGES) {

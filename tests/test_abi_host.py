@@ -86,14 +86,16 @@ def test_block_range_errors(fc):
 def test_workspace_size(fc):
     s = fc.Shape(8192, 6144, 24576, (2, 2, 2))
     assert fc.axonn_fc_workspace_size("fwd", s, 0) == 0
-    assert fc.axonn_fc_workspace_size("fwd", s, fc.VGRID) == 1 * 8192 * 24576 * 4
-    assert fc.axonn_fc_workspace_size("dgrad", s, fc.VGRID) == 1 * 8192 * 6144 * 4
-    assert fc.axonn_fc_workspace_size("wgrad", s, fc.VGRID) == 1 * 6144 * 24576 * 4
+    P = fc.VGRID | fc.VGRID_PARTIALS   # the two-launch form keeps G-1 partials
+    assert fc.axonn_fc_workspace_size("fwd", s, fc.VGRID) == 0   # chained: none
+    assert fc.axonn_fc_workspace_size("fwd", s, P) == 1 * 8192 * 24576 * 4
+    assert fc.axonn_fc_workspace_size("dgrad", s, P) == 1 * 8192 * 6144 * 4
+    assert fc.axonn_fc_workspace_size("wgrad", s, P) == 1 * 6144 * 24576 * 4
     s4 = fc.Shape(4096, 16384, 18432, (1, 4, 4))
-    assert fc.axonn_fc_workspace_size("fwd", s4, fc.VGRID) == 0      # G_x = 1
-    assert fc.axonn_fc_workspace_size("dgrad", s4, fc.VGRID) == 3 * 4096 * 16384 * 4
+    assert fc.axonn_fc_workspace_size("fwd", s4, P) == 0      # G_x = 1
+    assert fc.axonn_fc_workspace_size("dgrad", s4, P) == 3 * 4096 * 16384 * 4
     odd = fc.Shape(100, 60, 1001, (1, 1, 3))
-    assert fc.axonn_fc_workspace_size("wgrad", odd, fc.VGRID) == 2 * 60 * 1008 * 4
+    assert fc.axonn_fc_workspace_size("wgrad", odd, P) == 2 * 60 * 1008 * 4
 
 
 def _status(fc, fn, *args):
@@ -120,7 +122,10 @@ FAKE = 0x10000000  # never dereferenced: every case below fails validation
     (dict(shape=(64, 64, 64), ldp=32), 1),
     (dict(shape=(64, 64, 64), C=FAKE + 4), 2),
     (dict(shape=(64, 64, 64), P=0), 1),
-    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x8), 4),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x8 | 0x100), 4),
+    # the two-launch grid sum needs the virtual grid and excludes the order-free one
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x100), 1),
+    (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x8 | 0x100 | 0x80 | 0x4), 1),
     # the order-free sum needs the virtual grid and an accumulating fp32 output
     (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80), 1),
     (dict(shape=(64, 64, 64), grid=(2, 1, 1), flags=0x80 | 0x8), 1),
@@ -153,14 +158,15 @@ def test_reduce_add_needs_no_workspace(fc):
     s = fc.Shape(64, 64, 64, (2, 2, 2))
     f = fc.VGRID | fc.ACCUM_F32
     for op in ("fwd", "dgrad", "wgrad"):
-        assert fc.axonn_fc_workspace_size(op, s, f) == 1 * 64 * 64 * 4
+        assert fc.axonn_fc_workspace_size(op, s, f | fc.VGRID_PARTIALS) == 1 * 64 * 64 * 4
+        assert fc.axonn_fc_workspace_size(op, s, f) == 0
         assert fc.axonn_fc_workspace_size(op, s, f | fc.REDUCE_ADD) == 0
     torch = pytest.importorskip("torch")
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, s, f | fc.REDUCE_ADD)
     assert st in (fc.ERR_CUDA, fc.ERR_UNSUPPORTED), fc.axonn_last_error()
-    st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, s, f)
+    st = _raw(fc, "axonn_fc_fwd", FAKE, FAKE, FAKE, 64, 64, 64, s, f | fc.VGRID_PARTIALS)
     assert st == fc.ERR_WORKSPACE
 
 

@@ -76,11 +76,13 @@ def test_gpt_block_h6144_t8192(cuda_lib, gpt6144, layer, op):
                    seed=zlib.crc32(f"{layer}:{op}".encode()) & 0xFFFF)
 
 
+@pytest.mark.parametrize("form", ["chained", "partials"])
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
-def test_gpt_block_vgrid_2x2x2_up(cuda_lib, gpt6144, op):
+def test_gpt_block_vgrid_2x2x2_up(cuda_lib, gpt6144, op, form):
     K, N = LAYERS6["up"]
     X, W, dY = gpt6144["up"]
-    _run_and_check(cuda_lib, op, X, W, dY, T6, K, N, grid=(2, 2, 2), flags=cuda_lib.VGRID,
+    flags = cuda_lib.VGRID | (cuda_lib.VGRID_PARTIALS if form == "partials" else 0)
+    _run_and_check(cuda_lib, op, X, W, dY, T6, K, N, grid=(2, 2, 2), flags=flags,
                    n_random=32768, seed=7)
 
 
@@ -125,11 +127,13 @@ def test_large_h16384_full(cuda_lib, large16384, layer, op):
     _run_and_check(cuda_lib, op, X, W, dY, T, K, N, n_random=8192, seed=13)
 
 
+@pytest.mark.parametrize("form", ["chained", "partials"])
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
-def test_large_h16384_vgrid_1x4x4_up(cuda_lib, large16384, op):
+def test_large_h16384_vgrid_1x4x4_up(cuda_lib, large16384, op, form):
     T, K, N = 4096, 16384, 53248
     X, W, dY = large16384["up"]
-    _run_and_check(cuda_lib, op, X, W, dY, T, K, N, grid=(1, 4, 4), flags=cuda_lib.VGRID,
+    flags = cuda_lib.VGRID | (cuda_lib.VGRID_PARTIALS if form == "partials" else 0)
+    _run_and_check(cuda_lib, op, X, W, dY, T, K, N, grid=(1, 4, 4), flags=flags,
                    n_random=8192, seed=17)
 
 

@@ -58,30 +58,83 @@ def test_config1_single_layer_random(cuda_lib, forced, op):
     assert_within_bound(host_f64(out), C, S, f"config1 {op}")
 
 
+# The virtual grid's two fixed-order sums: the G block products of a tile
+# chained into one accumulator (default), or fp32 partials in the workspace
+# summed in the last block's epilogue (AXONN_VGRID_PARTIALS).
+FORMS = ["chained", "partials"]
+
+
+def _vgrid_flags(fc, form):
+    return fc.VGRID | (fc.VGRID_PARTIALS if form == "partials" else 0)
+
+
+@pytest.mark.parametrize("form", FORMS)
 @pytest.mark.parametrize("forced", CONFIGS, indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("grid", [(2, 2, 2), (1, 4, 4), (3, 1, 2), (2, 3, 1)])
-def test_vgrid_integer_exact(cuda_lib, forced, op, grid):
+def test_vgrid_integer_exact(cuda_lib, forced, op, grid, form):
     T, K, N = 300, 200, 520
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, False, seed=31, kind="int")
     Q = make_operand(qn, T, K, N, False, seed=31, kind="int")
-    out = run_gpu(cuda_lib, op, P, Q, False, False, T, K, N, grid=grid, extra=cuda_lib.VGRID)
+    out = run_gpu(cuda_lib, op, P, Q, False, False, T, K, N, grid=grid,
+                  extra=_vgrid_flags(cuda_lib, form))
     C, _ = oracle.fc_vgrid(op, P, Q, False, False, T, K, N, grid)
     assert np.array_equal(host_bits(out), oracle.bf16_rne(C))
 
 
+@pytest.mark.parametrize("forced", [1, 2, 5, 6], indirect=True)
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
-def test_vgrid_random_config3_shape_scaled(cuda_lib, op):
+@pytest.mark.parametrize("p_t,q_t", LAYOUTS)
+@pytest.mark.parametrize("grid,TKN", [((2, 2, 2), (520, 384, 776)), ((3, 1, 2), (300, 1000, 257)),
+                                      ((1, 4, 4), (1024, 200, 640)), ((4, 2, 1), (129, 1000, 520))])
+def test_vgrid_chain_layouts_and_ragged_blocks(cuda_lib, forced, op, p_t, q_t, grid, TKN):
+    """Chained block products in every storage layout, with block extents
+    that are not tile multiples (so every member's tensor maps zero-fill at
+    its own edges) and members of unequal reduction length: bitwise."""
+    T, K, N = TKN
+    pn, qn = operand_names(op)
+    P = make_operand(pn, T, K, N, p_t, seed=33, kind="int")
+    Q = make_operand(qn, T, K, N, q_t, seed=33, kind="int")
+    out = run_gpu(cuda_lib, op, P, Q, p_t, q_t, T, K, N, grid=grid, extra=cuda_lib.VGRID)
+    assert cuda_lib.axonn_last_kernel_config() == forced
+    C, _ = oracle.fc_vgrid(op, P, Q, p_t, q_t, T, K, N, grid)
+    bad = np.argwhere(host_bits(out) != oracle.bf16_rne(C))
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+def test_vgrid_chained_needs_no_workspace(cuda_lib):
+    """The chained sum keeps the partials in TMEM: no workspace is asked for
+    or passed, and the result is exact."""
+    fc = cuda_lib
+    T, K, N = 300, 200, 520
+    for op in ("fwd", "dgrad", "wgrad"):
+        assert fc.axonn_fc_workspace_size(op, fc.Shape(T, K, N, (2, 2, 2)), fc.VGRID) == 0
+        assert fc.axonn_fc_workspace_size(op, fc.Shape(T, K, N, (2, 2, 2)),
+                                          fc.VGRID | fc.VGRID_PARTIALS) > 0
+    X = make_operand("X", T, K, N, False, seed=35, kind="int")
+    W = make_operand("W", T, K, N, False, seed=35, kind="int")
+    import torch
+    from fc_cases import to_device
+    out = torch.zeros((T, N), dtype=torch.bfloat16, device="cuda")
+    fc.axonn_fc_fwd(to_device(X), to_device(W), out, fc.Shape(T, K, N, (4, 1, 1)), fc.VGRID, None)
+    fc.axonn_sync_status()
+    assert np.array_equal(host_bits(out), oracle.bf16_rne(oracle.fc_fwd(X, W)[0]))
+
+
+@pytest.mark.parametrize("form", FORMS)
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_vgrid_random_config3_shape_scaled(cuda_lib, op, form):
     """2x2x2 grid on an H=768, T=1024 layer (config-3 structure, scaled)."""
     T, K, N = 1024, 768, 3072
     grid = (2, 2, 2)
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, False, seed=1003)
     Q = make_operand(qn, T, K, N, False, seed=1003)
-    out = run_gpu(cuda_lib, op, P, Q, False, False, T, K, N, grid=grid, extra=cuda_lib.VGRID)
+    out = run_gpu(cuda_lib, op, P, Q, False, False, T, K, N, grid=grid,
+                  extra=_vgrid_flags(cuda_lib, form))
     C, S = oracle.fc_vgrid(op, P, Q, False, False, T, K, N, grid)
-    assert_within_bound(host_f64(out), C, S, f"vgrid {op}")
+    assert_within_bound(host_f64(out), C, S, f"vgrid {op} {form}")
 
 
 @pytest.mark.parametrize("forced", CONFIGS, indirect=True)
@@ -137,14 +190,15 @@ def test_wgrad_accumulate_f32(cuda_lib):
     assert np.array_equal(host_f64(out), host_f64(C0) + C)
 
 
-def test_vgrid_accumulate_f32(cuda_lib):
+@pytest.mark.parametrize("form", FORMS)
+def test_vgrid_accumulate_f32(cuda_lib, form):
     import torch
     T, K, N = 300, 200, 520
     X = make_operand("X", T, K, N, False, seed=53, kind="int")
     W = make_operand("W", T, K, N, False, seed=53, kind="int")
     out = torch.full((T, N), 3.0, dtype=torch.float32, device="cuda")
     run_gpu(cuda_lib, "fwd", X, W, False, False, T, K, N, grid=(2, 2, 2),
-            extra=cuda_lib.VGRID | cuda_lib.ACCUM_F32, out=out)
+            extra=_vgrid_flags(cuda_lib, form) | cuda_lib.ACCUM_F32, out=out)
     C, _ = oracle.fc_fwd(X, W)
     assert np.array_equal(host_f64(out), C + 3.0)
 

@@ -103,7 +103,7 @@ def test_reduce_add_random_config3_shape_scaled(cuda_lib, op):
     b64 = base.double().numpy()
     for red in (True, False):       # order-free, then the fixed-order sum
         out = base.cuda()
-        extra = fc.VGRID | fc.ACCUM_F32 | (fc.REDUCE_ADD if red else 0)
+        extra = fc.VGRID | fc.ACCUM_F32 | (fc.REDUCE_ADD if red else fc.VGRID_PARTIALS)
         run_gpu(fc, op, P, Q, False, False, T, K, N, grid=grid, extra=extra, out=out)
         assert_within_bound(host_f64(out), C + b64, S + np.abs(b64),
                             f"{op} {'order-free' if red else 'fixed order'}")
@@ -144,8 +144,9 @@ def test_reduce_add_repeat_and_graph(cuda_lib):
 
 def test_reduce_add_static_entry_point_needs_no_scratch(cuda_lib):
     """A product whose fixed-order partial (one slot of 4096 x 8192 fp32 =
-    128 MiB on a 2x1x1 grid) exceeds the built-in 64 MiB scratch: refused
-    without AXONN_REDUCE_ADD, exact with it."""
+    128 MiB on a 2x1x1 grid) exceeds the built-in 64 MiB scratch: refused in
+    the two-launch form (AXONN_VGRID_PARTIALS), exact with AXONN_REDUCE_ADD
+    and in the chained form, which need no scratch."""
     import torch
     fc = cuda_lib
     T, K, N = 4096, 64, 8192
@@ -156,7 +157,7 @@ def test_reduce_add_static_entry_point_needs_no_scratch(cuda_lib):
     out = torch.zeros((T, N), dtype=torch.float32, device="cuda")
     shape = fc.Shape(T, K, N, grid)
     with pytest.raises(fc.AxonnError) as ei:
-        fc.axonn_fc_vgrid_static("fwd", Xd, Wd, out, shape, fc.ACCUM_F32)
+        fc.axonn_fc_vgrid_static("fwd", Xd, Wd, out, shape, fc.ACCUM_F32 | fc.VGRID_PARTIALS)
     assert ei.value.status == fc.ERR_WORKSPACE
     fc.axonn_fc_vgrid_static("fwd", Xd, Wd, out, shape, fc.ACCUM_F32 | fc.REDUCE_ADD)
     fc.axonn_sync_status()
@@ -164,6 +165,10 @@ def test_reduce_add_static_entry_point_needs_no_scratch(cuda_lib):
     got = host_f64(out[torch.from_numpy(I).cuda(), torch.from_numpy(J).cuda()])
     C, _ = oracle.fc_entries("fwd", X, W, False, False, I, J)
     assert np.array_equal(got, C)
+    fc.axonn_fc_vgrid_static("fwd", Xd, Wd, out, shape, fc.ACCUM_F32)   # chained: adds again
+    fc.axonn_sync_status()
+    got = host_f64(out[torch.from_numpy(I).cuda(), torch.from_numpy(J).cuda()])
+    assert np.array_equal(got, 2 * C)
 
 
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
