@@ -87,12 +87,28 @@ WORKLOADS = {
 }
 DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 
-# DRAM traffic of the GEMM kernel from one ncu capture of the default
-# workload (dram__bytes_read.sum + dram__bytes_write.sum over the 12 launches
-# of one tuned step; summary and command in profiles/).  It is reported only
-# while the kernel sources hash to the value the capture was taken with.
-TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": "b3d3f66be45e8d80",
-           "bytes_per_step": (20398.4 + 2697.9) * 1e6, "launches_per_step": 12}
+# DRAM traffic of the GEMM kernel from ncu captures of the default workload:
+# dram__bytes_read.sum + dram__bytes_write.sum of each GEMM ("layer:op") in
+# each tuned choice ("config/group/stream-K tiles") captured (summary and command
+# in profiles/).  Reported only while the kernel sources hash to the value
+# the capture was taken with and every GEMM's choice of this run is in it.
+TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": None, "bytes": {}}
+
+
+def traffic_per_launch(workload, per, only):
+    """Mean DRAM bytes per GEMM launch of the step from the captured table,
+    or None when a GEMM's choice (or the kernel sources) was not captured."""
+    if workload != TRAFFIC["workload"] or only is not None or not per:
+        return None
+    if kernel_sources_hash() != TRAFFIC["kernel_sources"]:
+        return None
+    tot = 0.0
+    for p in per:
+        key = (f"{p['layer']}:{p['op']}", f"{p['config']}/{p['group_m']}/{p['streamk_tiles']}")
+        if key not in TRAFFIC["bytes"]:
+            return None
+        tot += TRAFFIC["bytes"][key]
+    return tot / len(per)
 
 
 def kernel_sources_hash():
@@ -148,14 +164,17 @@ def host_inputs(wl, layers):
 
 def device_inputs(wl, layers, dev):
     """Seeded bf16 operands drawn on the device (for workloads too large to
-    draw on the host in a benchmark run)."""
+    draw on the host in a benchmark run), with the workload's distributions:
+    activations and gradients N(0,1), weights N(0,0.02), or every operand
+    N(0,1) times the workload's scale."""
     import torch
     g = torch.Generator(device=dev)
     g.manual_seed(wl["seed"])
-    scale = wl.get("scale") or 1.0
+    scale = wl.get("scale")
     out = {}
     for name, T, K, N in layers:
-        out[name] = {k: (torch.randn(shape, generator=g, device=dev) * scale).to(torch.bfloat16)
+        out[name] = {k: (torch.randn(shape, generator=g, device=dev)
+                         * (scale or (0.02 if k == "W" else 1.0))).to(torch.bfloat16)
                      for k, shape in (("X", (T, K)), ("W", (K, N)), ("dY", (T, N)))}
     return out
 
@@ -419,30 +438,19 @@ def max_over_ranks(value, device):
 
 
 # ------------------------------------------------------------------ GPU arm
-def run_ours(args):
+def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_device=False):
+    """Times one GEMM workload: inputs, per-shape tuning, warm-up, then
+    `steps` CUDA-graph replays of a step (or eager steps with --no-graph)
+    and of each GEMM alone, with clocks sampled over the timed region.
+    Returns the state the caller reports from (a namespace)."""
+    import types
+
     import torch
     import torch.distributed as dist
 
     import fc_inputs
-    import pmm_fc_layer_gb300 as fc
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
-    dev = torch.device("cuda", torch.cuda.current_device())
-
-    from pmm_fc_layer_gb300 import build as _b
-    _b.build()
-    fc.load()
-    fc.axonn_set_kernel_config(args.config)
-    sms, max_pairs = fc.axonn_device_info()
-
-    wl = WORKLOADS[args.workload]
+    only = tuple(args.only.split(":")) if args.only and wl_name == args.workload else None
+    wl = WORKLOADS[wl_name]
     grid = wl.get("grid", (1, 1, 1))
     flags = fc.VGRID if grid != (1, 1, 1) else 0
     if args.accum_f32:
@@ -452,12 +460,15 @@ def run_ours(args):
     if args.vgrid_partials:
         flags |= fc.VGRID_PARTIALS
     out_dtype = torch.float32 if args.accum_f32 else torch.bfloat16
-    only = tuple(args.only.split(":")) if args.only else None
     layers = [l for l in wl["layers"] if only is None or l[0] == only[0]]
+    if args.shrink > 1 and wl_name == args.workload:
+        # a smaller case of the same kernels for profiling (not a bench line)
+        layers = [(n, max(8, T // args.shrink // 8 * 8), max(8, K // args.shrink // 8 * 8),
+                   max(8, N // args.shrink // 8 * 8)) for n, T, K, N in layers]
     glist = [g for g in gemms(layers) if only is None or (g[0], g[1]) == only]
 
     data = None
-    if wl.get("device_inputs"):
+    if wl.get("device_inputs") or on_device:
         dbuf = device_inputs(wl, layers, dev)
     else:
         data = host_inputs(wl, layers)
@@ -489,11 +500,14 @@ def run_ours(args):
 
     sk_tiles = [0] * len(plan)
 
+    swapped = [0] * len(plan)
+
     def call_gemm(gi):
         g = plan[gi]
         fc.call(g["op"], g["P"], g["Q"], g["C"], g["shape"], flags, ws, stream=stream)
         used[gi] = fc.axonn_last_choice()
         sk_tiles[gi] = fc.axonn_last_streamk_tiles()
+        swapped[gi] = fc.axonn_last_swap()
 
     def step(events=None):
         for gi in range(len(plan)):
@@ -505,15 +519,15 @@ def run_ours(args):
 
     # Per-shape tuning (outside every timed region): each GEMM's candidate
     # configurations are timed once and the fastest is kept by the library.
-    if args.tune_cache and os.path.exists(args.tune_cache):
-        fc.axonn_tune_cache_load(args.tune_cache)
+    if tune_cache and os.path.exists(tune_cache):
+        fc.axonn_tune_cache_load(tune_cache)
     elif not args.no_tune:
         with torch.cuda.stream(stream):
             for g in plan:
                 fc.axonn_fc_tune(g["op"], g["P"], g["Q"], g["C"], g["shape"], flags, ws,
                                  stream=stream)
-        if args.tune_cache:
-            fc.axonn_tune_cache_save(args.tune_cache)
+        if tune_cache:
+            fc.axonn_tune_cache_save(tune_cache)
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
             step()
@@ -522,8 +536,8 @@ def run_ours(args):
     fc.axonn_sync_status(stream)
 
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in plan]
-          for _ in range(args.steps)]
-    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+          for _ in range(steps)]
+    step_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
     gpu_index = int(vis) if vis.isdigit() else local
     if world > 1:
@@ -549,7 +563,7 @@ def run_ours(args):
         torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clocks:
         with torch.cuda.stream(stream):
-            for s in range(args.steps):
+            for s in range(steps):
                 step_ev[s][0].record(stream)
                 if args.no_graph:
                     step(ev[s])
@@ -560,7 +574,7 @@ def run_ours(args):
                     flush.fill_(1)        # outside the step's events
             if not args.no_graph:
                 for gi, gg in enumerate(gemm_graphs):
-                    for s in range(args.steps):
+                    for s in range(steps):
                         ev[s][gi][0].record(stream)
                         gg.replay()
                         ev[s][gi][1].record(stream)
@@ -574,7 +588,7 @@ def run_ours(args):
     split_reduces = sum(1 for u in used if u and u[1] > 1)
     sk_zeroing = sum(1 for t in sk_tiles if t > 0)   # the counter-zeroing kernel of a stream-K call
     # timed steps, plus (with graphs) the per-GEMM replays
-    launches = (args.steps * (len(plan) + reduce_launches + split_reduces + sk_zeroing)
+    launches = (steps * (len(plan) + reduce_launches + split_reduces + sk_zeroing)
                 * (1 if args.no_graph else 2))
 
     peaks = read_peaks()
@@ -582,7 +596,7 @@ def run_ours(args):
     gemm_ms_total = 0.0
     flops_per_step = sum(g["flops"] for g in plan)
     for gi, g in enumerate(plan):
-        ms = [ev[s][gi][0].elapsed_time(ev[s][gi][1]) for s in range(args.steps)]
+        ms = [ev[s][gi][0].elapsed_time(ev[s][gi][1]) for s in range(steps)]
         gemm_ms_total += sum(ms)
         med = statistics.median(ms)
         # the pages' own style: the mean of the last 8 of 10 runs
@@ -599,14 +613,263 @@ def run_ours(args):
                     "mean_last8_of_10_ms": round(last8, 4) if last8 is not None else None,
                     "config": fc.axonn_kernel_config_name(used[gi][0]),
                     "split": used[gi][1], "group_m": used[gi][2],
-                    "streamk_tiles": sk_tiles[gi]})
+                    "streamk_tiles": sk_tiles[gi], "swap": swapped[gi]})
+    # Exchanged operand roles, forced off and on, each GEMM in its tuned
+    # configuration otherwise (a comparison, after the timed region).
+    if getattr(args, "swap_compare", False) and not args.no_graph:
+        for mode in (0, 1):
+            fc.axonn_set_swap(mode)
+            for gi in range(len(plan)):
+                gg = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gg, stream=stream):
+                    call_gemm(gi)
+                applied = swapped[gi]
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                with torch.cuda.stream(stream):
+                    gg.replay()
+                    e0.record(stream)
+                    for _ in range(5):
+                        gg.replay()
+                    e1.record(stream)
+                torch.cuda.synchronize()
+                per[gi][f"ms_swap{mode}"] = round(e0.elapsed_time(e1) / 5, 4)
+                if mode == 1:
+                    per[gi]["swap_applies"] = applied
+        fc.axonn_set_swap(-1)
+        fc.axonn_sync_status(stream)
+
     # The dominant kernel's rate: with graphs the timed step is nothing but
     # this library's GEMM launches back to back, so the step's device time is
     # their summed duration; eagerly, the sum of the per-call events.
     if args.no_graph:
-        achieved = flops_per_step * args.steps / (gemm_ms_total * 1e9)
+        achieved = flops_per_step * steps / (gemm_ms_total * 1e9)
     else:
-        achieved = flops_per_step * args.steps / (elapsed_ms * 1e9)
+        achieved = flops_per_step * steps / (elapsed_ms * 1e9)
+
+    return types.SimpleNamespace(**{k: v for k, v in locals().items() if k != "types"})
+
+
+def sampled_check(m, fc, row_band=256, col_band=512, seed=11):
+    """A lighter whole-output check for the workloads object: every GEMM of
+    the step at one random row per `row_band` rows x one random column per
+    `col_band` columns (plus the first and last row and column), against the
+    fp64 oracle.  Operand rows and columns are copied from the device
+    tensors the GEMMs read (the seeded inputs), so workloads drawn on the
+    device are covered too.  Returns (worst error ratio, entries)."""
+    import numpy as np
+    import torch
+
+    import fc_inputs
+    import oracle
+    rng = np.random.default_rng(seed)
+    worst, entries = 0.0, 0
+    for g in m.plan:
+        A, a_t, B, b_t = oracle.operands(g["op"], g["P"], g["Q"], False, False)
+        M, N, _ = g["mnr"]
+        I, J = check_bands(M, N, rng, row_band, col_band)
+        ii = torch.from_numpy(I).to(A.device)
+        jj = torch.from_numpy(J).to(A.device)
+        Ab = fc_inputs.from_torch_bf16(A.index_select(1 if a_t else 0, ii))
+        Bb = fc_inputs.from_torch_bf16(B.index_select(0 if b_t else 1, jj))
+        C, S = oracle.gemm(Ab, a_t, Bb, b_t)
+        got = g["C"].index_select(0, ii).index_select(1, jj).to(torch.float64).cpu().numpy()
+        if m.flags & fc.ACCUM_F32:
+            continue      # accumulated outputs hold every step's sum
+        worst = max(worst, float(oracle.error_ratio(got, C, S).max()))
+        entries += C.size
+    return worst, entries
+
+
+def workload_summary(m, fc, check=True):
+    """One entry of the `workloads` object: the step's rate and fractions,
+    the clocks, and for shapes below the ridge point the HBM rate."""
+    peaks = m.peaks
+    tf = m.flops_per_step * m.steps / (m.elapsed_ms * 1e9)
+    ridge = peaks["burst"] * 1e12 / (peaks["hbm_gbs"] * 1e9)   # FLOP per byte
+    mem = [p for p in m.per if 2.0 * p["M"] * p["N"] * p["R"] / (
+        2.0 * (p["M"] * p["R"] + p["R"] * p["N"] + p["M"] * p["N"])) < ridge]
+    out = {"tflops": round(tf, 2), "frac_of_burst": round(tf / peaks["burst"], 4),
+           "frac_of_sustained": round(tf / peaks["sustained"], 4),
+           "ms_per_step": round(m.elapsed_ms / m.steps, 4), "gemms": len(m.plan),
+           "steps": m.steps, "sm_mhz": m.clocks.summary().get("sm_mhz"),
+           "clock_reasons": m.clocks.summary().get("reasons"),
+           "kernel_configs": sorted({p["config"] for p in m.per}),
+           "grid_sum": ("none" if m.grid == (1, 1, 1) else
+                        "two launches, fp32 partials" if m.flags & fc.VGRID_PARTIALS else
+                        "order-free reduction adds" if m.flags & fc.REDUCE_ADD else
+                        "chained in one accumulator"),
+           "l2": config_block(m.wl, "", 1)["l2"]}
+    if len(m.per) <= 12:
+        out["per_gemm_tflops"] = {f"{p['layer']}:{p['op']}": p["tflops"] for p in m.per}
+    else:
+        by_t = {}
+        for p in m.per:
+            by_t.setdefault(p["M"] if p["op"] != "wgrad" else p["R"], []).append(p["tflops"])
+        out["median_gemm_tflops_by_T"] = {str(t): round(statistics.median(v), 1)
+                                          for t, v in sorted(by_t.items())}
+        out["min_gemm_tflops"] = min(p["tflops"] for p in m.per)
+    if mem:
+        gbs = [p["gbs"] for p in mem]
+        out["below_ridge"] = {"gemms": len(mem), "max_gbs": max(gbs),
+                              "median_gbs": round(statistics.median(gbs), 1),
+                              "frac_of_hbm_max": round(max(gbs) / peaks["hbm_gbs"], 4),
+                              "rule": "algorithmic bytes 2(MR+RN+MN) over the median time; "
+                                      "shapes whose FLOP per byte is below the ridge point"}
+    if check:
+        worst, entries = sampled_check(m, fc)
+        out["check"] = {"max_error_ratio": worst, "entries": entries,
+                        "what": "every GEMM, one random row per 256-row band x one random "
+                                "column per 512-column band, plus first/last rows and columns; "
+                                "bound |C - C_ref| <= 1e-2 (|A|.|B|) + 1e-5"}
+    return out
+
+
+GOLDFISH = dict(name="goldfish_ce_t8192_v128256", B=4, S=2048, V=128256, k=2, h=13, seed=1007,
+                desc="Goldfish-masked cross-entropy and its gradient over bf16 logits: 4 "
+                     "sequences x 2048 tokens, a 128256-token vocabulary (the Llama-3 "
+                     "vocabulary of the models the pages train), k = 2, h = 13")
+
+
+def measure_goldfish(args, fc, dev, local, steps, check=True):
+    """Times the Goldfish loss (mask, rows, mean) on seeded synthetic logits
+    drawn on the device (N(0, 4)), token ids uniform over the vocabulary.
+    Algorithmic bytes per step: the kept rows' logits read once, every
+    gradient row written once (bf16), plus ids, labels and the per-token
+    outputs.  Returns the entry of the `workloads` object."""
+    import numpy as np
+    import torch
+
+    import fc_inputs
+    from oracle import goldfish as gf
+    c = GOLDFISH
+    B, S, V = getattr(args, "gf_batch", c["B"]), c["S"], c["V"]
+    T = B * S
+    rng = np.random.default_rng(c["seed"])
+    seqs = rng.integers(0, V, size=(B, S + 1))
+    ids = torch.from_numpy(seqs[:, :-1].astype(np.int32)).to(dev)
+    labels = torch.from_numpy(seqs[:, 1:].astype(np.int32)).to(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(c["seed"])
+    logits = (2.0 * torch.randn((T, V), generator=gen, device=dev)).to(torch.bfloat16)
+    dl = torch.empty((T, V), dtype=torch.bfloat16, device=dev)
+    keep = torch.empty(T, dtype=torch.uint8, device=dev)
+    tl = torch.empty(T, dtype=torch.float32, device=dev)
+    loss = torch.empty(1, dtype=torch.float32, device=dev)
+    kept = torch.empty(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step():
+        fc.axonn_goldfish_ce(logits, ids, labels, keep, tl, loss, kept, k=c["k"], h=c["h"],
+                             dlogits=dl, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    fc.axonn_sync_status(stream)
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0]
+    with ClockSampler(int(vis) if vis.isdigit() else local) as clocks:
+        with torch.cuda.stream(stream):
+            for s in range(steps):
+                ev[s][0].record(stream)
+                gr.replay()
+                ev[s][1].record(stream)
+        torch.cuda.synchronize()
+    fc.axonn_sync_status(stream)
+    ms = statistics.median(a.elapsed_time(b) for a, b in ev)
+    n = int(kept.item())
+    nbytes = 2.0 * n * V + 2.0 * T * V + T * (4 + 4 + 1 + 4)
+    peaks = read_peaks()
+    gbs = nbytes / ms / 1e6
+    out = {"desc": c["desc"], "ms_per_step": round(ms, 4), "gbs": round(gbs, 1),
+           "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "bound": "hbm",
+           "kept": n, "positions": T, "algorithmic_bytes_per_step": nbytes,
+           "launches_per_step": 3, "steps": steps,
+           "sm_mhz": clocks.summary().get("sm_mhz"),
+           "clock_reasons": clocks.summary().get("reasons"),
+           "timing": "CUDA-graph replays of one step (mask, rows, mean), median"}
+    if check:
+        # mask and count over every position; token losses and gradient rows
+        # on a sample of 24 positions, against the fp64 oracle
+        ids_h, lab_h = ids.cpu().numpy(), labels.cpu().numpy()
+        ref_keep = gf.goldfish_keep(ids_h, lab_h, c["k"], c["h"], vocab=V).reshape(-1)
+        sample = np.concatenate([np.arange(8), np.arange(T - 8, T), rng.choice(T, 8, replace=False)])
+        st = torch.from_numpy(sample).to(dev)
+        sample_bits = fc_inputs.from_torch_bf16(logits.index_select(0, st))
+        ref = gf.goldfish_ce(sample_bits, ids_h, lab_h, c["k"], c["h"], rows=sample)
+        g = dl.index_select(0, st).double().cpu().numpy()
+        tok = tl.index_select(0, st).double().cpu().numpy()
+        # bound of the gradient: bf16 rounding plus the fp32 softmax's error
+        # (logsumexp, the exponent's products, exp2), as the GPU tests derive
+        za = np.abs(fc_inputs.bf16_bits_to_f32(sample_bits).astype(np.float64))
+        lse = np.abs(ref["lse"])[:, None]
+        eps_p = 1e-5 + lse * 2.0 ** -22 + (za + lse) * 2.0 ** -23 + 2.0 ** -21
+        tol_g = (2.0 ** -8 * np.abs(ref["dlogits"])
+                 + (1 + 2.0 ** -8) * (ref["softmax"] * eps_p + 2.0 ** -23) / max(n, 1))
+        out["check"] = {
+            "mask_exact": bool(np.array_equal(keep.cpu().numpy(), ref_keep) and n == ref["n"]),
+            "token_loss_max_error_ratio": float(np.max(np.abs(tok - ref["token_loss"])
+                                                       / (1e-5 * (1 + np.abs(ref["lse"]))))),
+            "dlogits_max_error_ratio": float(np.max(np.abs(g - ref["dlogits"]) / tol_g)),
+            "what": "keep mask and count bit for bit over all positions; CE and gradient rows "
+                    "of 24 positions against the fp64 oracle (bounds 1e-5 (1 + |lse|) and "
+                    "2^-8 |g| + (p eps_p + 2^-23) / n; ratios <= 1 pass)"}
+    del logits, dl
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_workloads(args, fc, dev, world, local, skip):
+    """Every other configuration of the benchmark, each tuned and timed on
+    its own (fewer steps), for the `workloads` object of the default line."""
+    import torch
+    steps = min(args.steps, 10)
+    res = {}
+    for name in ("single_layer_t256", "single_layer_t256_warm", "gpt_h6144_t8192_vgrid_2x2x2",
+                 "large_h16384_t4096", "large_h16384_t4096_vgrid_1x4x4", "layout_sweep"):
+        if name == skip:
+            continue
+        m = measure(name, args, fc, dev, world, local, steps, on_device=True)
+        res[name] = {"desc": WORKLOADS[name]["desc"], **workload_summary(m, fc)}
+        del m
+        torch.cuda.empty_cache()
+    res[GOLDFISH["name"]] = measure_goldfish(args, fc, dev, local, steps)
+    return res
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import fc_inputs
+    import pmm_fc_layer_gb300 as fc
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    from pmm_fc_layer_gb300 import build as _b
+    _b.build()
+    fc.load()
+    fc.axonn_set_kernel_config(args.config)
+    sms, max_pairs = fc.axonn_device_info()
+
+    m = measure(args.workload, args, fc, dev, world, local, args.steps, tune_cache=args.tune_cache)
+    (wl, grid, flags, out_dtype, only, layers, glist, data, dbuf, plan, ws, flush, stream, used,
+     sk_tiles, elapsed_ms, launches, peaks, per, flops_per_step, achieved, clocks) = (
+        m.wl, m.grid, m.flags, m.out_dtype, m.only, m.layers, m.glist, m.data, m.dbuf, m.plan,
+        m.ws, m.flush, m.stream, m.used, m.sk_tiles, m.elapsed_ms, m.launches, m.peaks, m.per,
+        m.flops_per_step, m.achieved, m.clocks)
 
     # Context only, off the product path: the same products through
     # torch.matmul (cuBLAS), full layers, bf16 outputs, timed the same way.
@@ -760,10 +1023,12 @@ def run_ours(args):
                     if grid != (1, 1, 1) else "")),
             "per_gemm": per,
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
-                         "peak": peaks["sustained"], "unit": "TFLOP/s",
-                         "frac": round(achieved / peaks["sustained"], 4),
-                         "frac_of_burst": round(achieved / peaks["burst"], 4),
-                         "peak_source": f"{peaks['source']} (sustained; burst {peaks['burst']})",
+                         "peak": peaks["burst"], "unit": "TFLOP/s",
+                         "frac": round(achieved / peaks["burst"], 4),
+                         "frac_of_sustained": round(achieved / peaks["sustained"], 4),
+                         "peak_source": (f"{peaks['source']} burst (the timed region is "
+                                         f"{elapsed_ms / 1e3:.2f} s, a burst; sustained "
+                                         f"{peaks['sustained']})"),
                          "kernel": ("fc_gemm_tcgen05_kernel / fc_gemm_tcgen05_pair_kernel, "
                                     "every GEMM launch of the step in the configurations "
                                     "listed under device.kernel_configs") + (
@@ -773,11 +1038,12 @@ def run_ours(args):
                              "the second one's epilogue)" if flags & fc.VGRID_PARTIALS else
                              " (virtual grid: one launch per GEMM, each tile's block products "
                              "chained into one accumulator)" if flags & fc.VGRID else ""),
-                         "traffic": (TRAFFIC["bytes_per_step"] / TRAFFIC["launches_per_step"]
-                                     if args.workload == TRAFFIC["workload"] and only is None
-                                     and kernel_sources_hash() == TRAFFIC["kernel_sources"]
-                                     else None),
+                         "traffic": traffic_per_launch(args.workload, per, only),
                          "traffic_unit": "bytes per launch (mean over the step)",
+                         "traffic_rule": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of "
+                                          "each GEMM in the configuration the tuner chose here, "
+                                          "from the capture in profiles/; null when a choice or "
+                                          "the kernel sources differ from the capture's"),
                          "peak_at_clock": round(peak_at_clock, 1) if peak_at_clock else None,
                          "frac_at_clock": (round(achieved / peak_at_clock, 4)
                                            if peak_at_clock else None),
@@ -810,7 +1076,10 @@ def run_ours(args):
             "clocks": clk,
             **({"torch_matmul": torch_mm} if torch_mm is not None else {}),
         }
-        if only is not None:
+        if args.shrink > 1:
+            line["profile_case"] = (f"dimensions divided by {args.shrink}"
+                                    + (f", {only[0]}:{only[1]} only" if only else ""))
+        elif only is not None:
             line["profile_case"] = f"{only[0]}:{only[1]} only"
         elif data is not None and not args.no_cpu_baseline and world == 1 and args.accum_f32:
             # accumulated outputs hold the sum of every step: no row check
@@ -843,9 +1112,46 @@ def run_ours(args):
                          "full rows 0 and M-1, full columns 0 and N-1, and one random row per "
                          "32-row band x one random column per 64-column band (an entry in every "
                          "32 x 64 cell); bound |C - C_ref| <= 1e-2 * (|A|.|B|) + 1e-5")}
+        if (world == 1 and not args.no_workloads and only is None and args.shrink == 1
+                and args.workload == DEFAULT_WORKLOAD
+                and not (args.accum_f32 or args.order_free or args.vgrid_partials)):
+            # every other configuration, each on its own after the metric's
+            # workload, with fewer timed steps
+            del plan, dbuf, ws, m
+            torch.cuda.empty_cache()
+            t0 = time.perf_counter()
+            line["workloads"] = run_workloads(args, fc, dev, world, local, skip=args.workload)
+            line["workloads_seconds"] = round(time.perf_counter() - t0, 1)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    return 0
+
+
+def run_goldfish(args):
+    """The Goldfish-loss workload alone, as its own JSON line (HBM-bound)."""
+    import torch
+    import pmm_fc_layer_gb300 as fc
+    from pmm_fc_layer_gb300 import build as _b
+    torch.cuda.set_device(0)
+    _b.build()
+    fc.load()
+    dev = torch.device("cuda", 0)
+    r = measure_goldfish(args, fc, dev, 0, args.steps, check=not args.no_cpu_baseline)
+    peaks = read_peaks()
+    print(json.dumps({
+        "metric": "Goldfish-masked cross-entropy with gradient: HBM GB/s", "value": r["gbs"],
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": r["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 in/out, fp32 arithmetic",
+        "data": "synthetic, seeded: logits N(0,4) drawn on the device, token ids uniform",
+        "config": {"workload": f"{GOLDFISH['name']}: {GOLDFISH['desc']}"},
+        "roofline": {"bound": "hbm", "achieved": r["gbs"], "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": r["frac_of_hbm"], "traffic": None,
+                     "algorithmic_bytes": r["algorithmic_bytes_per_step"]},
+        "gpu_launches": 3 * args.steps, "detail": r,
+        **({"profile_case": f"{args.gf_batch} sequences instead of {GOLDFISH['B']}"}
+           if args.gf_batch != GOLDFISH["B"] else {})}), flush=True)
     return 0
 
 
@@ -940,7 +1246,8 @@ def main():
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["zsharded_h6144_2x2x2"],
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["zsharded_h6144_2x2x2",
+                                                               GOLDFISH["name"]],
                     default=DEFAULT_WORKLOAD)
     ap.add_argument("--config", type=int, default=-1,
                     help="force one kernel configuration (-1: the library's choice)")
@@ -959,6 +1266,16 @@ def main():
     ap.add_argument("--order-free", action="store_true",
                     help="virtual grid with --accum-f32: blocks added into the output by "
                          "atomics in one launch, instead of the fixed-order sum")
+    ap.add_argument("--shrink", type=int, default=1, metavar="S",
+                    help="divide the workload's dimensions by S (a profiling case; not a bench "
+                         "line)")
+    ap.add_argument("--gf-batch", type=int, default=GOLDFISH["B"], metavar="B",
+                    help="sequences of the Goldfish workload (smaller for profiling)")
+    ap.add_argument("--swap-compare", action="store_true",
+                    help="after the timed region, time every GEMM with the operand roles "
+                         "forced unexchanged and exchanged (per_gemm ms_swap0 / ms_swap1)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations after the default workload")
     ap.add_argument("--vgrid-partials", action="store_true",
                     help="virtual grid in its two-launch form: fp32 partials in a workspace, "
                          "summed in the last block's epilogue (default: chained)")
@@ -978,6 +1295,8 @@ def main():
         return run_reference(args)
     if args.workload == "zsharded_h6144_2x2x2":
         return run_zsharded(args)
+    if args.workload == GOLDFISH["name"]:
+        return run_goldfish(args)
     return run_ours(args)
 
 

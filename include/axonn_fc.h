@@ -220,13 +220,51 @@ axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void*
                                      uint32_t flags, cudaStream_t stream);
 
 /*
+ * Goldfish-loss masked cross-entropy over bf16 logits, with its gradient.
+ * Against memorisation the paper trains with Goldfish Loss, which leaves
+ * tokens out of the cross-entropy at random (pith.science review of arXiv
+ * 2502.08145, "What carries the argument"), with mask parameters k = 2 and
+ * h = 13 ("Assumptions & free parameters").  The rule, read from the
+ * method's own paper that the pages cite (Hans et al., arXiv 2406.10209):
+ *   label (b, t) is dropped when FNV-1a-64 of input_ids[b, t-h+1 .. t] (each
+ *   id as 4 little-endian bytes, oldest first) is 0 mod k; labels with
+ *   fewer than h tokens before them in their row are kept; k = 0 keeps all;
+ *   labels outside [0, vocab) are padding (neither kept nor counted).
+ *   CE_t = logsumexp(z_t) - z_t[y_t] (natural log, fp32 arithmetic)
+ *   loss = sum over kept t of CE_t / n, n = number kept (0 when n = 0)
+ *   dlogits_t = G_t (softmax(z_t) - e_{y_t}) / n  (zero rows where dropped)
+ * Arguments (DEVICE pointers, caller-owned; T = batch * seq positions in
+ * row-major (b, t) order):
+ *   logits      bf16 [T x vocab], leading dimension ld_logits (multiple of
+ *               8, 16-byte aligned base); rows of dropped labels are not read
+ *   input_ids   int32 [batch x seq], the tokens the windows are hashed from
+ *   labels      int32 [batch x seq], the token each position predicts
+ *   keep        out, uint8 [T]: 1 where the label counts
+ *   token_loss  out, fp32 [T]: CE_t where kept, 0 elsewhere
+ *   loss        out, fp32 [1]: the mean over kept labels (a fixed-order sum)
+ *   kept        out, int32 [1]: n
+ *   dlogits     out, bf16 [T x vocab] with ld_dlogits (same alignment), or
+ *               NULL for the loss alone
+ * 1 <= h <= 4096, k >= 0, vocab up to 8 x 49152.  Three kernel launches on
+ * `stream`, no workspace, no allocation.  A wait that expires is reported
+ * by axonn_sync_status.  AXONN_ERR_INVALID_ARG / _ALIGNMENT / _UNSUPPORTED
+ * as for the products.
+ */
+axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const int32_t* input_ids,
+                                 const int32_t* labels, int64_t batch, int64_t seq, int64_t vocab,
+                                 int32_t k, int32_t h, uint8_t* keep, float* token_loss,
+                                 float* loss, int32_t* kept, void* dlogits, int64_t ld_dlogits,
+                                 cudaStream_t stream);
+
+/*
  * Per-shape tuning -- the GB300 counterpart of the pages' "automated BLAS
  * kernel tuning" (TL;DR of the sciencestack.ai page; "The reading", review of
  * arXiv 2502.08145).  Runs this call once per candidate -- kernel
  * configuration x rasterisation group {8, 16 tile rows; 8, 16 tile columns,
  * written -8, -16}, every configuration for products that leave SMs idle
  * (with reduction splits {2, 4, 8} when workspace is given), the 128x256 and
- * 256-row configurations otherwise -- and times each (through a captured
+ * 256-row configurations otherwise, and the two best of them again with the
+ * operand roles exchanged (see axonn_set_swap) -- and times each (through a captured
  * CUDA graph where the stream allows it) relative to the default choice run
  * just before and after it, so clock drift under the power cap cancels.  The
  * call synchronises `stream`.  It
@@ -246,11 +284,12 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
 
 /* The tuning table as text, one JSON object per line:
  *   {"key": "...", "config": "<name>", "split": S, "group_m": G,
- *    "streamk": 0 | 1 | 2, "us": t}
+ *    "streamk": 0 | 1 | 2, "swap": 0 | 1, "us": t}
  * (S a whole number 1..8; G a whole number in -64..-1 or 1..64, tile rows
  * per rasterisation group, negative for tile columns; streamk: off, on for
  * a partial round at most a quarter full, on wherever it applies; a line
- * without it loads as 1).
+ * without it loads as 1; swap: operand roles exchanged, see axonn_set_swap;
+ * a line without it loads as 0).
  * save writes every entry; load merges a file's entries into the table
  * (AXONN_ERR_INVALID_ARG on an unreadable file or a malformed line, leaving
  * the table unchanged).  Host-only. */
@@ -345,6 +384,33 @@ int axonn_num_kernel_configs(void);
  * Not part of the source pages: it removes the idle SMs of the last wave.
  * AXONN_ERR_INVALID_ARG for another mode.  Host-only. */
 axonn_status_t axonn_set_streamk(int mode);
+
+/* Operand roles for later calls in this process: -1 = as tuned (default
+ * off), 0 = never exchanged, 1 = exchanged wherever it applies.  Exchanged,
+ * a call computes the transpose of its product, C^T = B^T . A^T: the second
+ * operand is read in the first operand's role (output rows) and the first
+ * in the second's, and the epilogue writes each tile back transposed, so
+ * the caller's output is the same matrix.  The tuner times the swap for the
+ * two best configurations of each call, the row-major BLAS counterpart of
+ * choosing among NN, NT and TN operand orders (the pages' "automated BLAS
+ * kernel tuning": TL;DR of the sciencestack.ai page; review of arXiv
+ * 2502.08145, "The reading").  It does not apply with a split reduction or
+ * AXONN_VGRID_PARTIALS.  Results may differ from the unswapped call in the
+ * last bit (another tile order of the same fp32 sums).  Host-only;
+ * AXONN_ERR_INVALID_ARG for another mode. */
+axonn_status_t axonn_set_swap(int mode);
+
+/* Programmatic dependent launch of the GEMM kernels (1, the default): each
+ * launch may start while the previous kernel in the stream finishes, so its
+ * barrier set-up, TMEM allocation and tensor-map prefetch overlap that
+ * kernel's last tiles; it reads and writes global memory only after the
+ * previous kernel has completed (griddepcontrol.wait), so stream order is
+ * kept.  0 launches them plainly.  Process-wide, host-only;
+ * AXONN_ERR_INVALID_ARG for another value. */
+axonn_status_t axonn_set_pdl(int on);
+
+/* 1 if the last call on this thread ran with exchanged operand roles. */
+int axonn_last_swap(void);
 
 /* Output tiles the last GEMM launch on this thread computed as stream-K
  * pieces (0: none).  Host-only. */

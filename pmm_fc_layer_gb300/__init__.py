@@ -30,13 +30,15 @@ OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_UNSUPPORTED, ERR_WORKSPACE, ERR_CUDA, ER
 STATUS_NAMES = ["OK", "INVALID_ARG", "ALIGNMENT", "UNSUPPORTED", "WORKSPACE", "CUDA", "TIMEOUT"]
 
 EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_static",
-           "axonn_shards_gather", "axonn_fc_wgrad_zsharded",
+           "axonn_shards_gather", "axonn_fc_wgrad_zsharded", "axonn_goldfish_ce",
            "axonn_fc_workspace_size", "axonn_fc_tune", "axonn_tune_cache_save",
            "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
            "axonn_last_choice",
            "axonn_block_range", "axonn_fc_block_extents", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs",
-           "axonn_set_streamk", "axonn_last_streamk_tiles", "axonn_device_info",
+           "axonn_set_streamk", "axonn_last_streamk_tiles", "axonn_set_swap", "axonn_last_swap",
+           "axonn_set_pdl",
+           "axonn_device_info",
            "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
            "axonn_version")
 
@@ -88,6 +90,9 @@ def load(path: str | None = None):
         lib.axonn_fc_wgrad_zsharded.argtypes = [vp, vp, ctypes.POINTER(vp), i64, i64, i64,
                                                 ctypes.POINTER(Shape), u32, vp, sz, vp]
         lib.axonn_fc_wgrad_zsharded.restype = ctypes.c_int
+        lib.axonn_goldfish_ce.argtypes = [vp, i64, vp, vp, i64, i64, i64, i32, i32, vp, vp, vp, vp,
+                                          vp, i64, vp]
+        lib.axonn_goldfish_ce.restype = ctypes.c_int
         lib.axonn_fc_vgrid_static.argtypes = [ctypes.c_int, vp, vp, vp, i64, i64, i64,
                                               ctypes.POINTER(Shape), u32, vp]
         lib.axonn_fc_vgrid_static.restype = ctypes.c_int
@@ -125,6 +130,12 @@ def load(path: str | None = None):
         lib.axonn_set_streamk.restype = ctypes.c_int
         lib.axonn_last_streamk_tiles.argtypes = []
         lib.axonn_last_streamk_tiles.restype = ctypes.c_int
+        lib.axonn_set_pdl.argtypes = [ctypes.c_int]
+        lib.axonn_set_pdl.restype = ctypes.c_int
+        lib.axonn_set_swap.argtypes = [ctypes.c_int]
+        lib.axonn_set_swap.restype = ctypes.c_int
+        lib.axonn_last_swap.argtypes = []
+        lib.axonn_last_swap.restype = ctypes.c_int
         lib.axonn_num_kernel_configs.restype = ctypes.c_int
         lib.axonn_device_info.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]
         lib.axonn_device_info.restype = ctypes.c_int
@@ -239,6 +250,21 @@ def axonn_fc_vgrid_static(op, P, Q, C, shape: Shape, flags: int = 0, ldp=None, l
     _check(st)
 
 
+def axonn_goldfish_ce(logits, input_ids, labels, keep, token_loss, loss, kept, k=2, h=13,
+                      dlogits=None, ld_logits=None, ld_dlogits=None, stream=None):
+    """Goldfish-masked cross-entropy of bf16 logits [B*S x V] for int32
+    input_ids / labels [B x S]: fills keep [B*S] (uint8), token_loss [B*S],
+    loss [1], kept [1] (int32) and, if given, dlogits (bf16, the gradient of
+    the mean loss)."""
+    B, S = input_ids.shape
+    V = logits.shape[1]
+    _check(load().axonn_goldfish_ce(_ptr(logits), _ld(logits, ld_logits), _ptr(input_ids),
+                                    _ptr(labels), B, S, V, int(k), int(h), _ptr(keep),
+                                    _ptr(token_loss), _ptr(loss), _ptr(kept), _ptr(dlogits),
+                                    _ld(dlogits, ld_dlogits) if dlogits is not None else 0,
+                                    _stream(stream)))
+
+
 def axonn_fc_tune(op, P, Q, C, shape: Shape, flags: int = 0, ws=None, ldp=None, ldq=None,
                   ldc=None, stream=None):
     """Time every candidate way to run this call and remember the fastest;
@@ -328,6 +354,21 @@ def axonn_set_streamk(mode: int):
 def axonn_last_streamk_tiles() -> int:
     """Stream-K tiles of the last GEMM launch on this thread (0: none)."""
     return int(load().axonn_last_streamk_tiles())
+
+
+def axonn_set_pdl(on: int):
+    """1 (default): GEMMs are programmatic dependent launches; 0: plain launches."""
+    _check(load().axonn_set_pdl(int(on)))
+
+
+def axonn_set_swap(mode: int):
+    """Operand roles: -1 as tuned, 0 never exchanged, 1 exchanged (C^T = B^T.A^T)."""
+    _check(load().axonn_set_swap(int(mode)))
+
+
+def axonn_last_swap() -> int:
+    """1 if the last call on this thread ran with exchanged operand roles."""
+    return int(load().axonn_last_swap())
 
 
 def axonn_device_info():

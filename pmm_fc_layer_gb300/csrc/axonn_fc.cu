@@ -21,6 +21,7 @@
 
 #include "axonn_fc.h"
 #include "gemm_kernel.cuh"
+#include "goldfish.h"
 #include "kernel_launch.h"
 
 namespace {
@@ -37,6 +38,7 @@ constexpr int kFewProblems = 8;
 thread_local std::string t_last_error;
 std::atomic<uint64_t> g_timeout_ns{4000000000ULL};
 std::atomic<int> g_inject{0};
+std::atomic<int> g_pdl{1};  // GEMMs launched as programmatic dependent launches
 
 axonn_status_t fail(axonn_status_t s, const char* fmt, ...) {
   char buf[512];
@@ -305,6 +307,7 @@ struct Block {
   // same M x N) whose products all add into one accumulator, in order; the
   // members after the head have chain = 0.  An ordinary block has chain = 1.
   int chain = 1;
+  bool out_t = false;          // computes the transpose (operand roles swapped)
   int phase = 1;               // 0: writes an fp32 partial that a phase-1 block reads
   int red_count = 0;           // partials to add in the epilogue (last partial only)
   const float* red_src = nullptr;
@@ -358,8 +361,10 @@ struct TuneChoice {
   int split = 1;
   int group_m = 16;
   int streamk = 1;  // StreamKMode (see configure_streamk)
+  int swap = 0;     // 1: run C^T = B^T . A^T (operand roles exchanged)
 };
 std::atomic<int> g_forced_streamk{-1};
+std::atomic<int> g_forced_swap{-1};
 thread_local TuneChoice t_last_choice;
 
 struct TuneEntry {
@@ -414,7 +419,8 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     d.red_src = b.red_src;
     d.red_stride = b.red_stride;
     d.red_ld = b.red_ld;
-    d.fast_bf16 = b.out_mode == axonn::kOutBF16 && b.red_count == 0 &&
+    d.out_t = b.out_t;
+    d.fast_bf16 = !b.out_t && b.out_mode == axonn::kOutBF16 && b.red_count == 0 &&
                   reinterpret_cast<uintptr_t>(b.C) % 32 == 0 && b.ldc % 16 == 0;
     d.a_3d = v.a_mn && b.M % 64 == 0;
     d.b_3d = v.b_mn && b.N % 64 == 0;
@@ -425,7 +431,7 @@ axonn_status_t fill_params(GemmParams<MAXP>& P, const OpView& v, const std::vect
     int64_t steps = 0, red = 0;
     for (size_t g = bi; g < next; ++g) {
       const Block& m = blocks[g];
-      if (m.M != b.M || m.N != b.N || (g > bi && m.chain != 0))
+      if (m.M != b.M || m.N != b.N || m.out_t != b.out_t || (g > bi && m.chain != 0))
         return fail(AXONN_ERR_INVALID_ARG, "chain members differ in output extent");
       if (m.R == 0) continue;
       if (nmaps >= MAXP) return fail(AXONN_ERR_UNSUPPORTED, "too many block products");
@@ -536,7 +542,7 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
   const int units = P.total_tiles < slots ? P.total_tiles : slots;
   st = configure_streamk(P, kConfigs[config], units, plan, stream);
   if (st != AXONN_OK) return st;
-  const cudaError_t e = axonn::kernels_launch<P1>(config, P, units, stream);
+  const cudaError_t e = axonn::kernels_launch<P1>(config, P, units, g_pdl.load() != 0, stream);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "GEMM launch: %s", cudaGetErrorString(e));
   return AXONN_OK;
 }
@@ -799,6 +805,8 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     const int forced_cfg = g_forced_config.load();
     if (forced_cfg >= 0) ch.config = forced_cfg;
   }
+  const int forced_sw = g_forced_swap.load();
+  if (forced_sw >= 0) ch.swap = forced_sw;
   const int forced_sk = g_forced_streamk.load();
   if (forced_sk >= 0) ch.streamk = forced_sk == 0 ? kStreamKOff : kStreamKAlways;
   if (ch.config < 0 || ch.config >= kNumConfigs) ch.config = choose_config(plan.blocks, *dev);
@@ -840,6 +848,22 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
       plan.blocks.push_back(b);
     }
   }
+  // Exchanged operand roles: C^T[N x M] = B^T . A^T, the same operands read
+  // through each other's tensor-map role, written back transposed by the
+  // epilogue.  Not with a split reduction or the two-launch grid sum, whose
+  // fp32 partials are laid out in the caller's orientation.
+  OpView lv = v;
+  if (ch.swap && (ch.split > 1 || partials)) ch.swap = 0;
+  if (ch.swap) {
+    lv.A = v.B; lv.lda = v.ldb; lv.a_mn = v.b_mn;
+    lv.B = v.A; lv.ldb = v.lda; lv.b_mn = v.a_mn;
+    lv.M = v.N; lv.N = v.M;
+    for (Block& b : plan.blocks) {
+      std::swap(b.A, b.B);
+      std::swap(b.M, b.N);
+      b.out_t = true;
+    }
+  }
   plan.config = ch.config;
   plan.group_m = ch.group_m;
   if (!vgrid && ch.split == 1) {
@@ -855,11 +879,11 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   last.blocks.clear();
   for (const Block& b : plan.blocks) (b.phase == 0 ? first : last).blocks.push_back(b);
   if (!first.blocks.empty()) {
-    st = run_blocks(v, first, *dev, stream);
+    st = run_blocks(lv, first, *dev, stream);
     if (st != AXONN_OK) return st;
   }
   if (!last.blocks.empty()) {
-    st = run_blocks(v, last, *dev, stream);
+    st = run_blocks(lv, last, *dev, stream);
     if (st != AXONN_OK) return st;
   }
 
@@ -1247,6 +1271,39 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
       best.us = cand_us[i];
       best.choice = cands[i];
     }
+  // Exchanged operand roles (C^T = B^T . A^T): the two best candidates are
+  // timed again with the roles swapped, each between reference runs like
+  // the others, and a swapped one is kept where it scores better.
+  if (best.us >= 0 && g_forced_swap.load() < 0) {
+    size_t order[2] = {cands.size(), cands.size()};
+    for (size_t i = 0; i < cands.size(); ++i) {
+      if (cand_ratio[i] < 0) continue;
+      if (order[0] == cands.size() || cand_ratio[i] < cand_ratio[order[0]]) {
+        order[1] = order[0];
+        order[0] = i;
+      } else if (order[1] == cands.size() || cand_ratio[i] < cand_ratio[order[1]]) {
+        order[1] = i;
+      }
+    }
+    for (size_t i : order) {
+      if (i == cands.size()) continue;
+      TuneChoice c = cands[i];
+      c.swap = 1;
+      if (fc_op(op, P, Q, C, ldp, ldq, ldc, shape, run_flags, ws, ws_bytes, stream, &c) != AXONN_OK ||
+          t_last_choice.swap != 1)
+        continue;  // the swap does not apply to this call
+      double us = 0, ref_next = 0;
+      if (!time_candidate(c, &us)) continue;
+      if (!time_candidate(ref, &ref_next)) ref_next = ref_us;
+      const double ratio = us / (0.5 * (ref_us + ref_next));
+      ref_us = ref_next;
+      if (ratio < best_ratio) {
+        best_ratio = ratio;
+        best.us = us;
+        best.choice = c;
+      }
+    }
+  }
   // The candidates ran with the default stream-K mode.  Time the best one
   // in all three modes back to back (so they see the same clock) and keep
   // the fastest; the modes are the same launch where no tail applies.
@@ -1290,9 +1347,10 @@ axonn_status_t axonn_tune_cache_save(const char* path) {
     char line[512];
     snprintf(line, sizeof(line),
              "{\"key\": \"%s\", \"config\": \"%s\", \"split\": %d, \"group_m\": %d, "
-             "\"streamk\": %d, \"us\": %.3f}\n",
+             "\"streamk\": %d, \"swap\": %d, \"us\": %.3f}\n",
              kv.first.c_str(), kConfigs[kv.second.choice.config].name, kv.second.choice.split,
-             kv.second.choice.group_m, kv.second.choice.streamk, kv.second.us);
+             kv.second.choice.group_m, kv.second.choice.streamk, kv.second.choice.swap,
+             kv.second.us);
     f << line;
   }
   return f ? ok() : fail(AXONN_ERR_INVALID_ARG, "write to %s failed", path);
@@ -1357,11 +1415,13 @@ axonn_status_t axonn_tune_cache_load(const char* path) {
     e.choice.config = -1;
     for (int c = 0; c < kNumConfigs; ++c)
       if (cfg == kConfigs[c].name) e.choice.config = c;
-    std::string sk;
+    std::string sk, sw;
     const bool has_sk = json_field(line, "streamk", &sk);
+    const bool has_sw = json_field(line, "swap", &sw);
     if (e.choice.config < 0 || !parse_int(split, 1, kMaxSplit, &e.choice.split) ||
         !parse_int(gm, -kMaxGroup, kMaxGroup, &e.choice.group_m) || e.choice.group_m == 0 ||
-        (has_sk && !parse_int(sk, kStreamKOff, kStreamKAlways, &e.choice.streamk)))
+        (has_sk && !parse_int(sk, kStreamKOff, kStreamKAlways, &e.choice.streamk)) ||
+        (has_sw && !parse_int(sw, 0, 1, &e.choice.swap)))
       return fail(AXONN_ERR_INVALID_ARG, "%s:%d: unknown configuration", path, lineno);
     e.us = atof(us.c_str());
     loaded[key] = e;
@@ -1426,6 +1486,58 @@ axonn_status_t axonn_block_range(int64_t D, int32_t G, int32_t b, int64_t* start
   return ok();
 }
 
+axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const int32_t* input_ids,
+                                 const int32_t* labels, int64_t batch, int64_t seq, int64_t vocab,
+                                 int32_t k, int32_t h, uint8_t* keep, float* token_loss,
+                                 float* loss, int32_t* kept, void* dlogits, int64_t ld_dlogits,
+                                 cudaStream_t stream) {
+  if (batch < 0 || seq < 0) return fail(AXONN_ERR_INVALID_ARG, "negative batch or sequence length");
+  if (vocab < 1 || vocab > INT32_MAX) return fail(AXONN_ERR_INVALID_ARG, "vocabulary size %lld", (long long)vocab);
+  if (k < 0) return fail(AXONN_ERR_INVALID_ARG, "k = %d", k);
+  if (h < 1 || h > 4096) return fail(AXONN_ERR_INVALID_ARG, "h = %d not in [1, 4096]", h);
+  if (seq > 0 && batch > (int64_t{1} << 31) / seq)
+    return fail(AXONN_ERR_UNSUPPORTED, "more than 2^31 positions");
+  const int64_t T = batch * seq;
+  if (!loss || !kept) return fail(AXONN_ERR_INVALID_ARG, "loss or kept is NULL");
+  if (T > 0 && (!logits || !input_ids || !labels || !keep || !token_loss))
+    return fail(AXONN_ERR_INVALID_ARG, "NULL input or output");
+  if (ld_logits < vocab) return fail(AXONN_ERR_INVALID_ARG, "logits leading dimension below the vocabulary");
+  if (ld_logits % 8 != 0 || !aligned16(logits))
+    return fail(AXONN_ERR_ALIGNMENT, "logits: 16-byte aligned base and leading dimension a multiple of 8");
+  if (dlogits) {
+    if (ld_dlogits < vocab) return fail(AXONN_ERR_INVALID_ARG, "dlogits leading dimension below the vocabulary");
+    if (ld_dlogits % 8 != 0 || !aligned16(dlogits))
+      return fail(AXONN_ERR_ALIGNMENT, "dlogits: 16-byte aligned base and leading dimension a multiple of 8");
+  }
+  const int cluster = axonn::goldfish_cluster(vocab);
+  if (cluster == 0)
+    return fail(AXONN_ERR_UNSUPPORTED, "vocabulary %lld needs more than 8 x 96 KB of shared memory per row",
+                (long long)vocab);
+  DeviceState* dev = nullptr;
+  axonn_status_t st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+  axonn::GoldfishArgs a;
+  a.logits = static_cast<const uint16_t*>(logits);
+  a.ld_logits = ld_logits;
+  a.input_ids = input_ids;
+  a.labels = labels;
+  a.batch = batch;
+  a.seq = seq;
+  a.vocab = vocab;
+  a.k = k;
+  a.h = h;
+  a.keep = keep;
+  a.token_loss = token_loss;
+  a.loss = loss;
+  a.kept = kept;
+  a.dlogits = static_cast<uint16_t*>(dlogits);
+  a.ld_dlogits = ld_dlogits;
+  a.timeout_ns = g_timeout_ns.load();
+  const cudaError_t e = axonn::goldfish_launch(a, cluster, dev->sms, stream);
+  if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "Goldfish loss launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 axonn_status_t axonn_fc_block_extents(int op, const axonn_fc_shape_t* shape, int64_t* rows,
                                       int64_t* red, int64_t* cols) {
   if (!rows || !red || !cols) return fail(AXONN_ERR_INVALID_ARG, "NULL output");
@@ -1445,11 +1557,13 @@ axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail) {
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "stream: %s", cudaGetErrorString(e));
   // One error word per kernel translation unit; report the first set.
   unsigned long long word = 0, w1 = 0, w8 = 0, w64 = 0;
+  unsigned long long wg = 0;
   e = axonn::kernels_take_status<1>(&w1, stream);
   if (e == cudaSuccess) e = axonn::kernels_take_status<kFewProblems>(&w8, stream);
   if (e == cudaSuccess) e = axonn::kernels_take_status<kMaxProblems>(&w64, stream);
+  if (e == cudaSuccess) e = axonn::goldfish_take_status(&wg, stream);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
-  word = w1 ? w1 : (w8 ? w8 : w64);
+  word = w1 ? w1 : (w8 ? w8 : (w64 ? w64 : wg));
   if (word == 0) return ok();
   if (detail) *detail = word;
   return fail(AXONN_ERR_TIMEOUT, "device wait expired: CTA %llu, site %llu", (word >> 8) & 0xFFFFFFull,
@@ -1474,6 +1588,20 @@ axonn_status_t axonn_set_streamk(int mode) {
   g_forced_streamk.store(mode);
   return ok();
 }
+
+axonn_status_t axonn_set_pdl(int on) {
+  if (on != 0 && on != 1) return fail(AXONN_ERR_INVALID_ARG, "PDL switch %d not 0 or 1", on);
+  g_pdl.store(on);
+  return ok();
+}
+
+axonn_status_t axonn_set_swap(int mode) {
+  if (mode < -1 || mode > 1) return fail(AXONN_ERR_INVALID_ARG, "swap mode %d not in {-1, 0, 1}", mode);
+  g_forced_swap.store(mode);
+  return ok();
+}
+
+int axonn_last_swap(void) { return t_last_choice.swap; }
 
 axonn_status_t axonn_device_info(int* sms, int* max_pairs) {
   DeviceState* d = nullptr;

@@ -94,6 +94,10 @@ struct ProblemDesc {
   // in TMEM.  chain = 1 for a single product.  num_k is the chain's total.
   int32_t chain;
   int32_t map0;
+  // The problem computes the transpose of the caller's product (operand
+  // roles swapped, C^T = B^T . A^T): its tile element (i, j) is the
+  // caller's output element (j, i), stored at C + j * ldc + i.
+  int32_t out_t;
 };
 
 template <int MAXP>
@@ -333,11 +337,38 @@ __device__ __forceinline__ void store_bf16_32(const ProblemDesc& d, int row, int
   }
 }
 
+// Writes 32 accumulator columns of a transposed problem: tile row `row` is
+// output column `row`, tile column col0 + j is output row col0 + j.  The
+// warp's lanes hold consecutive tile rows, so each store instruction writes
+// 32 consecutive elements of one output row.
+__device__ __forceinline__ void store_chunk_t(const ProblemDesc& d, int row, int col0, int ncols,
+                                              const uint32_t (&r)[32]) {
+  if (d.out_mode == kOutBF16) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(d.C) + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) out[static_cast<int64_t>(col0 + j) * d.ldc] = __float2bfloat16_rn(__uint_as_float(r[j]));
+  } else {
+    float* out = reinterpret_cast<float*>(d.C) + row;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      if (j >= ncols) continue;
+      float* o = out + static_cast<int64_t>(col0 + j) * d.ldc;
+      if (d.out_mode == kOutF32Red || d.out_mode == kOutF32Accum) red_add_f32(o, r[j]);
+      else *o = __uint_as_float(r[j]);
+    }
+  }
+}
+
 // Writes 32 accumulator columns [col0, col0+32) of one output row.
 __device__ __forceinline__ void store_chunk(const ProblemDesc& d, int row, int col0,
                                             uint32_t (&r)[32]) {
   const int ncols = min(32, d.N - col0);
   if (d.red_count > 0) add_partials(d, row, col0, ncols, r);
+  if (d.out_t) {
+    store_chunk_t(d, row, col0, ncols, r);
+    return;
+  }
   if (d.out_mode == kOutBF16) {
     uint32_t pk[16];
 #pragma unroll
@@ -485,6 +516,7 @@ __device__ __forceinline__ void epilogue_item(const GemmParams<MAXP>& P, const P
   dp.out_mode = kOutF32;
   dp.red_count = 0;
   dp.fast_bf16 = 0;
+  dp.out_t = 0;  // partial slots are tile-local, in the problem's own orientation
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int col0 = n0 + c * 32;
@@ -620,6 +652,10 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tmo = P.timeout_ns;
+  // Barrier set-up, TMEM allocation and tensor-map prefetch above overlap
+  // the previous kernel's tail; nothing below touches global memory before
+  // that kernel is complete.
+  griddep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -680,6 +716,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
         }
         return true;
       });
+      // Every load of this CTA is issued: the next kernel may begin its
+      // set-up on SMs as they free up.
+      griddep_launch_dependents();
       // Drain: the last load issued on each stage must have landed before
       // the CTA may exit.
       for (int s = 0; s < STAGES; ++s) {

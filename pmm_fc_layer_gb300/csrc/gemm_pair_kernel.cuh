@@ -104,6 +104,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tmo = P.timeout_ns;
+  // Barrier set-up, TMEM allocation and tensor-map prefetch above overlap
+  // the previous kernel's tail; nothing below touches global memory before
+  // that kernel is complete.
+  griddep_wait();
 
   constexpr bool kSplit = MH == 2;  // 12 warps, registers moved to the epilogue
   if (warp < epi_first_warp<MH, kSplit>()) shrink_registers<MH, kSplit>();
@@ -162,6 +166,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
         }
         return true;
       });
+      // Every load of this CTA is issued: the next kernel may begin its
+      // set-up on SMs as they free up.
+      griddep_launch_dependents();
       // Drain (even CTA): the full barriers count both CTAs' bytes, so the
       // last phase of each stage completing means every copy has landed.
       if (leader) {

@@ -1,0 +1,42 @@
+// Host interface of the Goldfish-loss kernels (goldfish.cu): the hashed
+// token mask, the masked cross-entropy with its gradient over bf16 logits,
+// and the fixed-order mean.  The C entry point that validates arguments and
+// calls these is axonn_goldfish_ce in axonn_fc.cu.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace axonn {
+
+struct GoldfishArgs {
+  const uint16_t* logits;  // bf16 [T x V], row stride ld_logits elements
+  int64_t ld_logits;
+  const int32_t* input_ids;  // [batch x seq]
+  const int32_t* labels;     // [batch x seq]
+  int64_t batch, seq, vocab;
+  int32_t k, h;
+  uint8_t* keep;       // [T]
+  float* token_loss;   // [T]
+  float* loss;         // [1]
+  int32_t* kept;       // [1]
+  uint16_t* dlogits;   // bf16 [T x V] or null, row stride ld_dlogits
+  int64_t ld_dlogits;
+  uint64_t timeout_ns;
+};
+
+// Slice of a row one CTA of the cluster holds: elements per CTA (a multiple
+// of 8) for a cluster of `cluster` CTAs over a row of `vocab` elements.
+int64_t goldfish_slice(int64_t vocab, int cluster);
+
+// Smallest cluster size in {1, 2, 4, 8} whose slice fits the per-CTA
+// shared-memory budget; 0 if none does.
+int goldfish_cluster(int64_t vocab);
+
+// The three launches (mask and count, rows, mean) on `stream`; `sms` sizes
+// the persistent grid.
+cudaError_t goldfish_launch(const GoldfishArgs& a, int cluster, int sms, cudaStream_t stream);
+
+// Reads (and clears if set) the device error word of these kernels.
+cudaError_t goldfish_take_status(unsigned long long* word, cudaStream_t stream);
+
+}  // namespace axonn

@@ -9,6 +9,25 @@ namespace axonn {
 constexpr int kPairStages = 6;   // 256 x 256 pair tiles, 32 KB stages
 constexpr int kPair2Stages = 4;  // 512 x 256 pair tiles, 48 KB stages
 
+// Launches `kernel` with cudaLaunchKernelEx; with `pdl` the launch may begin
+// while the previous kernel in the stream finishes (programmatic stream
+// serialization; the kernel waits for it with griddepcontrol.wait).
+template <typename K, int MAXP>
+cudaError_t launch_ex(K kernel, const GemmParams<MAXP>& P, int ctas, int threads, int smem,
+                      bool pdl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, P);
+}
+
 template <int BN, int BK, int STAGES, int MAXP, int MH>
 struct Single {
   static cudaError_t init() {
@@ -16,10 +35,9 @@ struct Single {
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 SmemLayout<BN, BK, STAGES, MH>::kBytes);
   }
-  static cudaError_t launch(const GemmParams<MAXP>& P, int ctas, cudaStream_t s) {
-    fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>
-        <<<ctas, cta_threads<MH>(), SmemLayout<BN, BK, STAGES, MH>::kBytes, s>>>(P);
-    return cudaGetLastError();
+  static cudaError_t launch(const GemmParams<MAXP>& P, int ctas, bool pdl, cudaStream_t s) {
+    return launch_ex(fc_gemm_tcgen05_kernel<BN, BK, STAGES, MAXP, MH>, P, ctas, cta_threads<MH>(),
+                     SmemLayout<BN, BK, STAGES, MH>::kBytes, pdl, s);
   }
 };
 
@@ -41,10 +59,9 @@ struct Pair {
     if (e == cudaSuccess && a.numRegs != kRegsAtLaunch) *ok = false;
     return e;
   }
-  static cudaError_t launch(const GemmParams<MAXP>& P, int pairs, cudaStream_t s) {
-    fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>
-        <<<2 * pairs, cta_threads<MH, MH == 2>(), PairSmemLayout<BN, STAGES, MH>::kBytes, s>>>(P);
-    return cudaGetLastError();
+  static cudaError_t launch(const GemmParams<MAXP>& P, int pairs, bool pdl, cudaStream_t s) {
+    return launch_ex(fc_gemm_tcgen05_pair_kernel<BN, STAGES, MAXP, MH>, P, 2 * pairs,
+                     cta_threads<MH, MH == 2>(), PairSmemLayout<BN, STAGES, MH>::kBytes, pdl, s);
   }
 };
 
@@ -74,15 +91,16 @@ cudaError_t kernels_init(bool* split_ok) {
 }
 
 template <int MAXP>
-cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, cudaStream_t s) {
+cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, bool pdl,
+                           cudaStream_t s) {
   switch (config) {
-    case 0: return C0<MAXP>::launch(P, units, s);
-    case 1: return C1<MAXP>::launch(P, units, s);
-    case 2: return C2<MAXP>::launch(P, units, s);
-    case 3: return C3<MAXP>::launch(P, units, s);
-    case 4: return C4<MAXP>::launch(P, units, s);
-    case 5: return C5<MAXP>::launch(P, units, s);
-    case 6: return C6<MAXP>::launch(P, units, s);
+    case 0: return C0<MAXP>::launch(P, units, pdl, s);
+    case 1: return C1<MAXP>::launch(P, units, pdl, s);
+    case 2: return C2<MAXP>::launch(P, units, pdl, s);
+    case 3: return C3<MAXP>::launch(P, units, pdl, s);
+    case 4: return C4<MAXP>::launch(P, units, pdl, s);
+    case 5: return C5<MAXP>::launch(P, units, pdl, s);
+    case 6: return C6<MAXP>::launch(P, units, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -23,9 +23,11 @@ template <int MAXP>
 cudaError_t kernels_init(bool* split_ok);
 
 // Launches configuration `config` over `units` persistent CTAs, or CTA pairs
-// for the pair configurations.
+// for the pair configurations; with `pdl` as a programmatic dependent launch
+// (its set-up overlaps the previous kernel in the stream).
 template <int MAXP>
-cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, cudaStream_t stream);
+cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, bool pdl,
+                           cudaStream_t stream);
 
 // Reads, and clears if set, the device error word of this MAXP's kernels
 // (each translation unit that instantiates kernels holds its own copy of

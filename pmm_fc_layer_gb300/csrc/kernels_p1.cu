@@ -3,7 +3,7 @@
 
 namespace axonn {
 template cudaError_t kernels_init<1>(bool*);
-template cudaError_t kernels_launch<1>(int, const GemmParams<1>&, int, cudaStream_t);
+template cudaError_t kernels_launch<1>(int, const GemmParams<1>&, int, bool, cudaStream_t);
 template cudaError_t kernels_take_status<1>(unsigned long long*, cudaStream_t);
 
 cudaError_t pair_clusters_resident(int sms, int* clusters) {

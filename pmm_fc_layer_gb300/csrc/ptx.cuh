@@ -134,6 +134,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* m, 
       : "memory");
 }
 
+// ---------------------------------------------------------------- launch order
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// finishing; griddepcontrol.wait blocks until that kernel has completed and
+// its memory writes are visible (it returns at once when there is no such
+// dependency).  launch_dependents lets the next such kernel in the stream
+// begin launching once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

@@ -54,8 +54,10 @@ def to_device(bits):
 
 
 def run_gpu(fc, op, P, Q, p_t, q_t, T, K, N, grid=(1, 1, 1), coords=(0, 0, 0), extra=0,
-            out=None, out_f32=False, local_shape=None):
-    """Call the op through the C ABI; returns the output tensor."""
+            out=None, out_f32=False, local_shape=None, workspace=True):
+    """Call the op through the C ABI; returns the output tensor.  With
+    workspace=False no workspace is passed (no reduction split, no stream-K
+    tail)."""
     import torch
     Pd, Qd = to_device(P), to_device(Q)
     flags = (fc.A_T if p_t else 0) | (fc.B_T if q_t else 0) | extra
@@ -65,7 +67,7 @@ def run_gpu(fc, op, P, Q, p_t, q_t, T, K, N, grid=(1, 1, 1), coords=(0, 0, 0), e
         dt = torch.float32 if (out_f32 or extra & (fc.ACCUM_F32 | fc.OUT_F32)) else torch.bfloat16
         ld = ((oshape[1] + 7) // 8) * 8
         out = torch.zeros((oshape[0], max(ld, 8)), dtype=dt, device="cuda")[:, : oshape[1]]
-    nbytes = fc.axonn_fc_workspace_size(op, shape, flags)
+    nbytes = fc.axonn_fc_workspace_size(op, shape, flags) if workspace else 0
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
     fc.call(op, Pd, Qd, out, shape, flags, ws)
     fc.axonn_sync_status()

@@ -186,11 +186,12 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     fc.axonn_tune_cache_clear()
     entries = [
         {"key": "op0_T8_K8_N8_g1x1x1_at0.0.0_f0_sm152", "config": "pair_256x256", "split": 1,
-         "group_m": 8, "streamk": 0, "us": 12.5},
+         "group_m": 8, "streamk": 0, "swap": 1, "us": 12.5},
         {"key": "op1_T64_K512_N16_g1x1x1_at0.0.0_f0_sm152", "config": "1cta_128x128",
-         "split": 4, "group_m": 16, "streamk": 2, "us": 3.25},
+         "split": 4, "group_m": 16, "streamk": 2, "swap": 0, "us": 3.25},
     ]
-    # a line written before the stream-K field existed loads with it on
+    # a line written before the stream-K and swap fields existed loads with
+    # the tail on and the roles as given
     legacy = {"key": "op2_T8_K8_N8_g1x1x1_at0.0.0_f0_sm152", "config": "pair_512x256", "split": 1,
               "group_m": -16, "us": 7.0}
     src = tmp_path / "tune.jsonl"
@@ -200,7 +201,7 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     out = tmp_path / "saved.jsonl"
     fc.axonn_tune_cache_save(str(out))
     saved = sorted((json.loads(l) for l in out.read_text().splitlines()), key=lambda e: e["key"])
-    assert saved == sorted(entries + [dict(legacy, streamk=1)], key=lambda e: e["key"])
+    assert saved == sorted(entries + [dict(legacy, streamk=1, swap=0)], key=lambda e: e["key"])
     # malformed or unknown entries are rejected and leave the table as it was
     bad = tmp_path / "bad.jsonl"
     bad.write_text('{"key": "x", "config": "no_such_config", "split": 1, "group_m": 8, "us": 1}\n')
@@ -217,9 +218,9 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     # (a larger one would overflow the kernel's tile walk), splits 1..8
     for field in ('"group_m": 100000', '"group_m": -65', '"group_m": 0', '"group_m": "8x"',
                   '"group_m": 8.5', '"split": 0', '"split": 9', '"split": 99999999999999999999',
-                  '"streamk": -1', '"streamk": "1 "'):
+                  '"streamk": -1', '"streamk": "1 "', '"swap": 2', '"swap": -1'):
         entry = {"key": "x", "config": "pair_512x256", "split": 1, "group_m": 8, "streamk": 1,
-                 "us": 1}
+                 "swap": 0, "us": 1}
         name = field.split(":")[0].strip('"')
         line = json.dumps(entry).replace(f'"{name}": {json.dumps(entry[name])}', field)
         assert field in line
@@ -239,6 +240,14 @@ def test_tune_cache_roundtrip(fc, tmp_path):
     assert fc.axonn_tune_cache_size() == 3
     fc.axonn_tune_cache_clear()
     assert fc.axonn_tune_cache_size() == 0
+
+
+def test_set_swap(fc):
+    for mode in (-1, 0, 1, -1):
+        fc.axonn_set_swap(mode)
+    for bad in (-2, 2):
+        with pytest.raises(fc.AxonnError):
+            fc.axonn_set_swap(bad)
 
 
 def test_set_streamk(fc):

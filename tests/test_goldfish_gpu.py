@@ -1,0 +1,206 @@
+"""GPU parity of the Goldfish-loss kernels through the C ABI against the
+fp64 oracle (oracle/goldfish.py).
+
+* The mask and the count are integers: bit for bit.
+* Per-token cross-entropy: the kernel sums each row's exponentials in fp32,
+  at most about 80 terms in series per thread (a 32 KB slice over 256
+  threads) and then a fixed tree of at most 11 levels, so the relative
+  error of the sum is below (80 + 11) * 2^-24 < 6e-6; the exponent's own
+  rounding and exp2/log2 add a few ulps.  That bounds |CE - CE_ref| by
+  1e-5 * (1 + |logsumexp|).
+* The mean adds at most one more fp32 summation of T terms (8 in series per
+  thread, then a 10-level tree): 1e-5 * (1 + |loss|) plus the per-token
+  bound.
+* The gradient: softmax p = exp2(z log2e - lse log2e) in fp32.  Its
+  relative error is the error of logsumexp (below 1e-5 + |lse| 2^-22, as
+  above) plus the rounding of the two products in the exponent ((|z| +
+  |lse|) 2^-23) and of exp2 and the multiply by 1/n (2^-21).  The label's
+  entry subtracts 1/n (one more rounding, 2^-23 / n), and the result is
+  rounded once to bf16 (8 significant bits: at most 2^-8 relative).  So
+  |g - g_ref| <= 2^-8 |g_ref| + (1 + 2^-8) (p_ref eps_p + 2^-23) / n with
+  eps_p = 1e-5 + |lse| 2^-22 + (|z| + |lse|) 2^-23 + 2^-21.
+"""
+import numpy as np
+import pytest
+
+import fc_inputs
+from oracle import goldfish as gf
+
+pytestmark = pytest.mark.gpu
+
+
+def _problem(B, S, V, seed, pad_every=0, sigma=2.0):
+    rng = np.random.default_rng(seed)
+    seqs = rng.integers(0, V, size=(B, S + 1))
+    ids, labels = seqs[:, :-1].astype(np.int32), seqs[:, 1:].astype(np.int32)
+    if pad_every:
+        labels[:, ::pad_every] = -100
+    logits = fc_inputs.normal_bf16((B * S, V), seed, 7, sigma=sigma)
+    return ids, labels, logits
+
+
+def _run(fc, ids, labels, logits, k, h, grad=True, ld_pad=0):
+    """Runs the entry point; logits and dlogits rows padded to a multiple of
+    8 (+ ld_pad) with sentinels in the padding.  Returns host arrays."""
+    import torch
+    T, V = logits.shape
+    ld = (V + 7) // 8 * 8 + ld_pad
+    L = torch.full((max(T, 1), ld), 1e30, dtype=torch.bfloat16, device="cuda")
+    if T:
+        L[:T, :V] = fc_inputs.as_torch_bf16(logits, "cuda")
+    ids_d = torch.from_numpy(np.ascontiguousarray(ids, np.int32)).cuda()
+    lab_d = torch.from_numpy(np.ascontiguousarray(labels, np.int32)).cuda()
+    keep = torch.full((max(T, 1),), 7, dtype=torch.uint8, device="cuda")
+    tl = torch.full((max(T, 1),), float("nan"), dtype=torch.float32, device="cuda")
+    loss = torch.full((1,), float("nan"), dtype=torch.float32, device="cuda")
+    kept = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    dl = torch.full((max(T, 1), ld), -3.0, dtype=torch.bfloat16, device="cuda") if grad else None
+    fc.axonn_goldfish_ce(L[:T, :V] if T else L[:0, :V], ids_d, lab_d, keep, tl, loss, kept, k=k,
+                         h=h, dlogits=(dl[:T, :V] if T else dl[:0, :V]) if grad else None)
+    fc.axonn_sync_status()
+    out = {"keep": keep[:T].cpu().numpy(), "token_loss": tl[:T].double().cpu().numpy(),
+           "loss": float(loss.item()), "n": int(kept.item())}
+    if grad:
+        out["dlogits"] = dl[:T, :V].double().cpu().numpy()
+        out["dl_pad"] = dl[:T, V:].double().cpu().numpy()
+    return out
+
+
+def grad_tolerance(ref, logit_bits, n):
+    """The gradient bound of the module docstring, per entry."""
+    z = np.abs(fc_inputs.bf16_bits_to_f32(logit_bits).astype(np.float64))
+    lse = np.abs(ref["lse"])[:, None]
+    eps_p = 1e-5 + lse * 2.0 ** -22 + (z + lse) * 2.0 ** -23 + 2.0 ** -21
+    return (2.0 ** -8 * np.abs(ref["dlogits"])
+            + (1 + 2.0 ** -8) * (ref["softmax"] * eps_p + 2.0 ** -23) / max(n, 1))
+
+
+def _check(got, ref, V, logits):
+    assert np.array_equal(got["keep"], ref["keep"])
+    assert got["n"] == ref["n"]
+    tol = 1e-5 * (1 + np.abs(ref["lse"]))
+    err = np.abs(got["token_loss"] - ref["token_loss"])
+    assert np.all(err <= tol), f"token loss: worst {float((err / tol).max()):.3g} of the bound"
+    assert abs(got["loss"] - ref["loss"]) <= 1e-5 * (1 + abs(ref["loss"])) + float(tol.max())
+    if "dlogits" in got:
+        g, gr = got["dlogits"], ref["dlogits"]
+        tol_g = grad_tolerance(ref, logits, ref["n"])
+        bad = np.abs(g - gr) > tol_g
+        assert not bad.any(), f"{int(bad.sum())} gradient entries out of bound"
+        assert np.all(got["dl_pad"] == -3.0), "padding columns of dlogits were written"
+
+
+@pytest.mark.parametrize("V", [1000, 1003, 20000, 50257])
+@pytest.mark.parametrize("k,h", [(2, 13), (0, 13), (1, 13), (3, 1), (4, 5)])
+def test_goldfish_vs_oracle(cuda_lib, V, k, h):
+    ids, labels, logits = _problem(2, 40, V, 100 + V % 97 + k + h, pad_every=9)
+    got = _run(cuda_lib, ids, labels, logits, k, h)
+    ref = gf.goldfish_ce(logits, ids, labels, k, h)
+    _check(got, ref, V, logits)
+
+
+@pytest.mark.parametrize("V", [128256, 300001])
+def test_goldfish_large_vocabularies(cuda_lib, V):
+    """Clusters of 8 CTAs per row (32 KB slices in a ring of four, and 75 KB
+    slices in a ring of two)."""
+    ids, labels, logits = _problem(1, 48, V, 200 + V % 13)
+    got = _run(cuda_lib, ids, labels, logits, 2, 13, ld_pad=8)
+    _check(got, gf.goldfish_ce(logits, ids, labels, 2, 13), V, logits)
+
+
+def test_goldfish_loss_only_and_padding_labels(cuda_lib):
+    V = 5000
+    ids, labels, logits = _problem(3, 30, V, 301)
+    labels[0, 20] = V            # outside the vocabulary: padding
+    labels[2, 5] = -1
+    got = _run(cuda_lib, ids, labels, logits, 2, 13, grad=False)
+    _check(got, gf.goldfish_ce(logits, ids, labels, 2, 13), V, logits)
+
+
+def test_goldfish_nothing_kept_and_empty(cuda_lib):
+    V = 777
+    ids, labels, logits = _problem(2, 16, V, 302)
+    got = _run(cuda_lib, ids, np.full_like(labels, -100), logits, 2, 13)
+    assert got["n"] == 0 and got["loss"] == 0.0
+    assert not got["keep"].any() and not got["token_loss"].any() and not got["dlogits"].any()
+    got = _run(cuda_lib, ids[:0], labels[:0], logits[:0], 2, 13)
+    assert got["n"] == 0 and got["loss"] == 0.0
+
+
+def test_goldfish_extreme_logits(cuda_lib):
+    """A dominant logit (softmax near one-hot) and very negative rows."""
+    V = 4096
+    ids, labels, _ = _problem(1, 24, V, 303)
+    z = np.zeros((24, V), np.float32)
+    z[np.arange(24), labels[0]] = 60.0       # the label dominates
+    z[5] = -80.0
+    z[7, :] = np.linspace(-50, 50, V)
+    logits = fc_inputs.f32_to_bf16_bits(z)
+    got = _run(cuda_lib, ids, labels, logits, 0, 13)
+    _check(got, gf.goldfish_ce(logits, ids, labels, 0, 13), V, logits)
+
+
+def test_goldfish_validation(cuda_lib):
+    import torch
+    fc = cuda_lib
+    V = 100
+    L = torch.zeros((4, 104), dtype=torch.bfloat16, device="cuda")
+    ids = torch.zeros((2, 2), dtype=torch.int32, device="cuda")
+    keep = torch.zeros(4, dtype=torch.uint8, device="cuda")
+    tl = torch.zeros(4, dtype=torch.float32, device="cuda")
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    kept = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with pytest.raises(fc.AxonnError) as e:
+        fc.axonn_goldfish_ce(L[:, 1:V + 1], ids, ids, keep, tl, loss, kept)    # misaligned
+    assert e.value.status == fc.ERR_ALIGNMENT
+    with pytest.raises(fc.AxonnError) as e:
+        fc.axonn_goldfish_ce(L[:, :V], ids, ids, keep, tl, loss, kept, h=0)
+    assert e.value.status == fc.ERR_INVALID_ARG
+    big = torch.zeros((1, 8 * 49152 + 8), dtype=torch.bfloat16, device="cuda")
+    one = torch.zeros((1, 1), dtype=torch.int32, device="cuda")
+    with pytest.raises(fc.AxonnError) as e:
+        fc.axonn_goldfish_ce(big, one, one, keep, tl, loss, kept)
+    assert e.value.status == fc.ERR_UNSUPPORTED
+
+
+def test_goldfish_full_size_t8192_v128256(cuda_lib):
+    """The benchmark's workload: 4 sequences of 2048 tokens, a 128256-token
+    vocabulary, k = 2, h = 13.  Mask and count bit for bit over all 8192
+    positions, the loss against the oracle's mean over every kept row, and
+    token losses and gradient rows on a sample of 48 positions."""
+    import torch
+    fc = cuda_lib
+    B, S, V, seed = 4, 2048, 128256, 1007
+    rng = np.random.default_rng(seed)
+    seqs = rng.integers(0, V, size=(B, S + 1))
+    ids, labels = seqs[:, :-1].astype(np.int32), seqs[:, 1:].astype(np.int32)
+    T = B * S
+
+    def rows(r0, r1):
+        return fc_inputs.normal_bf16((r1 - r0, V), seed, 8, sigma=2.0, start=r0 * V)
+
+    L = torch.empty((T, V), dtype=torch.bfloat16, device="cuda")
+    for r0 in range(0, T, 512):
+        L[r0:r0 + 512] = fc_inputs.as_torch_bf16(rows(r0, min(T, r0 + 512)), "cuda")
+    dl = torch.empty((T, V), dtype=torch.bfloat16, device="cuda")
+    keep = torch.empty(T, dtype=torch.uint8, device="cuda")
+    tl = torch.empty(T, dtype=torch.float32, device="cuda")
+    loss = torch.empty(1, dtype=torch.float32, device="cuda")
+    kept = torch.empty(1, dtype=torch.int32, device="cuda")
+    fc.axonn_goldfish_ce(L, torch.from_numpy(ids).cuda(), torch.from_numpy(labels).cuda(), keep,
+                         tl, loss, kept, k=2, h=13, dlogits=dl)
+    fc.axonn_sync_status()
+    ref_loss, n, ref_tl, ref_keep = gf.goldfish_loss_streamed(rows, ids, labels, 2, 13, vocab=V)
+    assert np.array_equal(keep.cpu().numpy(), ref_keep) and int(kept.item()) == n
+    assert 0.45 * T < n < 0.55 * T + 13 * B
+    got_tl = tl.double().cpu().numpy()
+    # |logsumexp| <= CE + |z_y| and the N(0, 4) logits stay below 20 in size
+    tol = 1e-5 * (21 + np.abs(ref_tl))
+    assert np.all(np.abs(got_tl - ref_tl) <= tol)
+    assert abs(float(loss.item()) - ref_loss) <= 1e-5 * (1 + ref_loss) + float(tol.max())
+    sample = np.concatenate([np.arange(16), np.arange(T - 16, T),
+                             rng.choice(T, 16, replace=False)])
+    sample_bits = np.stack([rows(r, r + 1)[0] for r in sample])
+    ref = gf.goldfish_ce(sample_bits, ids, labels, 2, 13, rows=sample)
+    g = dl[torch.from_numpy(sample).cuda()].double().cpu().numpy()
+    assert np.all(np.abs(g - ref["dlogits"]) <= grad_tolerance(ref, sample_bits, n))
