@@ -92,7 +92,22 @@ DEFAULT_WORKLOAD = "gpt_h6144_t8192"
 # each tuned choice ("config/group/stream-K tiles") captured (summary and command
 # in profiles/).  Reported only while the kernel sources hash to the value
 # the capture was taken with and every GEMM's choice of this run is in it.
-TRAFFIC = {"workload": "gpt_h6144_t8192", "kernel_sources": None, "bytes": {}}
+TRAFFIC = {
+    "workload": "gpt_h6144_t8192", "kernel_sources": "37a309afda25bc9c",
+    "bytes": {
+        ("qkv:fwd", "pair_512x256/-8/88"): 2117097728,
+        ("qkv:dgrad", "1cta_256x192/8/0"): 1750933248,
+        ("qkv:wgrad", "pair_512x256/-16/0"): 1750543616,
+        ("out:fwd", "1cta_256x192/-8/0"): 634757376,
+        ("out:dgrad", "1cta_256x192/-16/0"): 525072128,
+        ("out:wgrad", "pair_512x256/16/0"): 570256640,
+        ("up:fwd", "1cta_256x192/-16/0"): 2224966144,
+        ("up:dgrad", "1cta_256x192/8/0"): 2316426752,
+        ("up:wgrad", "pair_512x256/-16/88"): 2739174656,
+        ("down:fwd", "pair_512x256/8/80"): 3884671488,
+        ("down:dgrad", "1cta_256x192/-8/0"): 2577054976,
+        ("down:wgrad", "pair_512x256/16/88"): 3527472896,
+    }}
 
 
 def traffic_per_launch(workload, per, only):

@@ -18,15 +18,17 @@
 //     the count n (a block reduction, so no atomics and no zeroing).
 //  2. goldfish_rows_kernel: a cluster of C CTAs per row of logits,
 //     persistent over rows.  CTA c of the cluster holds elements
-//     [c*L, (c+1)*L) of the row in shared memory, brought in by one 1-D bulk
-//     copy (cp.async.bulk) and double-buffered so the next kept row loads
-//     while this one is computed.  Each CTA reduces its slice to (max, sum
-//     of exp), the owner of the label also its logit, and publishes them in
-//     its shared memory; after one cluster barrier every CTA reads the C
-//     triples through distributed shared memory and has logsumexp.  The
-//     gradient slice is then computed from shared memory and streamed out.
+//     [c*L, (c+1)*L) of a row in shared memory, brought in by one 1-D bulk
+//     copy (cp.async.bulk) into a ring of up to four buffers filled by a
+//     producer warp, so copies of the next kept rows are in flight while one
+//     is computed.  Sixteen consumer warps reduce the slice to (max, sum of
+//     exp) in one pass, the owner of the label adds its logit, and the entry
+//     is pushed into every CTA of the cluster through distributed shared
+//     memory (st.async onto an mbarrier); with all C entries a CTA has
+//     logsumexp and writes its gradient slice from shared memory.  The
+//     exchange of one row overlaps the gradient pass of the previous one.
 //     The logits of a row are read from HBM once; rows of dropped labels are
-//     not read at all (their gradient is zero).
+//     not read at all (their gradient rows are written as zeros first).
 //  3. goldfish_mean_kernel: one CTA sums token_loss[] in a fixed order and
 //     divides by n.
 // Every wait on a copy is bounded by a wall-clock limit; on expiry the CTA
@@ -37,6 +39,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <mutex>
 
 #include "goldfish.h"
 #include "ptx.cuh"
@@ -45,18 +48,16 @@ namespace axonn {
 
 namespace {
 
-constexpr int kGfConsumerWarps = 8;
+constexpr int kGfConsumerWarps = 16;
 constexpr int kGfConsumers = 32 * kGfConsumerWarps;
 constexpr int kGfThreads = kGfConsumers + 32;  // + the producer warp
 constexpr int kGfStages = 4;                   // slice buffers per CTA, at most
 constexpr int kMaskThreads = 1024;
-// Shared memory for one slice buffer: rows are split over as many CTAs as it
-// takes (up to a cluster of 8) to keep a slice within kTargetSliceBytes, so
-// that a ring of four buffers keeps 128 KB of copies in flight per SM; a
-// row needs at most kMaxSliceBytes per CTA (then with two buffers).
-constexpr int64_t kTargetSliceBytes = 32 * 1024;
+// Shared memory: a row is split over a cluster of C CTAs (C in {1, 2, 4,
+// 8}); each CTA's slice is at most kMaxSliceBytes, and its ring holds as
+// many slices (up to kGfStages) as fit in kRingBytes.
 constexpr int64_t kMaxSliceBytes = 96 * 1024;
-constexpr int64_t kRingBytes = 200 * 1024;  // buffers of the ring fit in this
+constexpr int64_t kRingBytes = 200 * 1024;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -91,6 +92,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           dst),
       "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// 2^x by the SFU's approximation (PTX ex2.approx.ftz.f32: relative error
+// about 2^-22; results below 2^-126 flush to zero, far below any bound the
+// loss or its bf16 gradient is held to).  The softmax's exponents are never
+// positive, so no overflow path is needed.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
@@ -156,19 +167,22 @@ struct RowParams {
   int64_t slice;  // elements per CTA (multiple of 8)
 };
 
+constexpr int kInbox = 3;  // inbox slots: rows kc, kc+1 and kc+2 may be in flight
+
 // Shared memory after the slice buffers.
 struct alignas(16) GfTail {
-  float4 inbox[2][8];  // [row parity][sending CTA]: max, sum of exp, label logit, has label
+  float4 inbox[kInbox][8];  // [row % kInbox][sending CTA]: max, sum of exp, label logit, has it
   uint64_t full[kGfStages];
   uint64_t empty[kGfStages];
-  uint64_t inbox_bar[2];
+  uint64_t inbox_bar[kInbox];
   int64_t meta_row[kGfStages];
   int32_t meta_y[kGfStages];
-  int32_t meta_keep[kGfStages];
   float red_m[kGfConsumerWarps];
   float red_s[kGfConsumerWarps];
+  int red_n[kGfConsumerWarps];
   float lse;
   int aborted;
+  uint8_t flags[kGfConsumers];  // mask flags of a chunk of the cluster's rows
 };
 
 // Barrier among the consumer warps only (the producer warp runs ahead).
@@ -186,10 +200,18 @@ __device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float4 v, uin
       : "memory");
 }
 
-// Element j (0..7) of eight packed bf16 values.
-__device__ __forceinline__ float lane_bf16(const uint4& v, int j) {
-  const uint32_t w = j < 2 ? v.x : (j < 4 ? v.y : (j < 6 ? v.z : v.w));
-  return bf16_to_f32(static_cast<uint16_t>(w >> (16 * (j & 1))));
+// The eight bf16 values of a 16-byte vector as floats (exact): a bf16 is
+// the high half of a float, so the high half of each 32-bit word is masked
+// out in place and the low half shifted up.
+__device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
+  x[0] = __uint_as_float(v.x << 16);
+  x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(v.y << 16);
+  x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  x[4] = __uint_as_float(v.z << 16);
+  x[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  x[6] = __uint_as_float(v.w << 16);
+  x[7] = __uint_as_float(v.w & 0xFFFF0000u);
 }
 
 // Writes zeros to elements [c0, c1) of a gradient row (16-byte stores for
@@ -202,23 +224,65 @@ __device__ __forceinline__ void zero_row(uint16_t* row, int64_t c0, int64_t c1, 
   for (int64_t i = v1 + ct; i < c1; i += kGfConsumers) row[i] = 0;
 }
 
-// Warp 0 is the producer: lane 0 walks the cluster's rows, records each
-// row's label and mask in a ring of kGfStages entries and, for a kept row,
-// bulk-copies this CTA's slice of its logits into the entry's buffer (a
-// dropped row gets a plain arrival: nothing to read).  Warps 1..8 consume
-// the ring in order.  For a kept row each CTA reduces its slice to (max,
-// sum of exp) and pushes it, with the label's logit if it owns it, into
-// every peer's inbox with st.async, completing on the peer's inbox barrier;
-// when its own inbox has all C entries it forms logsumexp and writes its
-// gradient slice.  A CTA pushes row i+2's entry (same inbox parity as row
-// i) only after it received every peer's entry for row i+1, which each
-// peer sends after it read row i's inbox: so two inbox slots suffice and no
-// cluster barrier is needed per row.
+// Number of consumer threads whose `pred` is true (a barrier among the
+// consumers; every consumer thread gets the count).
+__device__ __forceinline__ int consumers_count(bool pred, GfTail* tl);
+
+// Adds values to one thread's running (max, sum of exp(x - max)).
+__device__ __forceinline__ void online_add8(float& m, float& s, const float (&x)[8]) {
+  const float vm = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])),
+                         fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+  if (vm > m) {
+    s *= fast_exp2((m - vm) * kLog2e);  // 2^-inf = 0 on the first values
+    m = vm;
+  }
+  const float mb = m * kLog2e;
+  float t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    t0 += fast_exp2(fmaf(x[j], kLog2e, -mb));
+    t1 += fast_exp2(fmaf(x[j + 1], kLog2e, -mb));
+  }
+  s += t0 + t1;
+}
+
+__device__ __forceinline__ void online_add1(float& m, float& s, float x) {
+  if (x > m) {
+    s *= fast_exp2((m - x) * kLog2e);
+    m = x;
+  }
+  s += fast_exp2((x - m) * kLog2e);
+}
+
+__device__ __forceinline__ int consumers_count(bool pred, GfTail* tl) {
+  const int w = (threadIdx.x >> 5) - 1;
+  const int c = __popc(__ballot_sync(0xFFFFFFFFu, pred));
+  if ((threadIdx.x & 31) == 0) tl->red_n[w] = c;
+  consumer_sync();
+  int n = 0;
+#pragma unroll
+  for (int i = 0; i < kGfConsumerWarps; ++i) n += tl->red_n[i];
+  return n;
+}
+
+// Warp 0 is the producer: lane 0 bulk-copies this CTA's slice of every kept
+// row of the cluster, in order, into a ring of `stages` buffers.  Warps
+// 1..16 are the consumers.  They first write the zero gradient rows (and
+// zero losses) of the cluster's dropped labels, which need no logits.  Then,
+// for kept row kc, each CTA reduces its slice to (max, sum of exp), adds the
+// label's logit if it owns it, and pushes that entry with st.async into the
+// same inbox slot (kc mod 3) of every CTA of the cluster, completing on that
+// CTA's inbox barrier.  Row kc+1 is reduced and pushed before row kc's inbox
+// is read and its gradient written, so the exchange overlaps a gradient
+// pass.  A CTA pushes row kc+3 into slot kc mod 3 only after it has every
+// peer's entry for row kc+2, which each peer pushes after reading its row
+// kc entries: three slots suffice and no cluster barrier is needed per row.
 __global__ void __launch_bounds__(kGfThreads, 1)
     goldfish_rows_kernel(const __grid_constant__ RowParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GoldfishArgs& a = p.a;
   const int C = p.cluster;
+  const int NB = p.stages;
   const uint32_t rank = C > 1 ? cluster_ctarank() : 0u;
   const int64_t cl = blockIdx.x / C;
   const int64_t ncl = gridDim.x / C;
@@ -229,18 +293,17 @@ __global__ void __launch_bounds__(kGfThreads, 1)
   const int64_t n_load = s0 < vpad ? min(p.slice, vpad - s0) : 0;  // elements copied
   const int64_t n_valid = s0 < V ? min(p.slice, V - s0) : 0;       // elements of the row
   const int64_t buf_bytes = p.slice * 2;
-  GfTail* tl = reinterpret_cast<GfTail*>(smem + p.stages * buf_bytes);
+  GfTail* tl = reinterpret_cast<GfTail*>(smem + NB * buf_bytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns;
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < p.stages; ++b) {
+    for (int b = 0; b < NB; ++b) {
       mbar_init(smem_addr(&tl->full[b]), 1);
       mbar_init(smem_addr(&tl->empty[b]), kGfConsumerWarps);
     }
-    mbar_init(smem_addr(&tl->inbox_bar[0]), 1);
-    mbar_init(smem_addr(&tl->inbox_bar[1]), 1);
+    for (int q = 0; q < kInbox; ++q) mbar_init(smem_addr(&tl->inbox_bar[q]), 1);
     tl->aborted = 0;
     fence_mbarrier_init();
   }
@@ -249,29 +312,27 @@ __global__ void __launch_bounds__(kGfThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    const int NB = p.stages;
     int b = 0;
     uint32_t ph = 0;
-    int issued[kGfStages] = {};  // phases of each stage that carried a copy
+    int issued[kGfStages] = {};  // 1 + the last use of each stage that carried a copy
     int uses[kGfStages] = {};
     for (int64_t base = cl; base < T; base += 32 * ncl) {
       // 32 rows' labels and mask flags at once, one per lane
       const int64_t rr = base + lane * ncl;
       const int32_t keep_l = rr < T ? a.keep[rr] : 0;
       const int32_t y_l = rr < T ? a.labels[rr] : 0;
-      const int64_t left = (T - base + ncl - 1) / ncl;
-      const int cnt = left < 32 ? static_cast<int>(left) : 32;
-      for (int j = 0; j < cnt; ++j) {
-        const int32_t keep = __shfl_sync(0xFFFFFFFFu, keep_l, j);
+      uint32_t kept_bits = __ballot_sync(0xFFFFFFFFu, keep_l != 0);
+      while (kept_bits) {
+        const int j = __ffs(kept_bits) - 1;
+        kept_bits &= kept_bits - 1;
         const int32_t y = __shfl_sync(0xFFFFFFFFu, y_l, j);
         if (lane == 0) {
           const int64_t r = base + j * ncl;
           if (!gf_wait(smem_addr(&tl->empty[b]), ph ^ 1u, tmo, 3)) tl->aborted = 1;
           tl->meta_row[b] = r;
           tl->meta_y[b] = y;
-          tl->meta_keep[b] = keep;
           const uint32_t fb = smem_addr(&tl->full[b]);
-          if (keep && n_load > 0 && !tl->aborted) {
+          if (n_load > 0 && !tl->aborted) {
             mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n_load * 2));
             bulk_load(smem_addr(smem + b * buf_bytes), a.logits + r * a.ld_logits + s0,
                       static_cast<uint32_t>(n_load * 2), fb);
@@ -291,127 +352,166 @@ __global__ void __launch_bounds__(kGfThreads, 1)
     // Copies not consumed exist only after an expired wait: let them land
     // (bounded) before this CTA's shared memory goes away.
     if (lane == 0 && tl->aborted) {
-      for (int s = 0; s < NB; ++s)
-        if (issued[s] > 0) gf_wait(smem_addr(&tl->full[s]), (issued[s] - 1) & 1u, tmo, 2);
+      for (int q = 0; q < NB; ++q)
+        if (issued[q] > 0) gf_wait(smem_addr(&tl->full[q]), (issued[q] - 1) & 1u, tmo, 2);
     }
   } else {
     // ------------------------------------------------------------ consumers
-    const int cw = warp - 1;            // consumer warp 0..7
-    const int ct = threadIdx.x - 32;    // consumer thread 0..255
-    const int NB = p.stages;
+    const int cw = warp - 1;          // consumer warp
+    const int ct = threadIdx.x - 32;  // consumer thread
     const int32_t n = *a.kept;
     const float inv_n = n > 0 ? 1.0f / static_cast<float>(n) : 0.0f;
-    int b = 0;
-    uint32_t ph = 0;
-    int kc = 0;  // kept rows so far
-    for (int64_t r = cl; r < T; r += ncl) {
-      if (!gf_wait(smem_addr(&tl->full[b]), ph, tmo, 1)) tl->aborted = 1;
-      const int32_t y = tl->meta_y[b];
-      const int keep = tl->meta_keep[b];
-      const uint16_t* x = reinterpret_cast<const uint16_t*>(smem + b * buf_bytes);
-      if (!keep) {
+    const float log2n = n > 0 ? log2f(static_cast<float>(n)) : 0.0f;
+
+    // 1. rows of dropped labels: zero gradient slices and losses; count the
+    //    kept rows of this cluster.  The mask flags of kGfConsumers rows at a
+    //    time are read in parallel (one per thread) into shared memory.
+    int nk = 0;
+    for (int64_t base = cl; base < T; base += static_cast<int64_t>(kGfConsumers) * ncl) {
+      const int64_t rr = base + static_cast<int64_t>(ct) * ncl;
+      const int kf = rr < T ? a.keep[rr] : 1;
+      tl->flags[ct] = static_cast<uint8_t>(kf != 0);
+      nk += consumers_count(rr < T && kf != 0, tl);
+      for (int j = 0; j < kGfConsumers; ++j) {
+        const int64_t r = base + static_cast<int64_t>(j) * ncl;
+        if (r >= T) break;
+        if (tl->flags[j]) continue;
         if (a.dlogits && n_valid > 0) zero_row(a.dlogits + r * a.ld_dlogits, s0, s0 + n_valid, ct);
         if (rank == 0 && ct == 0) a.token_loss[r] = 0.0f;
-      } else {
-        const bool have = n_load > 0 && !tl->aborted;
-        // this slice's max, then its sum of exp(x - max)
-        float m = -INFINITY;
-        if (have) {
-          for (int64_t i = 8 * ct; i < n_valid; i += 8 * kGfConsumers) {
-            const uint4 v = *reinterpret_cast<const uint4*>(x + i);
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (i + j < n_valid) m = fmaxf(m, lane_bf16(v, j));
+      }
+      consumer_sync();  // flags are rewritten for the next chunk
+    }
+
+    // 2. kept rows, software-pipelined by one row
+    auto stage_of = [&](int kc) { return kc % NB; };
+    auto wait_full = [&](int kc) {
+      if (!gf_wait(smem_addr(&tl->full[stage_of(kc)]), static_cast<uint32_t>((kc / NB) & 1), tmo, 1))
+        tl->aborted = 1;
+    };
+    // reduce kept row kc to this slice's entry and push it to every CTA
+    auto reduce_push = [&](int kc) {
+      wait_full(kc);
+      const int b = stage_of(kc);
+      const uint16_t* x = reinterpret_cast<const uint16_t*>(smem + b * buf_bytes);
+      const int32_t y = tl->meta_y[b];
+      const bool have = n_load > 0 && !tl->aborted;
+      float m0 = -INFINITY, s0_ = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+      if (have) {
+        // whole 8-element vectors, two per iteration, then the ragged tail
+        const int64_t vfull = n_valid & ~int64_t{7};
+        for (int64_t i = 16 * ct; i < vfull; i += 16 * kGfConsumers) {
+          float xa[8];
+          unpack8(*reinterpret_cast<const uint4*>(x + i), xa);
+          online_add8(m0, s0_, xa);
+          if (i + 8 < vfull) {
+            float xb[8];
+            unpack8(*reinterpret_cast<const uint4*>(x + i + 8), xb);
+            online_add8(m1, s1, xb);
           }
         }
+        for (int64_t i = vfull + ct; i < n_valid; i += kGfConsumers)
+          online_add1(m1, s1, bf16_to_f32(x[i]));
+      }
+      // thread's (max, sum), then the slice's
+      float m = fmaxf(m0, m1);
+      float sm = (m0 > -INFINITY ? s0_ * fast_exp2((m0 - m) * kLog2e) : 0.0f) +
+                 (m1 > -INFINITY ? s1 * fast_exp2((m1 - m) * kLog2e) : 0.0f);
+      float wm = m;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-        if (lane == 0) tl->red_m[cw] = m;
-        consumer_sync();
-        m = tl->red_m[0];
+      for (int o = 16; o > 0; o >>= 1) wm = fmaxf(wm, __shfl_xor_sync(0xFFFFFFFFu, wm, o));
+      if (lane == 0) tl->red_m[cw] = wm;
+      consumer_sync();
+      float M = tl->red_m[0];
 #pragma unroll
-        for (int w = 1; w < kGfConsumerWarps; ++w) m = fmaxf(m, tl->red_m[w]);
-        float sum = 0.0f;
-        if (have && m > -INFINITY) {
-          const float mb = m * kLog2e;
-          for (int64_t i = 8 * ct; i < n_valid; i += 8 * kGfConsumers) {
-            const uint4 v = *reinterpret_cast<const uint4*>(x + i);
+      for (int w = 1; w < kGfConsumerWarps; ++w) M = fmaxf(M, tl->red_m[w]);
+      float ws = m > -INFINITY ? sm * fast_exp2((m - M) * kLog2e) : 0.0f;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (i + j < n_valid) sum += exp2f(fmaf(lane_bf16(v, j), kLog2e, -mb));
-          }
+      for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
+      if (lane == 0) tl->red_s[cw] = ws;
+      consumer_sync();
+      if (ct == 0) {
+        float S = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kGfConsumerWarps; ++w) S += tl->red_s[w];
+        const bool mine = have && y >= s0 && y < s0 + n_valid;
+        const float4 entry = make_float4(M, S, mine ? bf16_to_f32(x[y - s0]) : 0.0f,
+                                         mine ? 1.0f : 0.0f);
+        const int q = kc % kInbox;
+        const uint32_t ib = smem_addr(&tl->inbox_bar[q]);
+        mbar_arrive_expect_tx(ib, static_cast<uint32_t>(16 * C));
+        const uint32_t slot = smem_addr(&tl->inbox[q][rank]);
+        for (int c = 0; c < C; ++c)
+          st_async_v4(mapa_shared(slot, static_cast<uint32_t>(c)), entry,
+                      mapa_shared(ib, static_cast<uint32_t>(c)));
+      }
+    };
+    if (nk > 0) reduce_push(0);
+    for (int kc = 0; kc < nk; ++kc) {
+      if (kc + 1 < nk) reduce_push(kc + 1);
+      const int b = stage_of(kc);
+      const int64_t r = tl->meta_row[b];
+      const int32_t y = tl->meta_y[b];
+      const uint16_t* x = reinterpret_cast<const uint16_t*>(smem + b * buf_bytes);
+      const bool have = n_load > 0 && !tl->aborted;
+      if (cw == 0) {
+        // logsumexp of the row from the C entries of its inbox slot
+        const int q = kc % kInbox;
+        // every lane waits (each then sees the pushed entries)
+        if (!gf_wait(smem_addr(&tl->inbox_bar[q]), static_cast<uint32_t>((kc / kInbox) & 1), tmo, 4))
+          tl->aborted = 1;
+        const float4 e = lane < C ? tl->inbox[q][lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
+        float M = e.x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float S = e.x > -INFINITY ? e.y * fast_exp2((e.x - M) * kLog2e) : 0.0f;
+        float zy = e.w != 0.0f ? e.z : 0.0f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
+          zy += __shfl_xor_sync(0xFFFFFFFFu, zy, o);
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-        if (lane == 0) tl->red_s[cw] = sum;
-        consumer_sync();
-        if (ct == 0) {
-          float s = 0.0f;
-#pragma unroll
-          for (int w = 0; w < kGfConsumerWarps; ++w) s += tl->red_s[w];
-          const bool mine = have && y >= s0 && y < s0 + n_valid;
-          const float4 entry = make_float4(m, s, mine ? bf16_to_f32(x[y - s0]) : 0.0f,
-                                           mine ? 1.0f : 0.0f);
-          const int par = kc & 1;
-          const uint32_t ib = smem_addr(&tl->inbox_bar[par]);
-          mbar_arrive_expect_tx(ib, static_cast<uint32_t>(16 * C));
-          const uint32_t slot = smem_addr(&tl->inbox[par][rank]);
-          for (int c = 0; c < C; ++c)
-            st_async_v4(mapa_shared(slot, static_cast<uint32_t>(c)), entry,
-                        mapa_shared(ib, static_cast<uint32_t>(c)));
-          if (!gf_wait(ib, (kc >> 1) & 1u, tmo, 4)) tl->aborted = 1;
-          float M = -INFINITY, zy = 0.0f;
-          for (int c = 0; c < C; ++c) {
-            const float4 e = tl->inbox[par][c];
-            M = fmaxf(M, e.x);
-            if (e.w != 0.0f) zy = e.z;
-          }
-          float S = 0.0f;
-          for (int c = 0; c < C; ++c) {
-            const float4 e = tl->inbox[par][c];
-            if (e.x > -INFINITY) S += e.y * exp2f((e.x - M) * kLog2e);
-          }
+        if (lane == 0) {
           const float lse = M + log2f(S) * kLn2;
           tl->lse = lse;
           if (rank == 0) a.token_loss[r] = lse - zy;
         }
-        consumer_sync();
-        const float lse = tl->lse;
-        // gradient slice: (softmax - onehot) / n, from shared memory
-        if (a.dlogits && n_valid > 0) {
-          uint16_t* out = a.dlogits + r * a.ld_dlogits + s0;
-          const float lb = lse * kLog2e;
-          const int64_t yl = y - s0;  // the label's place in this slice (may be outside)
-          const int64_t vfull = n_valid & ~int64_t{7};
-          for (int64_t i = 8 * ct; i < vfull; i += 8 * kGfConsumers) {
-            const uint4 v = have ? *reinterpret_cast<const uint4*>(x + i) : make_uint4(0, 0, 0, 0);
-            float g[8];
+      }
+      consumer_sync();
+      const float lse = tl->lse;
+      // gradient slice: (softmax - onehot) / n, from shared memory
+      if (a.dlogits && n_valid > 0) {
+        uint16_t* out = a.dlogits + r * a.ld_dlogits + s0;
+        // p / n = 2^(z log2e - (lse log2e + log2 n)): the 1/n folded into
+        // the exponent
+        const float lb = fmaf(lse, kLog2e, log2n);
+        const int64_t yl = y - s0;  // the label's place in this slice (may be outside)
+        const int64_t vfull = n_valid & ~int64_t{7};
+        for (int64_t i = 8 * ct; i < vfull; i += 8 * kGfConsumers) {
+          float g[8];
+          unpack8(have ? *reinterpret_cast<const uint4*>(x + i) : make_uint4(0, 0, 0, 0), g);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              g[j] = exp2f(fmaf(lane_bf16(v, j), kLog2e, -lb)) * inv_n;
-              if (i + j == yl) g[j] -= inv_n;
-            }
-            __stcs(reinterpret_cast<int4*>(out + i),
-                   make_int4(static_cast<int>(pack2(g[0], g[1])), static_cast<int>(pack2(g[2], g[3])),
-                             static_cast<int>(pack2(g[4], g[5])), static_cast<int>(pack2(g[6], g[7]))));
+          for (int j = 0; j < 8; ++j) g[j] = fast_exp2(fmaf(g[j], kLog2e, -lb));
+          const int64_t d = yl - i;  // the label's element, if in this vector
+          if (d >= 0 && d < 8) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              if (j == d) g[j] -= inv_n;
           }
-          for (int64_t i = vfull + ct; i < n_valid; i += kGfConsumers) {
-            const float z = have ? bf16_to_f32(x[i]) : 0.0f;
-            float g = exp2f(fmaf(z, kLog2e, -lb)) * inv_n;
-            if (i == yl) g -= inv_n;
-            __nv_bfloat16 h = __float2bfloat16_rn(g);
-            out[i] = *reinterpret_cast<uint16_t*>(&h);
-          }
+          __stcs(reinterpret_cast<int4*>(out + i),
+                 make_int4(static_cast<int>(pack2(g[0], g[1])), static_cast<int>(pack2(g[2], g[3])),
+                           static_cast<int>(pack2(g[4], g[5])), static_cast<int>(pack2(g[6], g[7]))));
         }
-        ++kc;
+        for (int64_t i = vfull + ct; i < n_valid; i += kGfConsumers) {
+          const float z = have ? bf16_to_f32(x[i]) : 0.0f;
+          float g = fast_exp2(fmaf(z, kLog2e, -lb));
+          if (i == yl) g -= inv_n;
+          __nv_bfloat16 h = __float2bfloat16_rn(g);
+          out[i] = *reinterpret_cast<uint16_t*>(&h);
+        }
       }
       // this warp is done with the stage's buffer
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&tl->empty[b]));
-      if (++b == NB) {
-        b = 0;
-        ph ^= 1u;
-      }
     }
   }
   // no CTA leaves while a peer may still push into its inbox
@@ -446,45 +546,115 @@ int64_t goldfish_slice(int64_t vocab, int cluster) {
 
 int goldfish_cluster(int64_t vocab) {
   for (int c = 1; c <= 8; c *= 2)
-    if (goldfish_slice(vocab, c) * 2 <= kTargetSliceBytes) return c;
-  for (int c = 1; c <= 8; c *= 2)
     if (goldfish_slice(vocab, c) * 2 <= kMaxSliceBytes) return c;
   return 0;
 }
 
-cudaError_t goldfish_launch(const GoldfishArgs& a, int cluster, int sms, cudaStream_t stream) {
+namespace {
+
+// Ring depth and shared memory of the rows kernel for a slice.
+int ring_stages(int64_t slice) {
+  return static_cast<int>(std::min<int64_t>(kGfStages, kRingBytes / (slice * 2)));
+}
+size_t rows_smem(int64_t slice) {
+  return static_cast<size_t>(ring_stages(slice) * slice * 2) + sizeof(GfTail);
+}
+
+cudaLaunchConfig_t rows_config(int cluster, int64_t slice, int grid, cudaStream_t stream,
+                               cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kGfThreads, 1, 1);
+  cfg.dynamicSmemBytes = rows_smem(slice);
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// The cluster size for a vocabulary: among the sizes whose slices fit a ring
+// of at least two buffers, the one that keeps the most SMs busy when the
+// GPU holds as many clusters as it can at once (a cluster must fit in one
+// GPC, so fewer large clusters may fit than SMs / C), and its cluster
+// count.  Decided once per device and vocabulary.
+struct ClusterPick {
+  int64_t vocab = -1;
+  int device = -1;
+  int cluster = 0;
+  int resident = 0;
+};
+std::mutex g_pick_mu;
+ClusterPick g_picks[16];
+
+cudaError_t pick_cluster(int64_t vocab, int sms, int* cluster, int* resident) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_pick_mu);
+  for (const ClusterPick& c : g_picks)
+    if (c.vocab == vocab && c.device == dev) {
+      *cluster = c.cluster;
+      *resident = c.resident;
+      return cudaSuccess;
+    }
+  int best_c = 0, best_r = 0;
+  for (int c = 8; c >= 1; c /= 2) {
+    const int64_t slice = goldfish_slice(vocab, c);
+    if (slice * 2 > kMaxSliceBytes || ring_stages(slice) < 2) continue;
+    e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(rows_smem(slice)));
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = rows_config(c, slice, c * sms, nullptr, attr);
+    int r = 0;
+    if (cudaOccupancyMaxActiveClusters(&r, reinterpret_cast<const void*>(goldfish_rows_kernel),
+                                       &cfg) != cudaSuccess || r < 1) {
+      (void)cudaGetLastError();
+      r = std::max(1, sms / c);
+    }
+    if (best_c == 0 || r * c > best_r * best_c) {
+      best_c = c;
+      best_r = r;
+    }
+  }
+  if (best_c == 0) return cudaErrorInvalidValue;
+  static int next = 0;
+  g_picks[next] = ClusterPick{vocab, dev, best_c, best_r};
+  next = (next + 1) % 16;
+  *cluster = best_c;
+  *resident = best_r;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream) {
   const int64_t T = a.batch * a.seq;
   goldfish_mask_kernel<<<1, kMaskThreads, 0, stream>>>(a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  RowParams p;
-  p.a = a;
-  p.cluster = cluster;
-  p.slice = goldfish_slice(a.vocab, cluster);
-  p.stages = static_cast<int>(std::min<int64_t>(kGfStages, kRingBytes / (p.slice * 2)));
-  const size_t smem = static_cast<size_t>(p.stages * p.slice * 2) + sizeof(GfTail);
-  e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem));
-  if (e != cudaSuccess) return e;
-  // Persistent clusters: as many as fit at once (no cluster waits for
-  // another, so a larger grid would only queue), at most one per row.
-  const int per_sm = static_cast<int>(std::min<size_t>(4, (227 * 1024) / (smem + 1024)));
-  int64_t clusters = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1) / cluster;
-  if (clusters < 1) clusters = 1;
-  if (clusters > T) clusters = T;
   if (T > 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(clusters * cluster), 1, 1);
-    cfg.blockDim = dim3(kGfThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
+    int cluster = 0, resident = 0;
+    e = pick_cluster(a.vocab, sms, &cluster, &resident);
+    if (e != cudaSuccess) return e;
+    RowParams p;
+    p.a = a;
+    p.cluster = cluster;
+    p.slice = goldfish_slice(a.vocab, cluster);
+    p.stages = ring_stages(p.slice);
+    e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(rows_smem(p.slice)));
+    if (e != cudaSuccess) return e;
+    // Persistent clusters: as many as the GPU holds at once, at most one per
+    // row (with more, the rest would run as a second wave).
+    const int64_t clusters = std::min<int64_t>(resident, T);
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchConfig_t cfg = rows_config(cluster, p.slice, static_cast<int>(clusters * cluster),
+                                         stream, attr);
     e = cudaLaunchKernelEx(&cfg, goldfish_rows_kernel, p);
     if (e != cudaSuccess) return e;
   }

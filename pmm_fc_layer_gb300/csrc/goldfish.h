@@ -29,12 +29,13 @@ struct GoldfishArgs {
 int64_t goldfish_slice(int64_t vocab, int cluster);
 
 // Smallest cluster size in {1, 2, 4, 8} whose slice fits the per-CTA
-// shared-memory budget; 0 if none does.
+// shared-memory budget; 0 if none does (the vocabulary is too large).
 int goldfish_cluster(int64_t vocab);
 
-// The three launches (mask and count, rows, mean) on `stream`; `sms` sizes
-// the persistent grid.
-cudaError_t goldfish_launch(const GoldfishArgs& a, int cluster, int sms, cudaStream_t stream);
+// The three launches (mask and count, rows, mean) on `stream`.  The rows
+// kernel's cluster size is the feasible one that keeps the most of the
+// `sms` SMs busy (decided once per device and vocabulary).
+cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream);
 
 // Reads (and clears if set) the device error word of these kernels.
 cudaError_t goldfish_take_status(unsigned long long* word, cudaStream_t stream);

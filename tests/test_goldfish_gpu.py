@@ -11,12 +11,13 @@ fp64 oracle (oracle/goldfish.py).
 * The mean adds at most one more fp32 summation of T terms (8 in series per
   thread, then a 10-level tree): 1e-5 * (1 + |loss|) plus the per-token
   bound.
-* The gradient: softmax p = exp2(z log2e - lse log2e) in fp32.  Its
-  relative error is the error of logsumexp (below 1e-5 + |lse| 2^-22, as
-  above) plus the rounding of the two products in the exponent ((|z| +
-  |lse|) 2^-23) and of exp2 and the multiply by 1/n (2^-21).  The label's
-  entry subtracts 1/n (one more rounding, 2^-23 / n), and the result is
-  rounded once to bf16 (8 significant bits: at most 2^-8 relative).  So
+* The gradient: p / n = exp2(z log2e - (lse log2e + log2 n)) in fp32.
+  Its relative error is the error of logsumexp (below 1e-5 + |lse| 2^-22,
+  as above) plus the rounding of the products and sums in the exponent
+  ((|z| + |lse| + log2 n) 2^-23, with log2 n < 24 folded into the 1e-5)
+  and the SFU's exp2 (2^-21).  The label's entry subtracts 1/n (one more
+  rounding, 2^-23 / n), and the result is rounded once to bf16 (8
+  significant bits: at most 2^-8 relative).  So
   |g - g_ref| <= 2^-8 |g_ref| + (1 + 2^-8) (p_ref eps_p + 2^-23) / n with
   eps_p = 1e-5 + |lse| 2^-22 + (|z| + |lse|) 2^-23 + 2^-21.
 """
