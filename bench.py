@@ -681,7 +681,9 @@ def sampled_check(m, fc, row_band=256, col_band=512, seed=11):
     for g in m.plan:
         A, a_t, B, b_t = oracle.operands(g["op"], g["P"], g["Q"], False, False)
         M, N, _ = g["mnr"]
-        I, J = check_bands(M, N, rng, row_band, col_band)
+        # finer bands on small outputs: at least 16 x 16 sampled rows x columns
+        I, J = check_bands(M, N, rng, min(row_band, max(32, M // 16)),
+                           min(col_band, max(64, N // 16)))
         ii = torch.from_numpy(I).to(A.device)
         jj = torch.from_numpy(J).to(A.device)
         Ab = fc_inputs.from_torch_bf16(A.index_select(1 if a_t else 0, ii))
@@ -734,7 +736,8 @@ def workload_summary(m, fc, check=True):
         worst, entries = sampled_check(m, fc)
         out["check"] = {"max_error_ratio": worst, "entries": entries,
                         "what": "every GEMM, one random row per 256-row band x one random "
-                                "column per 512-column band, plus first/last rows and columns; "
+                                "column per 512-column band (finer on small outputs: at least "
+                                "16 x 16), plus first/last rows and columns; "
                                 "bound |C - C_ref| <= 1e-2 (|A|.|B|) + 1e-5"}
     return out
 
