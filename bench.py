@@ -600,10 +600,11 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
         dist.barrier()
     fc.axonn_sync_status(stream)
     elapsed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_ev), dev)
-    split_reduces = sum(1 for u in used if u and u[1] > 1)
-    sk_zeroing = sum(1 for t in sk_tiles if t > 0)   # the counter-zeroing kernel of a stream-K call
+    # the counter-zeroing kernel before a stream-K call (a split reduction
+    # is one launch)
+    sk_zeroing = sum(1 for t in sk_tiles if t > 0)
     # timed steps, plus (with graphs) the per-GEMM replays
-    launches = (steps * (len(plan) + reduce_launches + split_reduces + sk_zeroing)
+    launches = (steps * (len(plan) + reduce_launches + sk_zeroing)
                 * (1 if args.no_graph else 2))
 
     peaks = read_peaks()

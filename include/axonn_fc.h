@@ -136,8 +136,13 @@ typedef struct {
  *   ws / ws_bytes: device workspace, needed with AXONN_VGRID |
  *   AXONN_VGRID_PARTIALS when G_x > 1 (size from
  *   axonn_fc_workspace_size).  Otherwise optional: a full-size one enables
- *   the reduction split of small products and the stream-K tail of large
- *   ones; NULL / 0 runs without them.
+ *   the stream-K tail of large products; NULL / 0 runs without it.
+ *   Reduction split: a single product (no AXONN_VGRID) whose tiles leave
+ *   SMs idle may have its reduction range cut into S = 2, 4 or 8 pieces of
+ *   whole 64-deep stages, computed by the S CTAs of a thread-block cluster
+ *   and added in fixed order (pieces 0, 1, ..., S-1) inside it, with no
+ *   workspace and no extra launch.  Without a tuning entry it is chosen
+ *   for reductions of 32 stages or more; the tuner times S = 2, 4, 8.
  */
 axonn_status_t axonn_fc_fwd(const void* X, const void* W, void* Y, int64_t ldx, int64_t ldw,
                             int64_t ldy, const axonn_fc_shape_t* shape, uint32_t flags,
@@ -262,8 +267,9 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
  * arXiv 2502.08145).  Runs this call once per candidate -- kernel
  * configuration x rasterisation group {8, 16 tile rows; 8, 16 tile columns,
  * written -8, -16}, every configuration for products that leave SMs idle
- * (with reduction splits {2, 4, 8} when workspace is given), the 128x256 and
- * 256-row configurations otherwise, and the two best of them again with the
+ * (with reduction splits {2, 4, 8} of the 128x128 configuration, each piece
+ * at least 128 deep), the 128x256 and 256-row configurations otherwise,
+ * and the two best of them again with the
  * operand roles exchanged (see axonn_set_swap) -- and times each (through a captured
  * CUDA graph where the stream allows it) relative to the default choice run
  * just before and after it, so clock drift under the power cap cancels.  The
@@ -285,7 +291,9 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
 /* The tuning table as text, one JSON object per line:
  *   {"key": "...", "config": "<name>", "split": S, "group_m": G,
  *    "streamk": 0 | 1 | 2, "swap": 0 | 1, "us": t}
- * (S a whole number 1..8; G a whole number in -64..-1 or 1..64, tile rows
+ * (S a whole number 1..8, run as the largest power of two not above it
+ * or the product's stage count, and only on the 128x128 configuration;
+ * G a whole number in -64..-1 or 1..64, tile rows
  * per rasterisation group, negative for tile columns; streamk: off, on for
  * a partial round at most a quarter full, on wherever it applies; a line
  * without it loads as 1; swap: operand roles exchanged, see axonn_set_swap;
@@ -306,11 +314,10 @@ void axonn_last_choice(int* config, int* split, int* group_m);
  * axonn_op_t.  With AXONN_VGRID | AXONN_VGRID_PARTIALS it is the fp32
  * partials 0..G-2 of the reduced grid axis ((G-1) * M * ceil8(N) * 4); the
  * other virtual-grid forms need none.  Without AXONN_VGRID it is nonzero
- * for products that leave most SMs idle (fewer 128x256 tiles than two
- * waves), which may then split their reduction range, and for products of
- * more than one wave of 128x128 tiles, which may run a stream-K tail (see
- * axonn_set_streamk; up to about 80 MB on a 152-SM GPU).  Passing less
- * workspace just disables either.
+ * for products of more than one wave of 128x128 tiles, which may run a
+ * stream-K tail (see axonn_set_streamk; up to about 80 MB on a 152-SM GPU);
+ * the reduction split needs none.  Passing less workspace just disables
+ * the tail.
  * Returns AXONN_ERR_INVALID_ARG for a bad shape or flag. */
 axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, uint32_t flags,
                                        size_t* bytes);
@@ -394,8 +401,8 @@ axonn_status_t axonn_set_streamk(int mode);
  * two best configurations of each call, the row-major BLAS counterpart of
  * choosing among NN, NT and TN operand orders (the pages' "automated BLAS
  * kernel tuning": TL;DR of the sciencestack.ai page; review of arXiv
- * 2502.08145, "The reading").  It does not apply with a split reduction or
- * AXONN_VGRID_PARTIALS.  Results may differ from the unswapped call in the
+ * 2502.08145, "The reading").  It does not apply with AXONN_VGRID_PARTIALS.
+ * Results may differ from the unswapped call in the
  * last bit (another tile order of the same fp32 sums).  Host-only;
  * AXONN_ERR_INVALID_ARG for another mode. */
 axonn_status_t axonn_set_swap(int mode);

@@ -74,6 +74,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct DeviceState {
   int sms = 0;
   int max_pairs = 0;  // CTA pairs (clusters of 2) resident at once
+  // Clusters of the reduction-split kernel resident at once, by pieces:
+  // [1] 2 pieces, [2] 4, [3] 8.
+  int split_clusters[4] = {0, 0, 0, 0};
   bool attrs_set = false;
 };
 
@@ -126,6 +129,17 @@ axonn_status_t device_state(DeviceState** out) {
       clusters = d.sms / 2;
     }
     d.max_pairs = clusters;
+    e = axonn::split_kernel_init();
+    if (e != cudaSuccess)
+      return fail(AXONN_ERR_CUDA, "split kernel attributes: %s", cudaGetErrorString(e));
+    for (int lg = 1; lg <= 3; ++lg) {
+      int n = 0;
+      if (axonn::split_clusters_resident(d.sms, 1 << lg, &n) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        n = 0;  // this split is not offered on the device
+      }
+      d.split_clusters[lg] = n;
+    }
     d.attrs_set = true;
   }
   *out = &d;
@@ -349,13 +363,14 @@ struct LaunchPlan {
   int group_m = 16;
   std::vector<Block> blocks;
   int streamk = kStreamKOff;
+  int split = 1;       // pieces of the reduction split (cluster size), 1 = none
   void* ws = nullptr;  // workspace for the stream-K partials and counters
   size_t ws_bytes = 0;
 };
 
 // One way to run a call: kernel configuration, split of the reduction range
-// into `split` slices summed in fixed order (needs workspace), and the
-// rasterisation group height.
+// into `split` pieces summed in fixed order inside a cluster (configuration
+// 0 only), and the rasterisation group height.
 struct TuneChoice {
   int config = -1;
   int split = 1;
@@ -540,6 +555,25 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
   if (st != AXONN_OK || P.num_problems == 0) return st;
   const int slots = kConfigs[config].pair ? dev.max_pairs : dev.sms;
   const int units = P.total_tiles < slots ? P.total_tiles : slots;
+  if (plan.split > 1) {
+    // The reduction split: clusters of plan.split CTAs, one tile per
+    // cluster at a time, as many clusters as are resident at once.
+    t_last_sk_tiles = 0;
+    if constexpr (P1 == 1) {
+      const int lg = plan.split == 2 ? 1 : (plan.split == 4 ? 2 : 3);
+      const int resident = dev.split_clusters[lg];
+      if (config != 0 || P.num_problems != 1 || resident <= 0 || (plan.split & (plan.split - 1)) ||
+          plan.split > 8)
+        return fail(AXONN_ERR_UNSUPPORTED, "reduction split of %d pieces not available here", plan.split);
+      const int clusters = P.total_tiles < resident ? P.total_tiles : resident;
+      const cudaError_t e =
+          axonn::split_kernel_launch(P, plan.split, clusters, g_pdl.load() != 0, stream);
+      if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "split GEMM launch: %s", cudaGetErrorString(e));
+      return AXONN_OK;
+    } else {
+      return fail(AXONN_ERR_UNSUPPORTED, "reduction split of a multi-product launch");
+    }
+  }
   st = configure_streamk(P, kConfigs[config], units, plan, stream);
   if (st != AXONN_OK) return st;
   const cudaError_t e = axonn::kernels_launch<P1>(config, P, units, g_pdl.load() != 0, stream);
@@ -592,17 +626,32 @@ bool split_eligible(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
   return tiles < 2 * dev.sms && R >= 4 * kSplitMinR;
 }
 
-size_t split_ws_bytes(int64_t M, int64_t N, int split) {
-  const int64_t ldp = (N + 7) / 8 * 8;
-  return static_cast<size_t>(split) * static_cast<size_t>(M) * static_cast<size_t>(ldp) * 4u;
+// The reduction split runs on configuration 0 (128 x 128 tiles) only: the
+// kernel that holds a split tile's inbox beside its operand ring.
+bool split_config(int c) { return c == 0; }
+
+// The split actually run for a request of `want` pieces over nk reduction
+// steps: a power of two (the tile's 128 rows are dealt out in equal bands),
+// at most kMaxSplit and at most nk (no empty piece), or 1 for none.
+int split_pieces(int want, int64_t nk) {
+  int sp = 1;
+  while (sp * 2 <= want && sp * 2 <= kMaxSplit && sp * 2 <= nk) sp *= 2;
+  return sp;
 }
 
-// Default split: the largest power of two up to kMaxSplit that keeps the
-// 128x128 tiles within one wave and every slice at least kSplitMinR deep.
+// Default split (no tuning entry): only for reductions of at least
+// kSplitMinSteps 64-deep stages, where the pieces' shorter mainloops repay
+// the exchange of fp32 partials inside the cluster (measured on GB300: the
+// 256x512x2048 data gradient, 32 stages over 8 tiles, gains 16 % split in
+// 8; products of 8 to 16 stages lose).  Then the largest power of two up to
+// kMaxSplit that keeps at least 4 stages a piece and one CTA per SM.
+constexpr int64_t kSplitMinSteps = 32;
 int choose_split(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
   const int64_t tiles = ((M + 127) / 128) * ((N + 127) / 128);
+  const int64_t nk = (R + 63) / 64;
+  if (nk < kSplitMinSteps) return 1;
   int split = 1;
-  while (split < kMaxSplit && tiles * split * 2 <= dev.sms && R / (split * 2) >= kSplitMinR) split *= 2;
+  while (split < kMaxSplit && tiles * split * 2 <= dev.sms && nk / (split * 2) >= 4) split *= 2;
   return split;
 }
 
@@ -812,48 +861,22 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   if (ch.config < 0 || ch.config >= kNumConfigs) ch.config = choose_config(plan.blocks, *dev);
   if (ch.group_m == 0) ch.group_m = 16;
 
-  // Split of the reduction range: S slices of whole stages, fp32 partials in
-  // the workspace, then the fixed-order sum into the caller's output.
-  Block whole;
+  // Split of the reduction range into S pieces of whole stages, computed
+  // by the S CTAs of a cluster and summed in order inside it (the kernel's
+  // kSplit form): one launch, no workspace.  Single products only.
   if (ch.split > 1) {
     const Block& b0 = plan.blocks[0];
-    const bool ws_ok = !vgrid && ws && aligned16(ws) &&
-                       ws_bytes >= split_ws_bytes(b0.M, b0.N, ch.split) && b0.R >= ch.split;
-    if (!ws_ok) ch.split = 1;
-  }
-  int64_t ld_split = 0;
-  if (ch.split > 1) {
-    whole = plan.blocks[0];
-    plan.blocks.clear();
-    ld_split = (whole.N + 7) / 8 * 8;
-    const int64_t units = (whole.R + 63) / 64;
-    for (int sidx = 0; sidx < ch.split; ++sidx) {
-      const int64_t u0 = units * sidx / ch.split, u1 = units * (sidx + 1) / ch.split;
-      const int64_t r0 = 64 * u0, r1 = std::min<int64_t>(64 * u1, whole.R);
-      Block b = whole;
-      b.A = whole.A + 2 * (v.a_mn ? r0 * v.lda : r0);
-      b.B = whole.B + 2 * (v.b_mn ? r0 * v.ldb : r0);
-      b.R = r1 > r0 ? r1 - r0 : 0;
-      if (sidx < ch.split - 1) {
-        b.C = static_cast<char*>(ws) + 4 * (static_cast<int64_t>(sidx) * whole.M * ld_split);
-        b.ldc = ld_split;
-        b.out_mode = axonn::kOutF32;
-        b.phase = 0;
-      } else {
-        b.red_count = ch.split - 1;
-        b.red_src = reinterpret_cast<const float*>(ws);
-        b.red_stride = whole.M * ld_split;
-        b.red_ld = ld_split;
-      }
-      plan.blocks.push_back(b);
-    }
+    const bool able = !vgrid && plan.blocks.size() == 1 && split_config(ch.config);
+    ch.split = able ? split_pieces(ch.split, (b0.R + 63) / 64) : 1;
+    if (ch.split > 1 && dev->split_clusters[ch.split == 2 ? 1 : (ch.split == 4 ? 2 : 3)] <= 0)
+      ch.split = 1;
   }
   // Exchanged operand roles: C^T[N x M] = B^T . A^T, the same operands read
   // through each other's tensor-map role, written back transposed by the
-  // epilogue.  Not with a split reduction or the two-launch grid sum, whose
-  // fp32 partials are laid out in the caller's orientation.
+  // epilogue.  Not with the two-launch grid sum, whose fp32 partials are
+  // laid out in the caller's orientation.
   OpView lv = v;
-  if (ch.swap && (ch.split > 1 || partials)) ch.swap = 0;
+  if (ch.swap && partials) ch.swap = 0;
   if (ch.swap) {
     lv.A = v.B; lv.lda = v.ldb; lv.a_mn = v.b_mn;
     lv.B = v.A; lv.ldb = v.lda; lv.b_mn = v.a_mn;
@@ -866,8 +889,9 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
   }
   plan.config = ch.config;
   plan.group_m = ch.group_m;
-  if (!vgrid && ch.split == 1) {
-    plan.streamk = ch.streamk;
+  plan.split = ch.split;
+  if (!vgrid) {
+    if (ch.split == 1) plan.streamk = ch.streamk;
     plan.ws = ws;
     plan.ws_bytes = ws_bytes;
   }
@@ -1176,10 +1200,9 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
     for (int gm : {8, 16, -8, -16}) cands.push_back(TuneChoice{c, 1, gm});
   }
   if (!(flags & AXONN_VGRID) && small)
-    for (int c = 0; c < 2; ++c)
-      for (int sp = 2; sp <= kMaxSplit; sp *= 2)
-        if (red.len() / sp >= kSplitMinR && ws && ws_bytes >= split_ws_bytes(rows.len(), cols.len(), sp))
-          cands.push_back(TuneChoice{c, sp, 16});
+    for (int sp = 2; sp <= kMaxSplit; sp *= 2)
+      if (red.len() / sp >= kSplitMinR)
+        for (int gm : {16, -16}) cands.push_back(TuneChoice{0, sp, gm});
 
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {
@@ -1459,7 +1482,8 @@ axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, ui
   }
   *bytes = vgrid_ws_bytes(op, *shape, flags);
   if (!(flags & AXONN_VGRID)) {
-    // Products that leave SMs idle may split their reduction range.
+    // The reduction split needs none; products of more than one wave of
+    // tiles may run a stream-K tail.
     DeviceState* dev = nullptr;
     if (device_state(&dev) == AXONN_OK) {
       const axonn_fc_shape_t& s = *shape;
@@ -1467,9 +1491,6 @@ axonn_status_t axonn_fc_workspace_size(int op, const axonn_fc_shape_t* shape, ui
       full_dims(op, s, &M, &N, &R);
       Range rows{0, M}, red{0, R}, cols{0, N};
       if (s.gx * s.gy * s.gz > 1) block_ranges(op, s, s.x, s.y, s.z, &rows, &red, &cols);
-      if (rows.len() > 0 && cols.len() > 0 && split_eligible(rows.len(), cols.len(), red.len(), *dev))
-        *bytes = split_ws_bytes(rows.len(), cols.len(), kMaxSplit);
-      // Products of more than one wave of tiles may run a stream-K tail.
       const int64_t tiles128 = ((rows.len() + 127) / 128) * ((cols.len() + 127) / 128);
       if (tiles128 > dev->sms)
         for (const KernelConfig& c : kConfigs)

@@ -139,8 +139,22 @@ enum WorkKind : int { kWhole = 0, kHead = 1, kTail = 2 };
 // compile as they do without stream-K (an iterator object there slowed the
 // producer's issue loop by 14 %).  The host keeps sk_tiles * num_k below
 // 2^31.
-template <int MAXP, typename F>
+//
+// The reduction-split kernel (kSplit) walks instead the tiles c, c + C, ...
+// of its cluster c (C clusters), this CTA taking piece `rank` of each: steps
+// [nk rank / S, nk (rank + 1) / S) of S, S the cluster's size.
+template <bool kSplit = false, int MAXP, typename F>
 __device__ __forceinline__ void for_each_work(const GemmParams<MAXP>& P, int u, int units, F&& f) {
+  if constexpr (kSplit) {
+    const int S = static_cast<int>(cluster_nctarank());
+    const int rank = static_cast<int>(cluster_ctarank());
+    const int nk = P.prob[0].num_k;
+    const int k0 = nk * rank / S, k1 = nk * (rank + 1) / S;
+    const int nc = static_cast<int>(num_clusters_x());
+    for (int t = static_cast<int>(cluster_id_x()); t < P.total_tiles; t += nc)
+      if (!f(t, k0, k1, kWhole)) return;
+    return;
+  }
   const int dp_end = P.total_tiles - P.sk_tiles;
   for (int t = u; t < dp_end; t += units)
     if (!f(t, 0, -1, kWhole)) return;
@@ -172,6 +186,9 @@ enum WaitSite : uint32_t {
   kSiteEpiTmemFull = 4,
   kSiteDrainLoads = 5,
   kSiteDrainMma = 6,
+  kSiteSplitFree = 7,
+  kSiteSplitInbox = 8,
+  kSiteSplitStaged = 9,
 };
 
 __device__ __forceinline__ void record_timeout(uint32_t site) {
@@ -196,6 +213,30 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint
     // tensor cores.  The limit and abort checks still run every poll.
     if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
     if (honor_abort && *abort_flag) return false;
+    if (global_timer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      record_timeout(site);
+      return false;
+    }
+  }
+}
+
+// Bounded wait that polls without ever suspending the thread, for the
+// reduction split's waits, which are short and on its critical path: a
+// warp whose thread has come back from a suspending try_wait was measured
+// to run the code after it several times slower for thousands of cycles
+// (the split's band sums, on GB300).  `cluster` gives the test acquire
+// semantics at cluster scope (a phase completed by other CTAs).  The clock
+// and abort flag are read every 256 polls.
+template <bool kCluster>
+__device__ __forceinline__ bool wait_polling(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                             volatile int* abort_flag, uint32_t site) {
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
     if (global_timer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       record_timeout(site);
@@ -559,16 +600,124 @@ __device__ __forceinline__ void epilogue_item(const GemmParams<MAXP>& P, const P
   }
 }
 
-template <int BN, int BK, int STAGES, int MH = 1>
+// Four consecutive output columns col..col+3 of one row (the reduction
+// split's epilogue): one vector access where all four exist and the address
+// allows it, else one per column.  Rounding and output modes as store_chunk,
+// transposed (out_t) as store_chunk_t.
+__device__ __forceinline__ void store_quad(const ProblemDesc& d, int row, int col, float4 v) {
+  const int n = min(4, d.N - col);
+  const float x[4] = {v.x, v.y, v.z, v.w};
+  if (d.out_t) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (j >= n) continue;
+      const int64_t at = static_cast<int64_t>(col + j) * d.ldc + row;
+      if (d.out_mode == kOutBF16) {
+        reinterpret_cast<__nv_bfloat16*>(d.C)[at] = __float2bfloat16_rn(x[j]);
+      } else {
+        float* o = reinterpret_cast<float*>(d.C) + at;
+        if (d.out_mode == kOutF32Red || d.out_mode == kOutF32Accum) red_add_f32(o, __float_as_uint(x[j]));
+        else *o = x[j];
+      }
+    }
+    return;
+  }
+  if (d.out_mode == kOutBF16) {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(d.C) + row * d.ldc + col;
+    if (n == 4 && (reinterpret_cast<uintptr_t>(o) & 7u) == 0) {
+      __stwb(reinterpret_cast<uint2*>(o), make_uint2(pack_bf16x2(__float_as_uint(v.x), __float_as_uint(v.y)),
+                                                     pack_bf16x2(__float_as_uint(v.z), __float_as_uint(v.w))));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (j < n) o[j] = __float2bfloat16_rn(x[j]);
+    }
+    return;
+  }
+  float* o = reinterpret_cast<float*>(d.C) + row * d.ldc + col;
+  const bool add = d.out_mode == kOutF32Red || d.out_mode == kOutF32Accum;
+  if (n == 4 && (reinterpret_cast<uintptr_t>(o) & 15u) == 0) {
+    if (add)
+      red_add_v4_f32(o, __float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                     __float_as_uint(v.w));
+    else
+      *reinterpret_cast<float4*>(o) = v;
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if (j >= n) continue;
+    if (add) red_add_f32(o + j, __float_as_uint(x[j]));
+    else o[j] = x[j];
+  }
+}
+
+// The reduction split's band sum for S pieces (S a compile-time constant,
+// so that all S loads of a row are issued before the adds): warp q takes
+// band rows q, q + 4, ...; a lane four consecutive columns.  Piece g's rows
+// are this CTA's staged rows when g == me, else block g (g < me) or g - 1
+// (g > me) of the inbox (shared-memory addresses); rows are kLd floats
+// apart.  The sum runs over
+// pieces 0, 1, ..., S-1 in that order.
+template <int S, int BN, int kLd>
+__device__ __forceinline__ void split_band_sum(uint32_t own, uint32_t inboxed, int me, int q,
+                                               int lane, int row0, int n0, const ProblemDesc& od) {
+  constexpr int band = kBM / S;
+  const bool bf16_rows = od.out_mode == kOutBF16 && !od.out_t;
+  for (int i = q; i < band; i += kEpiWarps) {
+    const int row = row0 + i;
+    if (row >= od.M) break;
+#pragma unroll
+    for (int cb = 0; cb < BN; cb += 128) {
+      const int col = cb + 4 * lane;
+      if (col >= BN || n0 + col >= od.N) continue;
+      float4 x[S];
+#pragma unroll
+      for (int g = 0; g < S; ++g) {
+        const int at = g == me ? i * kLd + col : ((g < me ? g : g - 1) * band + i) * kLd + col;
+        x[g] = ld_shared_v4((g == me ? own : inboxed) + static_cast<uint32_t>(at * 4));
+      }
+      float4 a = x[0];
+#pragma unroll
+      for (int g = 1; g < S; ++g) {
+        a.x += x[g].x;
+        a.y += x[g].y;
+        a.z += x[g].z;
+        a.w += x[g].w;
+      }
+      // bf16 rows with all four columns present and the address aligned:
+      // one 8-byte store (measured a third cheaper than store_quad's
+      // general path here); the other cases through store_quad.
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(od.C) + row * od.ldc + n0 + col;
+      if (bf16_rows && n0 + col + 4 <= od.N && (reinterpret_cast<uintptr_t>(o) & 7u) == 0)
+        *reinterpret_cast<uint2*>(o) = make_uint2(pack_bf16x2(__float_as_uint(a.x), __float_as_uint(a.y)),
+                                                  pack_bf16x2(__float_as_uint(a.z), __float_as_uint(a.w)));
+      else
+        store_quad(od, row, n0 + col, a);
+    }
+  }
+}
+
+// kSplit adds the reduction split's staging tile (this piece's 128 x BN
+// fp32 rows, each padded by 16 bytes so that a warp's row-per-lane stores
+// and row-wise loads meet no bank conflict), its inbox (the other pieces'
+// rows of this CTA's band: at most 7 bands of 16 rows, or 1 of 64, i.e.
+// 128 - 128/S rows for S = 2, 4, 8) and three barriers.
+constexpr int kSplitMaxPieces = 8;
+template <int BN, int BK, int STAGES, int MH = 1, bool kSplit = false>
 struct SmemLayout {
   static constexpr int kAHalfBytes = kBM * BK * 2;
   static constexpr int kABytes = MH * kAHalfBytes;
   static constexpr int kBBytes = BN * BK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kNumBars = 2 * STAGES + 5;
-  // 1024 B of slack for aligning the tile ring, the ring, barriers, TMEM slot
-  // and the abort flag.
-  static constexpr int kBytes = 1024 + STAGES * kStageBytes + kNumBars * 8 + 16;
+  static constexpr int kSplitLd = BN + 4;  // floats per staged row
+  static constexpr int kStagingBytes = kSplit ? kBM * kSplitLd * 4 : 0;
+  static constexpr int kInboxBytes = kSplit ? (kBM - kBM / kSplitMaxPieces) * kSplitLd * 4 : 0;
+  static constexpr int kNumBars = 2 * STAGES + 5 + (kSplit ? 3 : 0);
+  // 1024 B of slack for aligning the tile ring, the ring, the staging tile
+  // and inbox, barriers, TMEM slot and the abort flag.
+  static constexpr int kBytes =
+      1024 + STAGES * kStageBytes + kStagingBytes + kInboxBytes + kNumBars * 8 + 16;
 };
 
 // Shared-memory descriptor of the K=16 slice kk of a stage's operand tile.
@@ -587,10 +736,25 @@ __device__ __forceinline__ uint64_t operand_desc(uint32_t tile, int kk, bool mn_
 // MH = 2: 256 x BN tiles as two M = 128 MMAs sharing each B slice (a third
 // fewer operand bytes per FLOP); the two accumulators fill TMEM (2 x BN
 // columns, single-buffered) and 8 epilogue warps drain them.
-template <int BN, int BK, int STAGES, int MAXP, int MH = 1>
+//
+// kSplit (MH = 1, one problem): the reduction split.  The launch is made
+// of clusters of S CTAs (S = 2, 4 or 8); a cluster owns whole tiles and its
+// CTA of rank p computes piece p of each (see for_each_work) into TMEM.  The
+// 128 rows of a tile are dealt out in S bands of 128/S, band o finished by
+// CTA o.  Each CTA pushes its piece's rows, fp32, into the inbox of the
+// band's CTA (st.async into that CTA's shared memory, counted in bytes on
+// its inbox barrier), at block p of that inbox.  Once its inbox is full a
+// CTA adds blocks 0, 1, ..., S-1 in that order -- the pieces in reduction
+// order, whatever order they arrived in -- and writes its band to the
+// output; then it tells every CTA of the cluster (their "free" barriers)
+// that their blocks have been read and the inbox may take the next tile.
+// No workspace and no second launch; pieces meet only inside the cluster,
+// whose CTAs the hardware schedules together.
+template <int BN, int BK, int STAGES, int MAXP, int MH = 1, bool kSplit = false>
 __global__ void __launch_bounds__(cta_threads<MH>(), 1)
     fc_gemm_tcgen05_kernel(const __grid_constant__ GemmParams<MAXP> P) {
-  using L = SmemLayout<BN, BK, STAGES, MH>;
+  using L = SmemLayout<BN, BK, STAGES, MH, kSplit>;
+  static_assert(!kSplit || (MH == 1 && MAXP == 1), "reduction split: 128-row tiles, one problem");
   static_assert(BK == 64 || BK == 32, "stage depth");
   static_assert(MH == 1 || MH == 2, "row halves per CTA");
   constexpr int kAccBufs = MH == 1 ? 2 : 1;
@@ -608,7 +772,11 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t ring = (raw + 1023u) & ~1023u;
   uint8_t* ring_ptr = smem_raw + (ring - raw);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * L::kStageBytes);
+  // kSplit only: staging tile, then inbox, after the ring
+  const uint32_t staging = ring + STAGES * L::kStageBytes;
+  const uint32_t inbox = staging + L::kStagingBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring_ptr + STAGES * L::kStageBytes +
+                                               L::kStagingBytes + L::kInboxBytes);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + L::kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -618,6 +786,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   auto tfull_bar = [&](int b) { return smem_addr(bars + 2 * STAGES + b); };
   auto tempty_bar = [&](int b) { return smem_addr(bars + 2 * STAGES + 2 + b); };
   const uint32_t mma_done_bar = smem_addr(bars + 2 * STAGES + 4);
+  const uint32_t inbox_full = smem_addr(bars + 2 * STAGES + 5);  // kSplit only
+  const uint32_t split_free = smem_addr(bars + 2 * STAGES + 6);  // kSplit only
+  const uint32_t staged_bar = smem_addr(bars + 2 * STAGES + 7);  // kSplit only
   auto a_tile = [&](int s) { return ring + s * L::kStageBytes; };
   auto b_tile = [&](int s) { return ring + s * L::kStageBytes + L::kABytes; };
 
@@ -634,6 +805,11 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       mbar_init(tempty_bar(b), kEpiWarps * MH);
     }
     mbar_init(mma_done_bar, 1);
+    if constexpr (kSplit) {
+      mbar_init(inbox_full, 1);
+      mbar_init(split_free, kEpiWarps * cluster_nctarank());
+      mbar_init(staged_bar, kEpiWarps);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -650,8 +826,16 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // The cluster's barriers exist before any CTA signals or stores into them.
+  if constexpr (kSplit) cluster_sync();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t tmo = P.timeout_ns;
+  // The pipeline's waits: suspending ones, except in the reduction split,
+  // whose pieces are a few stages long (see wait_polling).
+  auto wait_pipe = [&](uint32_t bar, uint32_t parity, uint32_t site) -> bool {
+    if constexpr (kSplit) return wait_polling<false>(bar, parity, tmo, abort_flag, site);
+    else return wait_bounded(bar, parity, tmo, abort_flag, site);
+  };
   // Barrier set-up, TMEM allocation and tensor-map prefetch above overlap
   // the previous kernel's tail; nothing below touches global memory before
   // that kernel is complete.
@@ -663,7 +847,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t loads = 0;
-      for_each_work(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
+      for_each_work<kSplit>(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
         ChainPos cp = chain_start(P, d, k0);
@@ -673,8 +857,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
         const int n0 = tc.n_blk * BN;
         const int kend = k1 < 0 ? d.num_k : k1;
         for (int k = k0; k < kend; ++k) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, tmo, abort_flag, kSiteProducerEmpty))
-            return false;
+          if (!wait_pipe(empty_bar(stage), phase ^ 1u, kSiteProducerEmpty)) return false;
           const uint32_t fb = full_bar(stage);
           mbar_arrive_expect_tx(fb, L::kStageBytes);
           const int r0 = cp.kl * BK;
@@ -734,18 +917,18 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t acc = 0;
-      for_each_work(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
+      for_each_work<kSplit>(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
         const int kend = k1 < 0 ? d.num_k : k1;
         if (kend <= k0) return true;
         const uint32_t b = acc % kAccBufs;
         const uint32_t acc_phase = (acc / kAccBufs) & 1u;
-        if (!wait_bounded(tempty_bar(b), acc_phase ^ 1u, tmo, abort_flag, kSiteMmaTmemEmpty)) return false;
+        if (!wait_pipe(tempty_bar(b), acc_phase ^ 1u, kSiteMmaTmemEmpty)) return false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kAccCols;
         for (int k = k0; k < kend; ++k) {
-          if (!wait_bounded(full_bar(stage), phase, tmo, abort_flag, kSiteMmaFull)) return false;
+          if (!wait_pipe(full_bar(stage), phase, kSiteMmaFull)) return false;
           tc_fence_after();
           const uint32_t sa = a_tile(stage);
           const uint32_t sb = b_tile(stage);
@@ -772,7 +955,120 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       umma_commit(mma_done_bar);
       wait_bounded(mma_done_bar, 0, tmo, abort_flag, kSiteDrainMma, false);
     }
-  } else if (warp >= epi_first_warp<MH>()) {
+  } else if (kSplit && warp >= epi_first_warp<MH>()) {
+    // ------------------------------------------- epilogue, reduction split
+    // Per tile: this piece's rows go to the staging tile; one bulk copy per
+    // other CTA o of the cluster sends band o of them into o's inbox,
+    // counted on o's inbox barrier; this CTA's own band stays in place.
+    // The inbox holds the other pieces' blocks of this CTA's band in piece
+    // order, piece g at block g (g < me) or g - 1 (g > me).
+    constexpr int kLd = L::kSplitLd;
+    const int q = warp & 3;  // TMEM lane quarter: tile rows 32q .. 32q+31
+    const uint32_t S = cluster_nctarank();
+    const uint32_t me = cluster_ctarank();
+    const int band = kBM / static_cast<int>(S);  // rows each CTA finishes
+    const int r = q * 32 + lane;                  // the tile row this lane stages
+    const uint32_t band_bytes = static_cast<uint32_t>(band * kLd * 4);
+    uint32_t acc = 0, item = 0;
+    for_each_work<kSplit>(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
+      const TileCoord tc = decode_tile(P, t);
+      const ProblemDesc& d = P.prob[tc.p];
+      const int m0 = tc.m_blk * kTileM;
+      const int n0 = tc.n_blk * BN;
+      // 1. Every CTA has finished with this CTA's staging tile and inbox of
+      // the previous tile; the inbox (its previous phase complete) is told
+      // what this tile brings.
+      int ok = 1;
+      if (lane == 0) {
+        if (item > 0)
+          ok = wait_polling<true>(split_free, (item - 1) & 1u, tmo, abort_flag, kSiteSplitFree);
+        if (ok && q == 0) mbar_arrive_expect_tx(inbox_full, (S - 1) * band_bytes);
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) return false;
+      // 2. This piece's rows, fp32, to the staging tile (the whole tile,
+      // ragged edges included: the copies are whole bands).
+      const bool has = (k1 < 0 ? d.num_k : k1) > k0;
+      const uint32_t b = acc % kAccBufs;
+      if (has) {
+        if (lane == 0)
+          ok = wait_polling<false>(tfull_bar(b), (acc / kAccBufs) & 1u, tmo, abort_flag, kSiteEpiTmemFull);
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) return false;
+        tc_fence_after();
+      }
+      const uint32_t t_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols;
+      const uint32_t my_row = staging + static_cast<uint32_t>(r * kLd * 4);
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t v[32];
+        if (has) {
+          tmem_ld_32x32b_x32(t_row + c * 32, v);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0u;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          st_shared_v4(my_row + static_cast<uint32_t>((c * 32 + 4 * j) * 4), v[4 * j], v[4 * j + 1],
+                       v[4 * j + 2], v[4 * j + 3]);
+      }
+      if (has) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(b));
+        ++acc;
+      }
+      // 3. The staged rows are made visible to the copy engine and counted
+      // on the staged barrier; once all four warps have staged theirs, one
+      // thread sends each other CTA its band.
+      fence_proxy_async_shared();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(staged_bar);
+      if (q == 0) {
+        if (lane == 0) {
+          ok = wait_polling<false>(staged_bar, item & 1u, tmo, abort_flag, kSiteSplitStaged);
+          for (uint32_t o = 0; ok && o < S; ++o) {
+            if (o == me) continue;
+            const uint32_t blk = me < o ? me : me - 1;
+            bulk_copy_to_cluster(mapa_shared(inbox + blk * band_bytes, o), staging + o * band_bytes,
+                                 band_bytes, mapa_shared(inbox_full, o));
+          }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) return false;
+      }
+      // 4. Every other piece of this CTA's band has arrived.
+      if (lane == 0) ok = wait_polling<true>(inbox_full, item & 1u, tmo, abort_flag, kSiteSplitInbox);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) return false;
+      // 5. Pieces 0..S-1 added in that order, the band written out (see
+      // split_band_sum).  The output's fields are copied out of the
+      // parameter block first (the stores go through generic pointers,
+      // after which the compiler would read them again from there every
+      // row).
+      ProblemDesc od{};
+      od.C = d.C;
+      od.ldc = d.ldc;
+      od.M = d.M;
+      od.N = d.N;
+      od.out_mode = d.out_mode;
+      od.out_t = d.out_t;
+      const int row0 = m0 + static_cast<int>(me) * band;
+      const uint32_t own = staging + me * band_bytes;
+      if (S == 2) split_band_sum<2, BN, kLd>(own, inbox, static_cast<int>(me), q, lane, row0, n0, od);
+      else if (S == 4) split_band_sum<4, BN, kLd>(own, inbox, static_cast<int>(me), q, lane, row0, n0, od);
+      else split_band_sum<8, BN, kLd>(own, inbox, static_cast<int>(me), q, lane, row0, n0, od);
+      // 6. This warp is done with the staging tile and inbox: one arrival
+      // on every CTA's free barrier (kEpiWarps per CTA).
+      __syncwarp();
+      if (lane == 0)
+        for (uint32_t g = 0; g < S; ++g) mbar_arrive_cluster(mapa_shared(split_free, g));
+      ++item;
+      return true;
+    });
+  } else if (!kSplit && warp >= epi_first_warp<MH>()) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int hh = (warp - epi_first_warp<MH>()) >> 2;  // row half it drains
@@ -805,6 +1101,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // No CTA leaves while another may still store into its inbox or arrive
+  // on its barriers.
+  if constexpr (kSplit) cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);

@@ -190,16 +190,6 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGfConsumers) : "memory");
 }
 
-// 16-byte store into (possibly another CTA's) shared memory whose
-// completion is counted, in bytes, on an mbarrier of that CTA.
-__device__ __forceinline__ void st_async_v4(uint32_t cluster_addr, float4 v, uint32_t cluster_bar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          cluster_addr),
-      "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(cluster_bar)
-      : "memory");
-}
-
 // The eight bf16 values of a 16-byte vector as floats (exact): a bf16 is
 // the high half of a float, so the high half of each 32-bit word is masked
 // out in place and the low half shifted up.

@@ -9,6 +9,25 @@ namespace axonn {
 constexpr int kPairStages = 6;   // 256 x 256 pair tiles, 32 KB stages
 constexpr int kPair2Stages = 4;  // 512 x 256 pair tiles, 48 KB stages
 
+// Launch attributes: programmatic stream serialization (pdl) and, when
+// cluster > 0, the cluster size along x.
+inline int launch_attrs(cudaLaunchAttribute (&attr)[2], bool pdl, int cluster) {
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  return n;
+}
+
 // Launches `kernel` with cudaLaunchKernelEx; with `pdl` the launch may begin
 // while the previous kernel in the stream finishes (programmatic stream
 // serialization; the kernel waits for it with griddepcontrol.wait).
@@ -20,11 +39,9 @@ cudaError_t launch_ex(K kernel, const GemmParams<MAXP>& P, int ctas, int threads
   cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = static_cast<unsigned>(launch_attrs(attr, pdl, 0));
   return cudaLaunchKernelEx(&cfg, kernel, P);
 }
 

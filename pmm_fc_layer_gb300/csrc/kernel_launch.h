@@ -38,4 +38,13 @@ cudaError_t kernels_take_status(unsigned long long* word, cudaStream_t stream);
 // Clusters of 2 of the pair kernels that can be resident at once.
 cudaError_t pair_clusters_resident(int sms, int* clusters);
 
+// The reduction-split kernel (128 x 128 tiles, one problem; see
+// fc_gemm_tcgen05_kernel's kSplit): its shared-memory limit, how many of
+// its clusters of `pieces` CTAs (2, 4 or 8) can be resident at once, and a
+// launch of `clusters` such clusters.
+cudaError_t split_kernel_init();
+cudaError_t split_clusters_resident(int sms, int pieces, int* clusters);
+cudaError_t split_kernel_launch(const GemmParams<1>& P, int pieces, int clusters, bool pdl,
+                                cudaStream_t stream);
+
 }  // namespace axonn

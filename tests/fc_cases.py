@@ -56,8 +56,8 @@ def to_device(bits):
 def run_gpu(fc, op, P, Q, p_t, q_t, T, K, N, grid=(1, 1, 1), coords=(0, 0, 0), extra=0,
             out=None, out_f32=False, local_shape=None, workspace=True):
     """Call the op through the C ABI; returns the output tensor.  With
-    workspace=False no workspace is passed (no reduction split, no stream-K
-    tail)."""
+    workspace=False no workspace is passed (no stream-K tail, no two-launch
+    grid sum)."""
     import torch
     Pd, Qd = to_device(P), to_device(Q)
     flags = (fc.A_T if p_t else 0) | (fc.B_T if q_t else 0) | extra

@@ -33,8 +33,6 @@ def test_swap_integer_exact(cuda_lib, swapped, cfg, op, p_t, q_t, T, K, N):
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, p_t, seed=501, kind="int")
     Q = make_operand(qn, T, K, N, q_t, seed=501, kind="int")
-    # no workspace: a reduction split (which the swap does not apply to)
-    # would otherwise be the default for these small products
     out = run_gpu(cuda_lib, op, P, Q, p_t, q_t, T, K, N, workspace=False)
     assert cuda_lib.axonn_last_swap() == 1
     C, _ = oracle.fc(op, P, Q, p_t, q_t)
@@ -110,7 +108,7 @@ def test_swap_with_streamk_tail_exact(cuda_lib, swapped, cfg, op):
     assert np.array_equal(host_bits(out), oracle.bf16_rne(C))
 
 
-def test_swap_not_applied_to_split_or_partials(cuda_lib, swapped):
+def test_swap_not_applied_to_partials_but_to_split(cuda_lib, swapped):
     fc = cuda_lib
     T, K, N = 300, 200, 520
     X = make_operand("X", T, K, N, False, seed=509, kind="int")
@@ -119,10 +117,13 @@ def test_swap_not_applied_to_split_or_partials(cuda_lib, swapped):
                   extra=fc.VGRID | fc.VGRID_PARTIALS)
     assert fc.axonn_last_swap() == 0
     assert np.array_equal(host_bits(out), oracle.bf16_rne(oracle.fc_fwd(X, W)[0]))
-    # a small product that splits its reduction (workspace given)
+    # a small product whose reduction (33 stages) the default choice splits:
+    # the split's epilogue stores the transposed band
+    N = 2100
     dY = make_operand("dY", T, K, N, False, seed=509, kind="int")
+    W = make_operand("W", T, K, N, False, seed=509, kind="int")
     out = run_gpu(fc, "dgrad", dY, W, False, False, T, K, N)
-    assert fc.axonn_last_choice()[1] > 1 and fc.axonn_last_swap() == 0
+    assert fc.axonn_last_choice()[1] > 1 and fc.axonn_last_swap() == 1
     assert np.array_equal(host_bits(out), oracle.bf16_rne(oracle.fc_dgrad(dY, W)[0]))
 
 

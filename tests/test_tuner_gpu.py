@@ -38,25 +38,29 @@ def clean_cache(cuda_lib):
 
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 def test_small_layer_splits_reduction(clean_cache, op):
-    """The 256x512x2048 layer leaves most SMs idle: with workspace the
-    default choice splits the reduction range; without, it does not."""
+    """The 256x512x2048 layer leaves most SMs idle.  The default choice
+    splits only long reductions: the data gradient's 32 stages over 8 tiles,
+    with or without a workspace (the split needs none); not the forward
+    product's 8 stages, nor the weight gradient's 4."""
     fc = clean_cache
     T, K, N = 256, 512, 2048
     pn, qn = operand_names(op)
     P = make_operand(pn, T, K, N, False, seed=101, kind="int")
     Q = make_operand(qn, T, K, N, False, seed=101, kind="int")
     want = oracle.bf16_rne(oracle.fc(op, P, Q)[0])
-    out, choice, _ = _call(fc, op, P, Q, T, K, N)
-    assert np.array_equal(host_bits(out), want)
-    if op != "wgrad":          # wgrad reduces over T = 256: too short to split
-        assert choice[1] > 1, choice
-    out2, choice2, _ = _call(fc, op, P, Q, T, K, N, use_ws=False)
-    assert choice2[1] == 1
-    assert np.array_equal(host_bits(out2), want)
+    for use_ws in (True, False):
+        out, choice, _ = _call(fc, op, P, Q, T, K, N, use_ws=use_ws)
+        assert np.array_equal(host_bits(out), want)
+        if op == "dgrad":
+            assert choice[0] == 0 and choice[1] == 8, choice
+        else:
+            assert choice[1] == 1, choice
 
 
 def test_every_split_and_config_exact(clean_cache, tmp_path):
-    """Drive each (config, split, group) through a loaded tuning entry."""
+    """Drive each (config, split, group) through a loaded tuning entry.  The
+    reduction split runs on configuration 0 (128 x 128 tiles); the others
+    run such an entry unsplit."""
     fc = clean_cache
     T, K, N = 300, 1000, 520
     P = make_operand("X", T, K, N, False, seed=103, kind="int")
@@ -72,7 +76,7 @@ def test_every_split_and_config_exact(clean_cache, tmp_path):
                                             "split": split, "group_m": gm, "us": 1.0}) + "\n")
                 fc.axonn_tune_cache_load(str(path))
                 out, choice, _ = _call(fc, "fwd", P, Q, T, K, N)
-                assert choice == (cfg, split, gm)
+                assert choice == (cfg, split if cfg == 0 else 1, gm)
                 bad = np.argwhere(host_bits(out) != want)
                 assert bad.size == 0, (cfg, split, gm, bad[:3].tolist())
 
