@@ -881,6 +881,10 @@ def run_ours(args):
     _b.build()
     fc.load()
     fc.axonn_set_kernel_config(args.config)
+    if args.no_streamk:
+        fc.axonn_set_streamk(0)
+    if args.l2_budget is not None:
+        fc.axonn_set_l2_budget(int(args.l2_budget) << 20)
     sms, max_pairs = fc.axonn_device_info()
 
     m = measure(args.workload, args, fc, dev, world, local, args.steps, tune_cache=args.tune_cache)
@@ -1273,6 +1277,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the timed CPU oracle sample")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-streamk", action="store_true",
+                    help="run (and tune) every GEMM without a stream-K tail")
+    ap.add_argument("--l2-budget", type=int, default=None, metavar="MB",
+                    help="L2 budget of the operand loads' evict-last lines (0: no L2 hints)")
     ap.add_argument("--no-tune", action="store_true",
                     help="skip the per-shape tuning before the warm-up (use default choices)")
     ap.add_argument("--no-graph", action="store_true",

@@ -416,6 +416,20 @@ axonn_status_t axonn_set_swap(int mode);
  * AXONN_ERR_INVALID_ARG for another value. */
 axonn_status_t axonn_set_pdl(int on);
 
+/* L2 priorities of the GEMM operand loads.  A rasterisation group walks its
+ * tile rows (or columns) across the whole product, so each later wave of
+ * the group reads the group's panel of that operand again, while the other
+ * operand's panels pass through once.  With a budget of `bytes` > 0 the
+ * kept operand's loads mark their lines evict-last (the fraction
+ * min(1, bytes / panel bytes) of them, panel = group x tile edge x
+ * reduction x 2; createpolicy and the .L2::cache_hint form of the tensor
+ * copies); the other operand's keep the default priority.  0 issues all
+ * loads with the default priority.  Default 64 MiB.  Results are unchanged
+ * either way.
+ * Process-wide, host-only; AXONN_ERR_INVALID_ARG for a negative value. */
+axonn_status_t axonn_set_l2_budget(int64_t bytes);
+int64_t axonn_l2_budget(void);
+
 /* 1 if the last call on this thread ran with exchanged operand roles. */
 int axonn_last_swap(void);
 

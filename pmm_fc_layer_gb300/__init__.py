@@ -37,7 +37,7 @@ EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_s
            "axonn_block_range", "axonn_fc_block_extents", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs",
            "axonn_set_streamk", "axonn_last_streamk_tiles", "axonn_set_swap", "axonn_last_swap",
-           "axonn_set_pdl",
+           "axonn_set_pdl", "axonn_set_l2_budget", "axonn_l2_budget",
            "axonn_device_info",
            "axonn_kernel_config_name", "axonn_last_kernel_config", "axonn_last_error",
            "axonn_version")
@@ -132,6 +132,10 @@ def load(path: str | None = None):
         lib.axonn_last_streamk_tiles.restype = ctypes.c_int
         lib.axonn_set_pdl.argtypes = [ctypes.c_int]
         lib.axonn_set_pdl.restype = ctypes.c_int
+        lib.axonn_set_l2_budget.argtypes = [ctypes.c_int64]
+        lib.axonn_set_l2_budget.restype = ctypes.c_int
+        lib.axonn_l2_budget.argtypes = []
+        lib.axonn_l2_budget.restype = ctypes.c_int64
         lib.axonn_set_swap.argtypes = [ctypes.c_int]
         lib.axonn_set_swap.restype = ctypes.c_int
         lib.axonn_last_swap.argtypes = []
@@ -359,6 +363,16 @@ def axonn_last_streamk_tiles() -> int:
 def axonn_set_pdl(on: int):
     """1 (default): GEMMs are programmatic dependent launches; 0: plain launches."""
     _check(load().axonn_set_pdl(int(on)))
+
+
+def axonn_set_l2_budget(nbytes: int):
+    """L2 bytes a rasterisation group's kept operand panel may hold as
+    evict-last lines (0: operand loads without L2 priorities)."""
+    _check(load().axonn_set_l2_budget(int(nbytes)))
+
+
+def axonn_l2_budget() -> int:
+    return int(load().axonn_l2_budget())
 
 
 def axonn_set_swap(mode: int):

@@ -98,6 +98,14 @@ struct ProblemDesc {
   // roles swapped, C^T = B^T . A^T): its tile element (i, j) is the
   // caller's output element (j, i), stored at C + j * ldc + i.
   int32_t out_t;
+  // L2 priorities of the operand loads: l2_keep = 1 keeps A's lines (a
+  // fraction l2_keep_frac of them evict-last), 2 keeps B's, 0 neither; the
+  // other operand loads at the default priority.  A rasterisation group
+  // walks its tile rows (or columns) across the whole product, so the
+  // group's panel of the one operand is read again by every later wave of
+  // the group while the other operand's panels pass through once.
+  int32_t l2_keep;
+  float l2_keep_frac;
 };
 
 template <int MAXP>
@@ -850,6 +858,9 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       for_each_work<kSplit>(P, blockIdx.x, gridDim.x, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
+        // L2 priorities of this tile's operand lines (see ProblemDesc)
+        const uint64_t pol_a = l2_policy(d.l2_keep == 1, d.l2_keep_frac);
+        const uint64_t pol_b = l2_policy(d.l2_keep == 2, d.l2_keep_frac);
         ChainPos cp = chain_start(P, d, k0);
         const CUtensorMap* ma = &P.tma[d.map0 + cp.g];
         const CUtensorMap* mb = &P.tmb[d.map0 + cp.g];
@@ -865,7 +876,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
           // 128 B; with a 3-D tensor map {64, R, MN/64} one box brings all of
           // them (fewer TMA operations per stage), else one box per chunk.
           if (d.a_3d) {
-            tma_load_3d(a_tile(stage), ma, fb, 0, r0, m0 / 64);
+            tma_load_3d(a_tile(stage), ma, fb, 0, r0, m0 / 64, pol_a);
           } else
 #pragma unroll
           for (int hh = 0; hh < MH; ++hh) {
@@ -873,19 +884,19 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
             if (d.a_mn) {
 #pragma unroll
               for (int h = 0; h < kBM / 64; ++h)
-                tma_load_2d(at + h * (BK * 128), ma, fb, m0 + kBM * hh + 64 * h, r0);
+                tma_load_2d(at + h * (BK * 128), ma, fb, m0 + kBM * hh + 64 * h, r0, pol_a);
             } else {
-              tma_load_2d(at, ma, fb, r0, m0 + kBM * hh);
+              tma_load_2d(at, ma, fb, r0, m0 + kBM * hh, pol_a);
             }
           }
           if (d.b_3d) {
-            tma_load_3d(b_tile(stage), mb, fb, 0, r0, n0 / 64);
+            tma_load_3d(b_tile(stage), mb, fb, 0, r0, n0 / 64, pol_b);
           } else if (d.b_mn) {
 #pragma unroll
             for (int h = 0; h < BN / 64; ++h)
-              tma_load_2d(b_tile(stage) + h * (BK * 128), mb, fb, n0 + 64 * h, r0);
+              tma_load_2d(b_tile(stage) + h * (BK * 128), mb, fb, n0 + 64 * h, r0, pol_b);
           } else {
-            tma_load_2d(b_tile(stage), mb, fb, r0, n0);
+            tma_load_2d(b_tile(stage), mb, fb, r0, n0, pol_b);
           }
           if (chain_next(P, d, cp)) {
             ma = &P.tma[d.map0 + cp.g];

@@ -120,6 +120,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
       for_each_work(P, pair, num_pairs, [&](int t, int k0, int k1, int) -> bool {
         const TileCoord tc = decode_tile(P, t);
         const ProblemDesc& d = P.prob[tc.p];
+        // L2 priorities of this tile's operand lines (see ProblemDesc)
+        const uint64_t pol_a = l2_policy(d.l2_keep == 1, d.l2_keep_frac);
+        const uint64_t pol_b = l2_policy(d.l2_keep == 2, d.l2_keep_frac);
         ChainPos cp = chain_start(P, d, k0);
         const CUtensorMap* ma = &P.tma[d.map0 + cp.g];
         const CUtensorMap* mb = &P.tmb[d.map0 + cp.g];
@@ -133,26 +136,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads<MH, MH =
           const uint32_t fb = mapa_shared(full_bar(stage), 0);
           const int r0 = cp.kl * kBK;
           if (d.a_3d) {
-            tma_load_3d_pair(a_tile(stage), ma, fb, 0, r0, m0 / 64);
+            tma_load_3d_pair(a_tile(stage), ma, fb, 0, r0, m0 / 64, pol_a);
           } else
 #pragma unroll
           for (int hh = 0; hh < MH; ++hh) {
             const uint32_t at = a_tile(stage) + hh * L::kAHalfBytes;
             if (d.a_mn) {
-              tma_load_2d_pair(at, ma, fb, m0 + 128 * hh, r0);
-              tma_load_2d_pair(at + kBK * 128, ma, fb, m0 + 128 * hh + 64, r0);
+              tma_load_2d_pair(at, ma, fb, m0 + 128 * hh, r0, pol_a);
+              tma_load_2d_pair(at + kBK * 128, ma, fb, m0 + 128 * hh + 64, r0, pol_a);
             } else {
-              tma_load_2d_pair(at, ma, fb, r0, m0 + 128 * hh);
+              tma_load_2d_pair(at, ma, fb, r0, m0 + 128 * hh, pol_a);
             }
           }
           if (d.b_3d) {
-            tma_load_3d_pair(b_tile(stage), mb, fb, 0, r0, n0 / 64);
+            tma_load_3d_pair(b_tile(stage), mb, fb, 0, r0, n0 / 64, pol_b);
           } else if (d.b_mn) {
 #pragma unroll
             for (int h = 0; h < BN / 128; ++h)
-              tma_load_2d_pair(b_tile(stage) + h * (kBK * 128), mb, fb, n0 + 64 * h, r0);
+              tma_load_2d_pair(b_tile(stage) + h * (kBK * 128), mb, fb, n0 + 64 * h, r0, pol_b);
           } else {
-            tma_load_2d_pair(b_tile(stage), mb, fb, r0, n0);
+            tma_load_2d_pair(b_tile(stage), mb, fb, r0, n0, pol_b);
           }
           if (chain_next(P, d, cp)) {
             ma = &P.tma[d.map0 + cp.g];

@@ -276,3 +276,18 @@ def test_zsharded_validation(fc):
     # missing workspace
     st = lib.axonn_fc_wgrad_zsharded(FAKE, FAKE, shards, 64, 64, 32, ctypes.byref(s), 0, 0, 0, 0)
     assert st == fc.ERR_WORKSPACE
+
+
+def test_l2_budget_setting(fc):
+    old = fc.axonn_l2_budget()
+    assert old == 64 << 20
+    try:
+        fc.axonn_set_l2_budget(0)
+        assert fc.axonn_l2_budget() == 0
+        fc.axonn_set_l2_budget(96 << 20)
+        assert fc.axonn_l2_budget() == 96 << 20
+        with pytest.raises(fc.AxonnError):
+            fc.axonn_set_l2_budget(-1)
+        assert fc.axonn_l2_budget() == 96 << 20
+    finally:
+        fc.axonn_set_l2_budget(old)
