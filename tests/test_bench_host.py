@@ -202,16 +202,19 @@ def test_traffic_reported_only_for_captured_choices(monkeypatch):
     """roofline.traffic is the captured DRAM bytes of the step's GEMMs when
     every GEMM ran a choice in the committed table (and the kernel sources
     are the capture's); any other choice, source or workload gives null."""
-    keys = list(bench.TRAFFIC["bytes"])
-    assert len(keys) == 12
+    # one captured choice per GEMM of the step (the table may hold several)
+    first = {}
+    for (gemm, choice), b in bench.TRAFFIC["bytes"].items():
+        first.setdefault(gemm, (choice, b))
+    assert len(first) == 12
     per = []
-    for (gemm, choice) in keys:
+    for gemm, (choice, _) in first.items():
         layer, op = gemm.split(":")
         config, group, sk = choice.split("/")
         per.append({"layer": layer, "op": op, "config": config, "group_m": int(group),
                     "streamk_tiles": int(sk)})
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: bench.TRAFFIC["kernel_sources"])
-    want = sum(bench.TRAFFIC["bytes"].values()) / 12
+    want = sum(b for _, b in first.values()) / 12
     assert bench.traffic_per_launch("gpt_h6144_t8192", per, None) == pytest.approx(want)
     assert bench.traffic_per_launch("gpt_h6144_t8192", per, ("up", "fwd")) is None
     assert bench.traffic_per_launch("large_h16384_t4096", per, None) is None
