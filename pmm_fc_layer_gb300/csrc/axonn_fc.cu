@@ -348,10 +348,14 @@ constexpr KernelConfig kConfigs[] = {
     {"1cta_128x192", 128, 192, 64, false, 128},
     {"1cta_256x192", 256, 192, 64, false, 128},
     {"pair_512x256", 512, 256, 64, true, 256},
+    {"1cta_128x64", 128, 64, 64, false, 128},
 };
 // Throughput of each configuration relative to 1cta_128x256 on full waves
-// (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144).
-constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12, 1.2};
+// (measured on GB300 over the 12 GEMMs of a GPT block, H = 6144; the
+// 128x64 tile on an 8192 x 6144 x 6144 forward product).  The 128x64 tile
+// reads 1.5x the operand bytes per FLOP of 128x128: it is for products with
+// too few larger tiles to fill the GPU.
+constexpr double kConfigSpeed[] = {0.68, 1.0, 0.92, 1.06, 0.92, 1.12, 1.2, 0.36};
 constexpr int kNumConfigs = static_cast<int>(sizeof(kConfigs) / sizeof(kConfigs[0]));
 static_assert(kNumConfigs == axonn::kKernelConfigs, "configuration table and kernel instantiations");
 std::atomic<int> g_forced_config{-1};

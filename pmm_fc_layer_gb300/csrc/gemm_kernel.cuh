@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
   constexpr uint32_t kTmemUsed = kAccBufs * kAccCols;
   constexpr uint32_t kTmemCols = kTmemUsed <= 128 ? 128 : (kTmemUsed <= 256 ? 256 : 512);
   constexpr int kTileM = MH * kBM;
-  static_assert(BN % 64 == 0 && BN >= 128 && BN <= 256, "UMMA N: 128, 192 or 256");
+  static_assert(BN % 64 == 0 && BN >= 64 && BN <= 256, "UMMA N: 64, 128, 192 or 256");
   static_assert(kTmemUsed <= 512, "TMEM columns");
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];

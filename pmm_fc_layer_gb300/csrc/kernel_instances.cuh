@@ -96,12 +96,14 @@ template <int MAXP>
 using C5 = Single<192, 64, 4, MAXP, 2>;
 template <int MAXP>
 using C6 = Pair<256, kPair2Stages, MAXP, 2>;
+template <int MAXP>
+using C7 = Single<64, 64, 8, MAXP, 1>;  // 128 x 64 tiles, 24 KB stages
 
 template <int MAXP>
 cudaError_t kernels_init(bool* split_ok) {
   const cudaError_t es[] = {C0<MAXP>::init(), C1<MAXP>::init(), C2<MAXP>::init(),
                             C3<MAXP>::init(), C4<MAXP>::init(), C5<MAXP>::init(),
-                            C6<MAXP>::init(), C6<MAXP>::check_regs(split_ok)};
+                            C6<MAXP>::init(), C7<MAXP>::init(), C6<MAXP>::check_regs(split_ok)};
   for (cudaError_t e : es)
     if (e != cudaSuccess) return e;
   return cudaSuccess;
@@ -118,6 +120,7 @@ cudaError_t kernels_launch(int config, const GemmParams<MAXP>& P, int units, boo
     case 4: return C4<MAXP>::launch(P, units, pdl, s);
     case 5: return C5<MAXP>::launch(P, units, pdl, s);
     case 6: return C6<MAXP>::launch(P, units, pdl, s);
+    case 7: return C7<MAXP>::launch(P, units, pdl, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -12,8 +12,9 @@ namespace axonn {
 
 // Kernel configurations by index (the host's configuration table uses the
 // same order): 0 1cta_128x128, 1 1cta_128x256, 2 pair_256x256,
-// 3 1cta_256x256, 4 1cta_128x192, 5 1cta_256x192, 6 pair_512x256.
-constexpr int kKernelConfigs = 7;
+// 3 1cta_256x256, 4 1cta_128x192, 5 1cta_256x192, 6 pair_512x256,
+// 7 1cta_128x64.
+constexpr int kKernelConfigs = 8;
 
 // Sets the dynamic shared memory limit of every instantiation for this
 // MAXP on the current device, and checks that each 12-warp kernel was built

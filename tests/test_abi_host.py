@@ -44,10 +44,10 @@ def test_version(fc):
 
 def test_kernel_config_table(fc):
     n = fc.axonn_num_kernel_configs()
-    assert n == 7
+    assert n == 8
     assert [fc.axonn_kernel_config_name(i) for i in range(n)] == \
         ["1cta_128x128", "1cta_128x256", "pair_256x256", "1cta_256x256", "1cta_128x192",
-         "1cta_256x192", "pair_512x256"]
+         "1cta_256x192", "pair_512x256", "1cta_128x64"]
     with pytest.raises(fc.AxonnError):
         fc.axonn_set_kernel_config(n)
     fc.axonn_set_kernel_config(2)

@@ -15,7 +15,7 @@ from fc_cases import (assert_within_bound, host_bits, host_f64, make_operand, op
 pytestmark = pytest.mark.gpu
 
 LAYOUTS = [(False, False), (False, True), (True, False), (True, True)]
-CONFIGS = [0, 1, 2, 3, 4, 5, 6]   # every kernel configuration of the library
+CONFIGS = [0, 1, 2, 3, 4, 5, 6, 7]   # every kernel configuration of the library
 
 
 @pytest.fixture

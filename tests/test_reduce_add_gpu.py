@@ -21,7 +21,7 @@ from fc_cases import (assert_within_bound, host_f64, make_operand, operand_names
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [0, 1, 2, 3, 4, 5, 6]
+CONFIGS = [0, 1, 2, 3, 4, 5, 6, 7]
 GRIDS = [(2, 2, 2), (1, 4, 4), (3, 1, 2), (2, 3, 1)]
 
 

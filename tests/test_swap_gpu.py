@@ -24,7 +24,7 @@ def swapped(cuda_lib):
     cuda_lib.axonn_set_streamk(-1)
 
 
-@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4, 5, 6, 7])
 @pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
 @pytest.mark.parametrize("p_t,q_t", LAYOUTS)
 @pytest.mark.parametrize("T,K,N", [(300, 200, 520), (129, 1000, 257), (520, 136, 776)])
