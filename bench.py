@@ -382,7 +382,13 @@ def cpu_baseline(data, glist, gpu_rows=None, rows=CPU_STRIPE_ROWS):
     return out
 
 
-def config_block(wl, name, world, output=None):
+STEP_TIMING = {
+    1: "one step per graph replay, CUDA events around each step",
+    0: "the K timed steps back to back in one CUDA graph, CUDA events around the "
+       "span (steps of a few microseconds with L2-resident operands)"}
+
+
+def config_block(wl, name, world, output=None, reps=1):
     cfg = {"workload": f"{name}: {wl['desc']}"}
     if output:
         cfg["output"] = output
@@ -395,6 +401,7 @@ def config_block(wl, name, world, output=None):
                  else "operands exceed the 129 MB L2; no flush" if all(big)
                  else "operands L2-resident (warm), by design of this workload" if not any(big)
                  else "mixed: the larger shapes exceed L2, the smallest can stay resident")
+    cfg["step_timing"] = STEP_TIMING[1 if reps == 1 else 0]
     return cfg
 
 
@@ -428,7 +435,8 @@ def run_reference(args):
             "ms_per_step": 1e3 * tot_s / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
             "config": {**config_block(wl, args.workload, 1),
-                       "parallelism": "host cores (OpenMP)"},
+                       "parallelism": "host cores (OpenMP)",
+                       "step_timing": "host wall clock around each step's oracle products"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": ("each step: one of the " + str(n) + " GEMMs, whole"
                                         if rows != CPU_STRIPE_ROWS else
@@ -573,18 +581,30 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    # Steps of a few microseconds (the single layer) with L2-resident
+    # operands: the K timed steps run back to back from one graph and are
+    # timed as one span, as consecutive layers would run in a model step;
+    # one graph launch per step would put its launch latency (several us,
+    # larger than such a GEMM) into every step.  Flushed and large steps are
+    # timed one step per replay.
+    batched = (not args.no_graph) and flush is None and \
+        sum(g["flops"] for g in plan) < 2e10
+    reps = steps if batched else 1
     if not args.no_graph:
-        # One step, and each GEMM on its own, captured as CUDA graphs: the
-        # timed loops replay them, so host-side launch overhead (which
-        # dominates the small products) is not part of the device timeline.
+        # One step (or K), and each GEMM on its own (or K times), captured as
+        # CUDA graphs: the timed loops replay them, so host-side launch
+        # overhead (which dominates the small products) is not part of the
+        # device timeline.
         step_graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(step_graph, stream=stream):
-            step()
+            for _ in range(reps):
+                step()
         gemm_graphs = []
         for gi in range(len(plan)):
             gg = torch.cuda.CUDAGraph()
             with torch.cuda.graph(gg, stream=stream):
-                call_gemm(gi)
+                for _ in range(reps):
+                    call_gemm(gi)
             gemm_graphs.append(gg)
         with torch.cuda.stream(stream):
             step_graph.replay()
@@ -593,7 +613,7 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
         torch.cuda.synchronize()
     with ClockSampler(gpu_index) as clocks:
         with torch.cuda.stream(stream):
-            for s in range(steps):
+            for s in range(steps // reps):
                 step_ev[s][0].record(stream)
                 if args.no_graph:
                     step(ev[s])
@@ -604,7 +624,7 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
                     flush.fill_(1)        # outside the step's events
             if not args.no_graph:
                 for gi, gg in enumerate(gemm_graphs):
-                    for s in range(steps):
+                    for s in range(steps // reps):
                         ev[s][gi][0].record(stream)
                         gg.replay()
                         ev[s][gi][1].record(stream)
@@ -614,7 +634,7 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
     if world > 1:
         dist.barrier()
     fc.axonn_sync_status(stream)
-    elapsed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_ev), dev)
+    elapsed_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in step_ev[:steps // reps]), dev)
     # the counter-zeroing kernel before a stream-K call (a split reduction
     # is one launch)
     sk_zeroing = sum(1 for t in sk_tiles if t > 0)
@@ -627,7 +647,10 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
     gemm_ms_total = 0.0
     flops_per_step = sum(g["flops"] for g in plan)
     for gi, g in enumerate(plan):
-        ms = [ev[s][gi][0].elapsed_time(ev[s][gi][1]) for s in range(steps)]
+        if reps > 1:   # one span of K back-to-back calls: K equal shares
+            ms = [ev[0][gi][0].elapsed_time(ev[0][gi][1]) / reps] * steps
+        else:
+            ms = [ev[s][gi][0].elapsed_time(ev[s][gi][1]) for s in range(steps)]
         gemm_ms_total += sum(ms)
         med = statistics.median(ms)
         # the pages' own style: the mean of the last 8 of 10 runs
@@ -731,7 +754,8 @@ def workload_summary(m, fc, check=True):
                         "two launches, fp32 partials" if m.flags & fc.VGRID_PARTIALS else
                         "order-free reduction adds" if m.flags & fc.REDUCE_ADD else
                         "chained in one accumulator"),
-           "l2": config_block(m.wl, "", 1)["l2"]}
+           "l2": config_block(m.wl, "", 1)["l2"],
+           "step_timing": STEP_TIMING[1 if m.reps == 1 else 0]}
     if len(m.per) <= 12:
         out["per_gemm_tflops"] = {f"{p['layer']}:{p['op']}": p["tflops"] for p in m.per}
     else:
@@ -1053,7 +1077,7 @@ def run_ours(args):
             "data": DATA if not wl.get("scale") else
             DATA.replace("activations/grads N(0,1), weights N(0,0.02)", "all operands N(0,1)*0.05"),
             "config": config_block(
-                wl, args.workload, world,
+                wl, args.workload, world, reps=m.reps,
                 output=None if not args.accum_f32 else
                 "fp32, every step adds its product into it (C += A.B)" + (
                     "; grid partials added by atomics in one launch (order-free)"
