@@ -271,8 +271,9 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
  * at least 128 deep), the 128x256 and 256-row configurations otherwise,
  * and the two best of them again with the
  * operand roles exchanged (see axonn_set_swap) -- and times each (through a captured
- * CUDA graph where the stream allows it) relative to the default choice run
- * just before and after it, so clock drift under the power cap cancels.  The
+ * CUDA graph of 3 calls, 20 for products under 2e10 FLOP, where the stream
+ * allows it) relative to the default choice run just before and after it,
+ * so clock drift under the power cap cancels.  The
  * call synchronises `stream`.  It
  * records the fastest for later calls with the same op, sizes, grid, block
  * and flags on a GPU with the same SM count.  Arguments are those of the

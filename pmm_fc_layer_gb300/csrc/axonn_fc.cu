@@ -639,12 +639,16 @@ int choose_config(const std::vector<Block>& blocks, const DeviceState& dev) {
   return best;
 }
 
-// Split of the reduction range is offered for products that leave most
-// SMs idle: fewer 128x256 tiles than two waves, and a reduction of at least
-// 512.  Slices are whole 64-deep stages.
-bool split_eligible(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
+// Products that leave most SMs idle: fewer 128x256 tiles than two waves.
+// The split of the reduction range is offered to those with a reduction of
+// at least 512 as well.  Slices are whole 64-deep stages.
+bool underfilled(int64_t M, int64_t N, const DeviceState& dev) {
   const int64_t tiles = ((M + 127) / 128) * ((N + 255) / 256);
-  return tiles < 2 * dev.sms && R >= 4 * kSplitMinR;
+  return tiles < 2 * dev.sms;
+}
+
+bool split_eligible(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
+  return underfilled(M, N, dev) && R >= 4 * kSplitMinR;
 }
 
 // The reduction split runs on configuration 0 (128 x 128 tiles) only: the
@@ -1214,13 +1218,17 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   // Candidates.  Products that fill the GPU many times over only try the
   // configurations that ever win there (128x256, 256-row and 512-row tiles);
   // under-filled products try everything, reduction splits included.
-  const bool small = split_eligible(rows.len(), cols.len(), red.len(), *dev);
+  // Products that leave SMs idle (fewer 128x256 tiles than two waves) try
+  // every configuration; those with a long enough reduction also try the
+  // reduction split.
+  const bool small = underfilled(rows.len(), cols.len(), *dev);
+  const bool splittable = split_eligible(rows.len(), cols.len(), red.len(), *dev);
   std::vector<TuneChoice> cands;
   for (int c = 0; c < kNumConfigs; ++c) {
     if (!small && !(c == 1 || c == 3 || c == 5 || c == 6)) continue;
     for (int gm : {8, 16, -8, -16}) cands.push_back(TuneChoice{c, 1, gm});
   }
-  if (!(flags & AXONN_VGRID) && small)
+  if (!(flags & AXONN_VGRID) && splittable)
     for (int sp = 2; sp <= kMaxSplit; sp *= 2)
       if (red.len() / sp >= kSplitMinR)
         for (int gm : {16, -16}) cands.push_back(TuneChoice{0, sp, gm});
@@ -1237,7 +1245,13 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   // is timed, so small products are measured on the device timeline rather
   // than through host launch overhead.  Streams that cannot be captured
   // (the legacy default stream) are timed with eager launches instead.
-  constexpr int kReps = 3, kRounds = 2;
+  constexpr int kRounds = 2;
+  // Calls per timed graph: 3, or 20 for products of a few microseconds,
+  // whose differences between candidates would otherwise be within the
+  // jitter of one graph launch.
+  const double flops = 2.0 * static_cast<double>(rows.len()) * static_cast<double>(cols.len()) *
+                       static_cast<double>(red.len());
+  const int kReps = flops < 2e10 ? 20 : 3;
   std::vector<double> cand_us(cands.size(), -1.0);
   auto time_candidate = [&](const TuneChoice& c, double* us) -> bool {
     cudaGraph_t graph = nullptr;
