@@ -1134,8 +1134,10 @@ def run_ours(args):
             "gpu_launches": launches,
             "tuned": not args.no_tune,
             "timing": ("eager ABI calls, CUDA events around each" if args.no_graph else
-                       "CUDA-graph replay of one step per timed step; per-GEMM table from "
-                       "replays of each GEMM's own graph"),
+                       ("CUDA-graph replay of one step per timed step; per-GEMM table from "
+                        "replays of each GEMM's own graph" if m.reps == 1 else
+                        "the K timed steps back to back in one CUDA-graph replay; per-GEMM "
+                        "table from one replay of K back-to-back calls of each GEMM")),
             "device": {"sms": sms, "resident_cta_pairs": max_pairs,
                        "kernel_configs": sorted({p["config"] for p in per})},
             "clocks": clk,
