@@ -182,3 +182,28 @@ def test_split_only_on_the_128x128_configuration(cuda_lib, force_split):
         assert np.array_equal(host_bits(out), want)
     finally:
         fc.axonn_set_kernel_config(-1)
+
+
+@pytest.mark.parametrize("split", [2, 8])
+def test_split_bounded_wait_timeout_reports_and_recovers(cuda_lib, force_split, split):
+    """A producer that withholds its loads: every CTA of every cluster times
+    out in its own bounded waits (no piece ever stages its rows), all reach
+    the final cluster barrier, the library reports AXONN_ERR_TIMEOUT and the
+    context stays usable for a correct split product."""
+    fc = cuda_lib
+    T, K, N = 256, 1024, 512
+    X = make_operand("X", T, K, N, False, seed=709, kind="int")
+    W = make_operand("W", T, K, N, False, seed=709, kind="int")
+    force_split("fwd", T, K, N, 0, split)
+    try:
+        fc.axonn_set_wait_timeout_ns(20_000_000)
+        fc.axonn_debug_set_inject(1)
+        with pytest.raises(fc.AxonnError) as ei:
+            run_gpu(fc, "fwd", X, W, False, False, T, K, N, workspace=False)
+        assert ei.value.status == fc.ERR_TIMEOUT
+    finally:
+        fc.axonn_debug_set_inject(0)
+        fc.axonn_set_wait_timeout_ns(4_000_000_000)
+    out = run_gpu(fc, "fwd", X, W, False, False, T, K, N, workspace=False)
+    assert fc.axonn_last_choice()[1] == split
+    assert np.array_equal(host_bits(out), oracle.bf16_rne(oracle.fc_fwd(X, W)[0]))
