@@ -508,6 +508,47 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
     }
     return;
   }
+  if (d.out_t && d.out_mode == kOutBF16 && d.red_count == 0 && n0 + BN <= d.N &&
+      ((reinterpret_cast<uintptr_t>(d.C) & 3) | (d.ldc & 1)) == 0) {
+    // Transposed bf16 output (exchanged operand roles): as above, the row is
+    // packed in registers and TMEM released before any store, so the next
+    // tile's MMAs do not wait for the stores.  Accumulator column j is output
+    // row n0 + j.  Lanes 2i and 2i+1 (adjacent accumulator rows) swap their
+    // packed column pairs, after which the even lane holds column 2w of both
+    // rows and the odd lane column 2w+1: one 32-bit store each per pair of
+    // columns, the warp covering 64 consecutive bytes of two output rows.
+    uint32_t pk[BN / 2];
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(t_row + c * 32, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 16; ++j) pk[16 * c + j] = cvt_bf16x2_ordered(r[2 * j], r[2 * j + 1]);
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (arrive) {
+      if (remote) mbar_arrive_cluster(tempty);
+      else mbar_arrive(tempty);
+    }
+    const int odd = row & 1;
+    const int rb = row - odd;  // first row of the lane pair
+    // even lane: (own low half, partner's low half); odd: (partner's high, own high)
+    const uint32_t sel = odd ? 0x3276u : 0x5410u;
+    const int64_t ld = d.ldc;
+    unsigned short* out = reinterpret_cast<unsigned short*>(d.C) + (n0 + odd) * ld + rb;
+    const bool both = rb + 1 < d.M, first = rb < d.M;
+#pragma unroll
+    for (int w = 0; w < BN / 2; ++w) {
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, pk[w], 1);
+      const uint32_t v = __byte_perm(pk[w], other, sel);
+      if (both) *reinterpret_cast<uint32_t*>(out) = v;
+      else if (first) out[0] = static_cast<unsigned short>(v & 0xFFFFu);
+      out += 2 * ld;
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     const int col0 = n0 + c * 32;

@@ -215,7 +215,7 @@ def test_reduce_add_tune_then_call(cuda_lib):
     scratch = torch.zeros((T, N), dtype=torch.float32, device="cuda")
     try:
         cfg, _, _, us = fc.axonn_fc_tune("fwd", Xd, Wd, scratch, shape, flags, None)
-        assert 0 <= cfg < 7 and us > 0
+        assert 0 <= cfg < fc.axonn_num_kernel_configs() and us > 0
         out = _int_base(T, N)
         want = host_f64(out) + oracle.fc_fwd(X, W)[0]
         fc.call("fwd", Xd, Wd, out, shape, flags, None)
