@@ -86,45 +86,46 @@ WORKLOADS = {
         batch=None, seq=None, seed=1005, scale=0.05, device_inputs=True),
 }
 DEFAULT_WORKLOAD = "gpt_h6144_t8192"
+# Tuning tables shipped for workloads (<workload>.jsonl, the library's tune
+# cache format): choices from a tuning run on a GB300, keyed by SM count.
+TUNED_DIR = os.path.join(ROOT, "pmm_fc_layer_gb300", "tuned")
 
 # DRAM traffic of the GEMM kernel from ncu captures of the default workload:
 # dram__bytes_read.sum + dram__bytes_write.sum of each GEMM ("layer:op") in
-# each tuned choice ("config/group/stream-K tiles") captured (summary and command
+# each tuned choice ("config/group/stream-K tiles/swap") captured (summary and command
 # in profiles/).  Reported only while the kernel sources hash to the value
 # the capture was taken with and every GEMM's choice of this run is in it.
 TRAFFIC = {
-    "workload": "gpt_h6144_t8192", "kernel_sources": "a15a19947cbbb13c",
+    "workload": "gpt_h6144_t8192", "kernel_sources": "c003daaa9b654152",
     "bytes": {
-        ("qkv:fwd", "pair_512x256/16/0"): 2125401088,
-        ("qkv:fwd", "pair_512x256/16/88"): 2420742016,
-        ("qkv:dgrad", "1cta_256x192/-8/0"): 1865000192,
-        ("qkv:dgrad", "1cta_256x192/8/0"): 1756556032,
-        ("qkv:wgrad", "pair_512x256/-8/0"): 1826479104,
-        ("qkv:wgrad", "pair_512x256/16/0"): 1760352896,
-        ("out:fwd", "1cta_256x192/-8/0"): 608231424,
-        ("out:fwd", "1cta_256x192/8/0"): 549133056,
-        ("out:dgrad", "1cta_256x192/-16/0"): 470689536,
-        ("out:dgrad", "1cta_256x192/-8/0"): 591498240,
-        ("out:dgrad", "1cta_256x192/16/0"): 583946752,
-        ("out:wgrad", "pair_512x256/-16/0"): 551914240,
-        ("out:wgrad", "pair_512x256/16/0"): 569865216,
-        ("out:wgrad", "pair_512x256/8/0"): 530995456,
-        ("up:fwd", "1cta_256x192/8/0"): 1745313792,
-        ("up:fwd", "pair_512x256/16/0"): 3010326272,
-        ("up:fwd", "pair_512x256/16/92"): 3383282944,
-        ("up:dgrad", "1cta_256x192/-8/0"): 2501632512,
-        ("up:dgrad", "1cta_256x192/16/0"): 2860091392,
-        ("up:dgrad", "1cta_256x192/8/0"): 2368038912,
-        ("up:wgrad", "pair_512x256/-8/0"): 2634232320,
-        ("up:wgrad", "pair_512x256/16/88"): 2767050496,
-        ("up:wgrad", "pair_512x256/8/88"): 2396079872,
-        ("down:fwd", "1cta_256x192/8/0"): 2380299520,
-        ("down:fwd", "pair_512x256/8/80"): 3944800512,
-        ("down:dgrad", "1cta_256x192/-8/0"): 2383250688,
-        ("down:dgrad", "1cta_256x192/8/0"): 1745791488,
-        ("down:dgrad", "pair_512x256/16/0"): 3066944256,
-        ("down:wgrad", "pair_512x256/-16/88"): 2782171136,
-        ("down:wgrad", "pair_512x256/16/88"): 3513981056,
+        ("qkv:fwd", "pair_512x256/-8/88/1"): 1774615296,
+        ("qkv:fwd", "pair_512x256/16/88/0"): 2422512896,
+        ("qkv:fwd", "pair_512x256/8/88/1"): 1855110656,
+        ("qkv:dgrad", "1cta_256x192/-8/0/0"): 1866920960,
+        ("qkv:dgrad", "1cta_256x192/-8/0/1"): 2038127360,
+        ("qkv:wgrad", "pair_512x256/-16/104/0"): 2357205760,
+        ("qkv:wgrad", "pair_512x256/16/0/0"): 1759607040,
+        ("qkv:wgrad", "pair_512x256/16/104/0"): 2414695168,
+        ("out:fwd", "1cta_256x192/-8/0/0"): 612128640,
+        ("out:fwd", "1cta_256x192/8/0/0"): 558925056,
+        ("out:dgrad", "1cta_256x192/-16/0/0"): 499828992,
+        ("out:dgrad", "1cta_256x192/-8/0/0"): 599616256,
+        ("out:dgrad", "1cta_256x192/-8/0/1"): 664706048,
+        ("out:wgrad", "pair_512x256/-8/0/0"): 575164160,
+        ("out:wgrad", "pair_512x256/16/0/0"): 571150080,
+        ("out:wgrad", "pair_512x256/8/0/1"): 532295936,
+        ("up:fwd", "1cta_256x192/8/0/0"): 1763546624,
+        ("up:fwd", "pair_512x256/16/92/0"): 3138863744,
+        ("up:dgrad", "1cta_256x192/-8/0/0"): 2467148544,
+        ("up:dgrad", "1cta_256x192/8/0/0"): 2321399552,
+        ("up:wgrad", "pair_512x256/16/88/0"): 2816802901,
+        ("down:fwd", "1cta_256x192/-8/0/0"): 2459280128,
+        ("down:fwd", "1cta_256x192/8/0/0"): 2319979520,
+        ("down:dgrad", "1cta_256x192/16/0/0"): 1700046592,
+        ("down:dgrad", "1cta_256x192/8/0/0"): 1760565760,
+        ("down:dgrad", "pair_512x256/-8/0/0"): 2352835840,
+        ("down:wgrad", "pair_512x256/-16/88/0"): 2600390144,
+        ("down:wgrad", "pair_512x256/16/88/0"): 3411776896,
     }}
 
 
@@ -137,7 +138,8 @@ def traffic_per_launch(workload, per, only):
         return None
     tot = 0.0
     for p in per:
-        key = (f"{p['layer']}:{p['op']}", f"{p['config']}/{p['group_m']}/{p['streamk_tiles']}")
+        key = (f"{p['layer']}:{p['op']}",
+               f"{p['config']}/{p['group_m']}/{p['streamk_tiles']}/{int(p.get('swap', 0))}")
         if key not in TRAFFIC["bytes"]:
             return None
         tot += TRAFFIC["bytes"][key]
@@ -560,13 +562,24 @@ def measure(wl_name, args, fc, dev, world, local, steps, tune_cache=None, on_dev
 
     # Per-shape tuning (outside every timed region): each GEMM's candidate
     # configurations are timed once and the fastest is kept by the library.
+    # A workload with a tuning table shipped in the package loads it first
+    # (unless --retune) and tunes only the GEMMs it holds no entry for.
+    tuning = "none: default choices"
     if tune_cache and os.path.exists(tune_cache):
         fc.axonn_tune_cache_load(tune_cache)
+        tuning = f"loaded from {tune_cache}"
     elif not args.no_tune:
+        shipped = os.path.join(TUNED_DIR, f"{wl_name}.jsonl")
+        if not args.retune and os.path.exists(shipped):
+            fc.axonn_tune_cache_load(shipped)
+        todo = [g for g in plan if not fc.axonn_tune_lookup(g["op"], g["shape"], flags)]
         with torch.cuda.stream(stream):
-            for g in plan:
+            for g in todo:
                 fc.axonn_fc_tune(g["op"], g["P"], g["Q"], g["C"], g["shape"], flags, ws,
                                  stream=stream)
+        tuning = ("tuned at run time" if len(todo) == len(plan) else
+                  f"shipped table {os.path.relpath(shipped, ROOT)}" if not todo else
+                  f"shipped table, {len(todo)} of {len(plan)} GEMMs tuned at run time")
         if tune_cache:
             fc.axonn_tune_cache_save(tune_cache)
     with torch.cuda.stream(stream):
@@ -1133,6 +1146,7 @@ def run_ours(args):
                     if e2e_steps else None),
             "gpu_launches": launches,
             "tuned": not args.no_tune,
+            "tuning": m.tuning,
             "timing": ("eager ABI calls, CUDA events around each" if args.no_graph else
                        ("CUDA-graph replay of one step per timed step; per-GEMM table from "
                         "replays of each GEMM's own graph" if m.reps == 1 else
@@ -1327,6 +1341,9 @@ def main():
                     help="L2 budget of the operand loads' evict-last lines (0: no L2 hints)")
     ap.add_argument("--no-tune", action="store_true",
                     help="skip the per-shape tuning before the warm-up (use default choices)")
+    ap.add_argument("--retune", action="store_true",
+                    help="tune every GEMM at run time, ignoring a tuning table shipped for "
+                         "the workload")
     ap.add_argument("--no-graph", action="store_true",
                     help="time eager ABI calls instead of CUDA-graph replays")
     ap.add_argument("--tune-cache", default=None, metavar="PATH",

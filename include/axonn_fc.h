@@ -307,6 +307,14 @@ axonn_status_t axonn_tune_cache_load(const char* path);
 void axonn_tune_cache_clear(void);
 int axonn_tune_cache_size(void);
 
+/* Whether the tuning table holds an entry that a call of op `op` (an
+ * axonn_op_t) with this shape and these flags would run on the current
+ * device (same SM count): *found = 1, else 0 (the call runs the default
+ * choice).  AXONN_ERR_INVALID_ARG for a bad shape or flag or a NULL
+ * `found`; AXONN_ERR_CUDA without a usable device.  Launches nothing. */
+axonn_status_t axonn_tune_lookup(int op, const axonn_fc_shape_t* shape, uint32_t flags,
+                                 int* found);
+
 /* How the last call on this thread ran: kernel configuration, reduction
  * split and rasterisation group. */
 void axonn_last_choice(int* config, int* split, int* group_m);

@@ -33,6 +33,7 @@ EXPORTS = ("axonn_fc_fwd", "axonn_fc_dgrad", "axonn_fc_wgrad", "axonn_fc_vgrid_s
            "axonn_shards_gather", "axonn_fc_wgrad_zsharded", "axonn_goldfish_ce",
            "axonn_fc_workspace_size", "axonn_fc_tune", "axonn_tune_cache_save",
            "axonn_tune_cache_load", "axonn_tune_cache_clear", "axonn_tune_cache_size",
+           "axonn_tune_lookup",
            "axonn_last_choice",
            "axonn_block_range", "axonn_fc_block_extents", "axonn_sync_status", "axonn_set_wait_timeout_ns",
            "axonn_debug_set_inject", "axonn_set_kernel_config", "axonn_num_kernel_configs",
@@ -107,6 +108,9 @@ def load(path: str | None = None):
         lib.axonn_tune_cache_load.restype = ctypes.c_int
         lib.axonn_tune_cache_clear.restype = None
         lib.axonn_tune_cache_size.restype = ctypes.c_int
+        lib.axonn_tune_lookup.argtypes = [ctypes.c_int, ctypes.POINTER(Shape), u32,
+                                          ctypes.POINTER(ctypes.c_int)]
+        lib.axonn_tune_lookup.restype = ctypes.c_int
         lib.axonn_last_choice.argtypes = [ctypes.POINTER(ctypes.c_int)] * 3
         lib.axonn_last_choice.restype = None
         lib.axonn_fc_workspace_size.argtypes = [ctypes.c_int, ctypes.POINTER(Shape), u32,
@@ -304,6 +308,15 @@ def axonn_last_choice():
     c, s, g = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
     load().axonn_last_choice(ctypes.byref(c), ctypes.byref(s), ctypes.byref(g))
     return c.value, s.value, g.value
+
+
+def axonn_tune_lookup(op, shape: Shape, flags: int = 0) -> bool:
+    """True when the tuning table holds an entry for this call on the
+    current device."""
+    op = OPS.get(op, op)
+    found = ctypes.c_int(0)
+    _check(load().axonn_tune_lookup(int(op), ctypes.byref(shape), flags, ctypes.byref(found)))
+    return bool(found.value)
 
 
 def axonn_fc_workspace_size(op, shape: Shape, flags: int = 0) -> int:

@@ -1499,6 +1499,20 @@ int axonn_tune_cache_size(void) {
   return static_cast<int>(g_tune.size());
 }
 
+axonn_status_t axonn_tune_lookup(int op, const axonn_fc_shape_t* shape, uint32_t flags,
+                                 int* found) {
+  if (!found) return fail(AXONN_ERR_INVALID_ARG, "found is NULL");
+  *found = 0;
+  axonn_status_t st = check_shape(op, shape, flags);
+  if (st != AXONN_OK) return st;
+  DeviceState* dev = nullptr;
+  st = device_state(&dev);
+  if (st != AXONN_OK) return st;
+  std::lock_guard<std::mutex> lk(g_tune_mu);
+  *found = g_tune.count(tune_key(op, *shape, flags, dev->sms)) ? 1 : 0;
+  return ok();
+}
+
 void axonn_last_choice(int* config, int* split, int* group_m) {
   if (config) *config = t_last_choice.config;
   if (split) *split = t_last_choice.split;

@@ -181,6 +181,43 @@ def test_binding_refuses_missing_library(tmp_path):
         m._lib = saved
 
 
+def test_tune_lookup_checks_arguments_before_the_device(fc):
+    """A bad shape is rejected as an argument error; a good one needs the
+    device's SM count, so on a host without a GPU the lookup reports a CUDA
+    error rather than an answer."""
+    import torch
+    with pytest.raises(fc.AxonnError) as ei:
+        fc.axonn_tune_lookup("fwd", fc.Shape(-1, 8, 8))
+    assert ei.value.status == fc.ERR_INVALID_ARG
+    if torch.cuda.is_available():
+        pytest.skip("a device is present: the lookup answers")
+    with pytest.raises(fc.AxonnError) as ei:
+        fc.axonn_tune_lookup("fwd", fc.Shape(8, 8, 8))
+    assert ei.value.status == fc.ERR_CUDA
+
+
+def test_shipped_tuning_tables_cover_their_workloads(fc):
+    """Every table shipped in the package loads, and holds exactly one entry
+    per GEMM of its workload as the benchmark calls them (single GPU, whole
+    operands, default flags) on a 152-SM GB300."""
+    import glob
+    import json
+    import bench
+    tables = sorted(glob.glob(os.path.join(ROOT, "pmm_fc_layer_gb300", "tuned", "*.jsonl")))
+    assert tables
+    for path in tables:
+        wl = bench.WORKLOADS[os.path.basename(path)[:-len(".jsonl")]]
+        keys = [json.loads(l)["key"] for l in open(path).read().splitlines() if l.strip()]
+        grid = "x".join(str(g) for g in wl.get("grid", (1, 1, 1)))
+        want = {f"op{fc.OPS[op]}_T{T}_K{K}_N{N}_g{grid}_at0.0.0_f0_sm152"
+                for _, T, K, N in wl["layers"] for op in ("fwd", "dgrad", "wgrad")}
+        assert sorted(keys) == sorted(want), path
+        fc.axonn_tune_cache_clear()
+        fc.axonn_tune_cache_load(path)
+        assert fc.axonn_tune_cache_size() == len(want)
+    fc.axonn_tune_cache_clear()
+
+
 def test_tune_cache_roundtrip(fc, tmp_path):
     import json
     fc.axonn_tune_cache_clear()

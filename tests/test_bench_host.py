@@ -210,9 +210,9 @@ def test_traffic_reported_only_for_captured_choices(monkeypatch):
     per = []
     for gemm, (choice, _) in first.items():
         layer, op = gemm.split(":")
-        config, group, sk = choice.split("/")
+        config, group, sk, swap = choice.split("/")
         per.append({"layer": layer, "op": op, "config": config, "group_m": int(group),
-                    "streamk_tiles": int(sk)})
+                    "streamk_tiles": int(sk), "swap": int(swap)})
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: bench.TRAFFIC["kernel_sources"])
     want = sum(b for _, b in first.values()) / 12
     assert bench.traffic_per_launch("gpt_h6144_t8192", per, None) == pytest.approx(want)
@@ -221,5 +221,12 @@ def test_traffic_reported_only_for_captured_choices(monkeypatch):
     other = [dict(p) for p in per]
     other[0]["group_m"] = 99
     assert bench.traffic_per_launch("gpt_h6144_t8192", other, None) is None
+    # the same configuration with the operand roles exchanged is another choice
+    flipped = [dict(p) for p in per]
+    flipped[0]["swap"] = 1 - flipped[0]["swap"]
+    if (f"{flipped[0]['layer']}:{flipped[0]['op']}",
+            "/".join(str(flipped[0][k]) for k in ("config", "group_m", "streamk_tiles", "swap"))) \
+            not in bench.TRAFFIC["bytes"]:
+        assert bench.traffic_per_launch("gpt_h6144_t8192", flipped, None) is None
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "0" * 16)
     assert bench.traffic_per_launch("gpt_h6144_t8192", per, None) is None
