@@ -96,36 +96,32 @@ TUNED_DIR = os.path.join(ROOT, "pmm_fc_layer_gb300", "tuned")
 # in profiles/).  Reported only while the kernel sources hash to the value
 # the capture was taken with and every GEMM's choice of this run is in it.
 TRAFFIC = {
-    "workload": "gpt_h6144_t8192", "kernel_sources": "c003daaa9b654152",
+    "workload": "gpt_h6144_t8192", "kernel_sources": "7d1573a93c8d0caa",
     "bytes": {
-        ("qkv:fwd", "pair_512x256/-8/88/1"): 1774615296,
-        ("qkv:fwd", "pair_512x256/16/88/0"): 2422512896,
-        ("qkv:fwd", "pair_512x256/8/88/1"): 1855110656,
-        ("qkv:dgrad", "1cta_256x192/-8/0/0"): 1866920960,
-        ("qkv:dgrad", "1cta_256x192/-8/0/1"): 2038127360,
-        ("qkv:wgrad", "pair_512x256/-16/104/0"): 2357205760,
-        ("qkv:wgrad", "pair_512x256/16/0/0"): 1759607040,
-        ("qkv:wgrad", "pair_512x256/16/104/0"): 2414695168,
-        ("out:fwd", "1cta_256x192/-8/0/0"): 612128640,
-        ("out:fwd", "1cta_256x192/8/0/0"): 558925056,
-        ("out:dgrad", "1cta_256x192/-16/0/0"): 499828992,
-        ("out:dgrad", "1cta_256x192/-8/0/0"): 599616256,
-        ("out:dgrad", "1cta_256x192/-8/0/1"): 664706048,
-        ("out:wgrad", "pair_512x256/-8/0/0"): 575164160,
-        ("out:wgrad", "pair_512x256/16/0/0"): 571150080,
-        ("out:wgrad", "pair_512x256/8/0/1"): 532295936,
-        ("up:fwd", "1cta_256x192/8/0/0"): 1763546624,
-        ("up:fwd", "pair_512x256/16/92/0"): 3138863744,
-        ("up:dgrad", "1cta_256x192/-8/0/0"): 2467148544,
-        ("up:dgrad", "1cta_256x192/8/0/0"): 2321399552,
-        ("up:wgrad", "pair_512x256/16/88/0"): 2816802901,
-        ("down:fwd", "1cta_256x192/-8/0/0"): 2459280128,
-        ("down:fwd", "1cta_256x192/8/0/0"): 2319979520,
-        ("down:dgrad", "1cta_256x192/16/0/0"): 1700046592,
-        ("down:dgrad", "1cta_256x192/8/0/0"): 1760565760,
-        ("down:dgrad", "pair_512x256/-8/0/0"): 2352835840,
-        ("down:wgrad", "pair_512x256/-16/88/0"): 2600390144,
-        ("down:wgrad", "pair_512x256/16/88/0"): 3411776896,
+        ("qkv:fwd", "pair_512x256/-8/88/0"): 2033709568,
+        ("qkv:fwd", "pair_512x256/16/88/0"): 2480573696,
+        ("qkv:dgrad", "1cta_256x192/-8/0/0"): 1863450112,
+        ("qkv:dgrad", "1cta_256x192/16/0/0"): 1770873344,
+        ("qkv:wgrad", "pair_512x256/-16/104/0"): 2358818816,
+        ("qkv:wgrad", "pair_512x256/16/0/0"): 1756339200,
+        ("out:fwd", "1cta_256x192/-8/0/0"): 612682411,
+        ("out:dgrad", "1cta_256x192/-8/0/0"): 598803883,
+        ("out:wgrad", "pair_512x256/-8/0/0"): 573971072,
+        ("out:wgrad", "pair_512x256/16/0/1"): 569758464,
+        ("up:fwd", "1cta_256x192/16/0/0"): 2034324480,
+        ("up:fwd", "pair_512x256/16/0/1"): 3029764864,
+        ("up:fwd", "pair_512x256/16/92/0"): 3113689600,
+        ("up:dgrad", "1cta_256x192/-8/0/0"): 2458654720,
+        ("up:dgrad", "1cta_256x192/16/0/0"): 2353478144,
+        ("up:dgrad", "1cta_256x192/8/0/0"): 2313691136,
+        ("up:wgrad", "pair_512x256/16/88/0"): 2767284096,
+        ("up:wgrad", "pair_512x256/8/88/0"): 2247602176,
+        ("down:fwd", "1cta_256x192/16/0/0"): 2343909120,
+        ("down:fwd", "1cta_256x192/8/0/0"): 2312553728,
+        ("down:fwd", "pair_512x256/8/80/1"): 3004876288,
+        ("down:dgrad", "1cta_256x192/16/0/0"): 2037140864,
+        ("down:dgrad", "pair_512x256/16/92/0"): 3128448768,
+        ("down:wgrad", "pair_512x256/-16/88/0"): 2537176064,
     }}
 
 

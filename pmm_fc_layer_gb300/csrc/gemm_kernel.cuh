@@ -481,7 +481,7 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
 // its rows are stored as 32-byte vectors.  Other tiles (partials to add,
 // fp32 output, a ragged right edge, rows not 32-byte aligned) are stored
 // chunk by chunk and release TMEM afterwards.
-template <int BN>
+template <int BN, bool kTransFast>
 __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t t_row, int row,
                                                   int n0, uint32_t tempty, bool arrive,
                                                   bool remote) {
@@ -508,7 +508,8 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
     }
     return;
   }
-  if (d.out_t && d.out_mode == kOutBF16 && d.red_count == 0 && n0 + BN <= d.N &&
+  if (kTransFast && d.out_t && d.out_mode == kOutBF16 && d.red_count == 0 && n0 + BN <= d.N &&
+      (row | 31) < d.M &&
       ((reinterpret_cast<uintptr_t>(d.C) & 3) | (d.ldc & 1)) == 0) {
     // Transposed bf16 output (exchanged operand roles): as above, the row is
     // packed in registers and TMEM released before any store, so the next
@@ -517,6 +518,9 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
     // packed column pairs, after which the even lane holds column 2w of both
     // rows and the odd lane column 2w+1: one 32-bit store each per pair of
     // columns, the warp covering 64 consecutive bytes of two output rows.
+    const int odd = row & 1;
+    // even lane: (own low half, partner's low half); odd: (partner's high, own high)
+    const uint32_t sel = odd ? 0x3276u : 0x5410u;
     uint32_t pk[BN / 2];
 #pragma unroll
     for (int c = 0; c < BN / 32; ++c) {
@@ -524,7 +528,10 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
       tmem_ld_32x32b_x32(t_row + c * 32, r);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 16; ++j) pk[16 * c + j] = cvt_bf16x2_ordered(r[2 * j], r[2 * j + 1]);
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t mine = cvt_bf16x2_ordered(r[2 * j], r[2 * j + 1]);
+        pk[16 * c + j] = __byte_perm(mine, __shfl_xor_sync(0xffffffffu, mine, 1), sel);
+      }
     }
     tc_fence_before();
     __syncwarp();
@@ -532,20 +539,13 @@ __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t
       if (remote) mbar_arrive_cluster(tempty);
       else mbar_arrive(tempty);
     }
-    const int odd = row & 1;
-    const int rb = row - odd;  // first row of the lane pair
-    // even lane: (own low half, partner's low half); odd: (partner's high, own high)
-    const uint32_t sel = odd ? 0x3276u : 0x5410u;
     const int64_t ld = d.ldc;
-    unsigned short* out = reinterpret_cast<unsigned short*>(d.C) + (n0 + odd) * ld + rb;
-    const bool both = rb + 1 < d.M, first = rb < d.M;
+    uint32_t* out = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned short*>(d.C) +
+                                                (n0 + odd) * ld + (row - odd));
 #pragma unroll
     for (int w = 0; w < BN / 2; ++w) {
-      const uint32_t other = __shfl_xor_sync(0xffffffffu, pk[w], 1);
-      const uint32_t v = __byte_perm(pk[w], other, sel);
-      if (both) *reinterpret_cast<uint32_t*>(out) = v;
-      else if (first) out[0] = static_cast<unsigned short>(v & 0xFFFFu);
-      out += 2 * ld;
+      *out = pk[w];
+      out += ld;  // two output rows of 16-bit elements
     }
     return;
   }
@@ -583,14 +583,14 @@ constexpr int kSkCountersPerUnit = 16;
 // either order, so the output does not depend on which piece comes second.
 // Co-residency of the units is not needed, so launches on other streams
 // cannot stall it.
-template <int BN, int MAXP>
+template <int BN, int MAXP, bool kTransFast = true>
 __device__ __forceinline__ void epilogue_item(const GemmParams<MAXP>& P, const ProblemDesc& d,
                                               int kind, int unit, int warp_slot, int tile_m0,
                                               int n0, uint32_t t_row, int row, uint32_t tempty,
                                               bool remote) {
   const int lane = threadIdx.x & 31;
   if (kind == kWhole) {
-    drain_accumulator<BN>(d, t_row, row, n0, tempty, lane == 0, remote);
+    drain_accumulator<BN, kTransFast>(d, t_row, row, n0, tempty, lane == 0, remote);
     return;
   }
   const bool head = kind == kHead;
@@ -1143,8 +1143,10 @@ __global__ void __launch_bounds__(cta_threads<MH>(), 1)
       tc_fence_after();
       const uint32_t t_row =
           tmem_base + (static_cast<uint32_t>(q * 32) << 16) + b * kAccCols + hh * kHalfCols;
-      epilogue_item<BN>(P, d, kind, blockIdx.x, warp - epi_first_warp<MH>(), tc.m_blk * kTileM, n0,
-                        t_row, row, tempty_bar(b), false);
+      // The transposed register-resident epilogue only where its registers
+      // fit: 320 threads leave 168 a thread, too few beside the plain one.
+      epilogue_item<BN, MAXP, MH == 1>(P, d, kind, blockIdx.x, warp - epi_first_warp<MH>(),
+                                       tc.m_blk * kTileM, n0, t_row, row, tempty_bar(b), false);
       ++acc;
       return true;
     });
