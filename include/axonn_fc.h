@@ -246,7 +246,8 @@ axonn_status_t axonn_fc_vgrid_static(int op, const void* P, const void* Q, void*
  *   labels      int32 [batch x seq], the token each position predicts
  *   keep        out, uint8 [T]: 1 where the label counts
  *   token_loss  out, fp32 [T]: CE_t where kept, 0 elsewhere
- *   loss        out, fp32 [1]: the mean over kept labels (a fixed-order sum)
+ *   loss        out, fp32 [1]: the mean over kept labels (a fixed-order sum);
+ *               during the call its word is the kernels' row counter
  *   kept        out, int32 [1]: n
  *   dlogits     out, bf16 [T x vocab] with ld_dlogits (same alignment), or
  *               NULL for the loss alone

@@ -1579,10 +1579,9 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
     if (ld_dlogits % 8 != 0 || !aligned16(dlogits))
       return fail(AXONN_ERR_ALIGNMENT, "dlogits: 16-byte aligned base and leading dimension a multiple of 8");
   }
-  const int cluster = axonn::goldfish_cluster(vocab);
-  if (cluster == 0)
-    return fail(AXONN_ERR_UNSUPPORTED, "vocabulary %lld needs more than 8 x 96 KB of shared memory per row",
-                (long long)vocab);
+  if (!axonn::goldfish_vocab_supported(vocab))
+    return fail(AXONN_ERR_UNSUPPORTED, "vocabulary %lld above %lld", (long long)vocab,
+                (long long)axonn::kGoldfishMaxVocab);
   DeviceState* dev = nullptr;
   axonn_status_t st = device_state(&dev);
   if (st != AXONN_OK) return st;

@@ -15,31 +15,31 @@
 //
 // Three launches on the caller's stream:
 //  1. goldfish_mask_kernel: one CTA hashes every window, writes keep[] and
-//     the count n (a block reduction, so no atomics and no zeroing).
-//  2. goldfish_rows_kernel: a cluster of C CTAs per row of logits,
-//     persistent over rows.  CTA c of the cluster holds elements
-//     [c*L, (c+1)*L) of a row in shared memory, brought in by one 1-D bulk
-//     copy (cp.async.bulk) into a ring of up to four buffers filled by a
-//     producer warp, so copies of the next kept rows are in flight while one
-//     is computed.  Sixteen consumer warps reduce the slice to (max, sum of
-//     exp) in one pass, the owner of the label adds its logit, and the entry
-//     is pushed into every CTA of the cluster through distributed shared
-//     memory (st.async onto an mbarrier); with all C entries a CTA has
-//     logsumexp and writes its gradient slice from shared memory.  The
-//     exchange of one row overlaps the gradient pass of the previous one.
-//     The logits of a row are read from HBM once; rows of dropped labels are
-//     not read at all (their gradient rows are written as zeros first).
+//     the count n (a block reduction, so no atomics and no zeroing), and
+//     zeroes the word of `loss`, which the rows kernel uses as its row
+//     counter until the mean kernel writes the loss there.
+//  2. goldfish_rows_kernel: one CTA per SM, persistent; each CTA claims the
+//     next row with an atomic add on that counter, so the rows spread over
+//     the SMs as they free up whatever the mix of kept and dropped labels.
+//     A dropped label's gradient row is written as zeros and its logits are
+//     never read.  A kept row is read twice through a ring of 32 KB chunks
+//     filled by a producer warp with 1-D bulk copies: the first pass (from
+//     HBM, lines marked evict-last in L2) reduces it to (max, sum of exp)
+//     and picks the label's logit; the second pass (the same lines, still
+//     in L2, marked evict-first) writes the gradient (softmax - onehot) / n.
+//     The HBM traffic is the kept rows read once and every gradient row
+//     written once.  The producer claims a row and starts its copies while
+//     the consumer warps finish the previous one.
 //  3. goldfish_mean_kernel: one CTA sums token_loss[] in a fixed order and
 //     divides by n.
-// Every wait on a copy is bounded by a wall-clock limit; on expiry the CTA
-// records an error word (read by axonn_sync_status), stops issuing copies,
-// keeps taking part in the cluster barriers and drains before exiting.
+// Every wait is bounded by a wall-clock limit; on expiry the CTA records an
+// error word (read by axonn_sync_status), stops claiming rows and issuing
+// copies, and lets the copies already issued land before it exits.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cstdint>
-#include <mutex>
 
 #include "goldfish.h"
 #include "ptx.cuh"
@@ -51,13 +51,10 @@ namespace {
 constexpr int kGfConsumerWarps = 16;
 constexpr int kGfConsumers = 32 * kGfConsumerWarps;
 constexpr int kGfThreads = kGfConsumers + 32;  // + the producer warp
-constexpr int kGfStages = 4;                   // slice buffers per CTA, at most
 constexpr int kMaskThreads = 1024;
-// Shared memory: a row is split over a cluster of C CTAs (C in {1, 2, 4,
-// 8}); each CTA's slice is at most kMaxSliceBytes, and its ring holds as
-// many slices (up to kGfStages) as fit in kRingBytes.
-constexpr int64_t kMaxSliceBytes = 96 * 1024;
-constexpr int64_t kRingBytes = 200 * 1024;
+constexpr int64_t kGfChunk = 16384;  // elements of one copy (32 KB)
+constexpr int kGfRing = 6;           // chunk buffers (192 KB)
+constexpr int kGfRowQ = 2;           // claimed rows handed to the consumers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -69,13 +66,15 @@ __device__ __forceinline__ void gf_record(uint32_t site) {
   atomicCAS(&g_goldfish_status, 0ULL, code);
 }
 
-// Bounded wait on an mbarrier phase; false (and an error word) on expiry.
+// Bounded wait on an mbarrier phase by polling (a suspended wait slows the
+// code after it); false (and an error word) on expiry.
 __device__ __forceinline__ bool gf_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
                                         uint32_t site) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
-    if (mbar_try_wait_suspend(bar, parity, 20000u)) return true;
+    for (int i = 0; i < 64; ++i)
+      if (mbar_test_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > timeout_ns) {
       gf_record(site);
       return false;
@@ -83,15 +82,36 @@ __device__ __forceinline__ bool gf_wait(uint32_t bar, uint32_t parity, uint64_t 
   }
 }
 
-// 1-D bulk copy global -> this CTA's shared memory, completion counted on
-// `bar` in bytes (both addresses 16-byte aligned, size a multiple of 16).
+// 1-D bulk copy global -> this CTA's shared memory with an L2 cache policy,
+// completion counted on `bar` in bytes (both addresses 16-byte aligned, size
+// a multiple of 16).
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
+                                          uint32_t bar, uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// Bounded wait of a whole warp: lane 0 polls, then every lane tests the
+// completed phase once (each lane's own acquire of the data it guards).  The
+// barriers waited on this way cannot complete their next phase before this
+// warp has released them, so the phase lane 0 saw is still the one tested.
+__device__ __forceinline__ bool gf_warp_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                             uint32_t site) {
+  bool got = true;
+  if ((threadIdx.x & 31) == 0) got = gf_wait(bar, parity, timeout_ns, site);
+  got = __shfl_sync(0xFFFFFFFFu, got, 0) != 0;
+  if (got) (void)mbar_test_wait(bar, parity);
+  return got;
+}
+
+// L2 policy marking every line of an access evict-first.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // 2^x by the SFU's approximation (PTX ex2.approx.ftz.f32: relative error
@@ -156,38 +176,49 @@ __global__ void __launch_bounds__(kMaskThreads) goldfish_mask_kernel(GoldfishArg
     int n = 0;
     for (int w = 0; w < kMaskThreads / 32; ++w) n += counts[w];
     *a.kept = n;
+    *reinterpret_cast<unsigned int*>(a.loss) = 0u;  // the rows kernel's row counter
   }
 }
 
 // ------------------------------------------------------------------ rows
 struct RowParams {
   GoldfishArgs a;
-  int cluster;    // CTAs per row
-  int stages;     // slice buffers in the ring (2 to kGfStages)
-  int64_t slice;  // elements per CTA (multiple of 8)
+  int chunks;  // copies per row: ceil(vpad / kGfChunk), vpad = V rounded up to 8
 };
 
-constexpr int kInbox = 3;  // inbox slots: rows kc, kc+1 and kc+2 may be in flight
-
-// Shared memory after the slice buffers.
+// Shared memory after the chunk buffers.
 struct alignas(16) GfTail {
-  float4 inbox[kInbox][8];  // [row % kInbox][sending CTA]: max, sum of exp, label logit, has it
-  uint64_t full[kGfStages];
-  uint64_t empty[kGfStages];
-  uint64_t inbox_bar[kInbox];
-  int64_t meta_row[kGfStages];
-  int32_t meta_y[kGfStages];
+  uint64_t full[kGfRing];
+  uint64_t empty[kGfRing];
+  uint64_t rq_full[kGfRowQ];
+  uint64_t rq_empty[kGfRowQ];
+  int64_t rq_row[kGfRowQ];  // claimed row, or -1: no more rows for this CTA
+  int32_t rq_y[kGfRowQ];
+  int32_t rq_keep[kGfRowQ];
   float red_m[kGfConsumerWarps];
   float red_s[kGfConsumerWarps];
-  int red_n[kGfConsumerWarps];
-  float lse;
+  float zy;  // the label's logit of the row in progress
   int aborted;
-  uint8_t flags[kGfConsumers];  // mask flags of a chunk of the cluster's rows
 };
 
 // Barrier among the consumer warps only (the producer warp runs ahead).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGfConsumers) : "memory");
+}
+
+// Barrier among the consumer warps that also ORs a predicate over them: every
+// consumer gets the same answer.
+__device__ __forceinline__ bool consumers_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(kGfConsumers)
+      : "memory");
+  return r != 0;
 }
 
 // The eight bf16 values of a 16-byte vector as floats (exact): a bf16 is
@@ -204,19 +235,14 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
   x[7] = __uint_as_float(v.w & 0xFFFF0000u);
 }
 
-// Writes zeros to elements [c0, c1) of a gradient row (16-byte stores for
-// the part whose start is 8-aligned, single elements for the tail), by the
-// consumer threads.
-__device__ __forceinline__ void zero_row(uint16_t* row, int64_t c0, int64_t c1, int ct) {
-  const int64_t v1 = c0 + ((c1 - c0) & ~int64_t{7});
-  for (int64_t i = c0 + 8 * ct; i < v1; i += 8 * kGfConsumers)
+// Writes zeros to elements [0, n) of a gradient row (16-byte stores for the
+// whole vectors, single elements for the tail), by the consumer threads.
+__device__ __forceinline__ void zero_row(uint16_t* row, int64_t n, int ct) {
+  const int64_t v1 = n & ~int64_t{7};
+  for (int64_t i = 8 * ct; i < v1; i += 8 * kGfConsumers)
     __stcs(reinterpret_cast<int4*>(row + i), make_int4(0, 0, 0, 0));
-  for (int64_t i = v1 + ct; i < c1; i += kGfConsumers) row[i] = 0;
+  for (int64_t i = v1 + ct; i < n; i += kGfConsumers) row[i] = 0;
 }
-
-// Number of consumer threads whose `pred` is true (a barrier among the
-// consumers; every consumer thread gets the count).
-__device__ __forceinline__ int consumers_count(bool pred, GfTail* tl);
 
 // Adds values to one thread's running (max, sum of exp(x - max)).
 __device__ __forceinline__ void online_add8(float& m, float& s, const float (&x)[8]) {
@@ -244,106 +270,92 @@ __device__ __forceinline__ void online_add1(float& m, float& s, float x) {
   s += fast_exp2((x - m) * kLog2e);
 }
 
-__device__ __forceinline__ int consumers_count(bool pred, GfTail* tl) {
-  const int w = (threadIdx.x >> 5) - 1;
-  const int c = __popc(__ballot_sync(0xFFFFFFFFu, pred));
-  if ((threadIdx.x & 31) == 0) tl->red_n[w] = c;
-  consumer_sync();
-  int n = 0;
-#pragma unroll
-  for (int i = 0; i < kGfConsumerWarps; ++i) n += tl->red_n[i];
-  return n;
-}
-
-// Warp 0 is the producer: lane 0 bulk-copies this CTA's slice of every kept
-// row of the cluster, in order, into a ring of `stages` buffers.  Warps
-// 1..16 are the consumers.  They first write the zero gradient rows (and
-// zero losses) of the cluster's dropped labels, which need no logits.  Then,
-// for kept row kc, each CTA reduces its slice to (max, sum of exp), adds the
-// label's logit if it owns it, and pushes that entry with st.async into the
-// same inbox slot (kc mod 3) of every CTA of the cluster, completing on that
-// CTA's inbox barrier.  Row kc+1 is reduced and pushed before row kc's inbox
-// is read and its gradient written, so the exchange overlaps a gradient
-// pass.  A CTA pushes row kc+3 into slot kc mod 3 only after it has every
-// peer's entry for row kc+2, which each peer pushes after reading its row
-// kc entries: three slots suffice and no cluster barrier is needed per row.
+// Warp 0 is the producer: lane 0 claims rows (atomic add on the counter),
+// hands each to the consumers through a queue of kGfRowQ entries and, for a
+// kept row, copies its chunks in order into the ring: the whole row for the
+// first pass, then the whole row again for the second (only the first when
+// no gradient is asked for).  Warps 1..16 are the consumers.  All consumer
+// threads wait on the same barriers and take every decision that ends the
+// loop together (consumers_any), so their barrier counts always match.
 __global__ void __launch_bounds__(kGfThreads, 1)
     goldfish_rows_kernel(const __grid_constant__ RowParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GoldfishArgs& a = p.a;
-  const int C = p.cluster;
-  const int NB = p.stages;
-  const uint32_t rank = C > 1 ? cluster_ctarank() : 0u;
-  const int64_t cl = blockIdx.x / C;
-  const int64_t ncl = gridDim.x / C;
   const int64_t T = a.batch * a.seq;
   const int64_t V = a.vocab;
   const int64_t vpad = (V + 7) & ~int64_t{7};
-  const int64_t s0 = static_cast<int64_t>(rank) * p.slice;
-  const int64_t n_load = s0 < vpad ? min(p.slice, vpad - s0) : 0;  // elements copied
-  const int64_t n_valid = s0 < V ? min(p.slice, V - s0) : 0;       // elements of the row
-  const int64_t buf_bytes = p.slice * 2;
-  GfTail* tl = reinterpret_cast<GfTail*>(smem + NB * buf_bytes);
+  const int nch = p.chunks;
+  const int passes = a.dlogits ? 2 : 1;
+  GfTail* tl = reinterpret_cast<GfTail*>(smem + kGfRing * kGfChunk * 2);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns;
+  auto buf = [&](int b) { return smem_addr(smem) + static_cast<uint32_t>(b * kGfChunk * 2); };
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < NB; ++b) {
+    for (int b = 0; b < kGfRing; ++b) {
       mbar_init(smem_addr(&tl->full[b]), 1);
       mbar_init(smem_addr(&tl->empty[b]), kGfConsumerWarps);
     }
-    for (int q = 0; q < kInbox; ++q) mbar_init(smem_addr(&tl->inbox_bar[q]), 1);
+    for (int q = 0; q < kGfRowQ; ++q) {
+      mbar_init(smem_addr(&tl->rq_full[q]), 1);
+      mbar_init(smem_addr(&tl->rq_empty[q]), kGfConsumerWarps);
+    }
     tl->aborted = 0;
     fence_mbarrier_init();
   }
-  // every CTA's barriers are set up before any peer pushes to them
-  cluster_sync();
+  __syncthreads();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    int b = 0;
-    uint32_t ph = 0;
-    int issued[kGfStages] = {};  // 1 + the last use of each stage that carried a copy
-    int uses[kGfStages] = {};
-    for (int64_t base = cl; base < T; base += 32 * ncl) {
-      // 32 rows' labels and mask flags at once, one per lane
-      const int64_t rr = base + lane * ncl;
-      const int32_t keep_l = rr < T ? a.keep[rr] : 0;
-      const int32_t y_l = rr < T ? a.labels[rr] : 0;
-      uint32_t kept_bits = __ballot_sync(0xFFFFFFFFu, keep_l != 0);
-      while (kept_bits) {
-        const int j = __ffs(kept_bits) - 1;
-        kept_bits &= kept_bits - 1;
-        const int32_t y = __shfl_sync(0xFFFFFFFFu, y_l, j);
-        if (lane == 0) {
-          const int64_t r = base + j * ncl;
-          if (!gf_wait(smem_addr(&tl->empty[b]), ph ^ 1u, tmo, 3)) tl->aborted = 1;
-          tl->meta_row[b] = r;
-          tl->meta_y[b] = y;
-          const uint32_t fb = smem_addr(&tl->full[b]);
-          if (n_load > 0 && !tl->aborted) {
-            mbar_arrive_expect_tx(fb, static_cast<uint32_t>(n_load * 2));
-            bulk_load(smem_addr(smem + b * buf_bytes), a.logits + r * a.ld_logits + s0,
-                      static_cast<uint32_t>(n_load * 2), fb);
-            issued[b] = uses[b] + 1;
-          } else {
-            mbar_arrive(fb);  // publishes the entry; nothing to copy
-          }
-          ++uses[b];
+    if (lane == 0) {
+      unsigned int* counter = reinterpret_cast<unsigned int*>(a.loss);
+      const uint64_t keep_pol = l2_policy(true, 1.0f);
+      const uint64_t drop_pol = evict_first_policy();
+      int b = 0, q = 0;
+      uint32_t ph = 0, qph = 0;
+      uint32_t uses[kGfRing] = {};  // copies issued into each buffer
+      bool ok = true;
+      while (true) {
+        ok = ok && gf_wait(smem_addr(&tl->rq_empty[q]), qph ^ 1u, tmo, 1);
+        const int64_t r = ok ? static_cast<int64_t>(atomicAdd(counter, 1u)) : T;
+        const bool more = r < T;
+        const int32_t keep = more ? a.keep[r] : 0;
+        tl->rq_row[q] = more ? r : -1;
+        tl->rq_y[q] = more ? a.labels[r] : 0;
+        tl->rq_keep[q] = keep;
+        mbar_arrive(smem_addr(&tl->rq_full[q]));
+        if (++q == kGfRowQ) {
+          q = 0;
+          qph ^= 1u;
         }
-        __syncwarp();
-        if (++b == NB) {
-          b = 0;
-          ph ^= 1u;
+        if (!more) break;
+        if (!keep) continue;
+        const uint16_t* src = a.logits + r * a.ld_logits;
+        for (int pass = 0; pass < passes && ok; ++pass) {
+          for (int c = 0; c < nch; ++c) {
+            ok = gf_wait(smem_addr(&tl->empty[b]), ph ^ 1u, tmo, 2);
+            if (!ok) break;
+            const int64_t e0 = c * kGfChunk;
+            const uint32_t bytes = static_cast<uint32_t>(min(kGfChunk, vpad - e0) * 2);
+            const uint32_t fb = smem_addr(&tl->full[b]);
+            mbar_arrive_expect_tx(fb, bytes);
+            bulk_load(buf(b), src + e0, bytes, fb, pass == 0 ? keep_pol : drop_pol);
+            ++uses[b];
+            if (++b == kGfRing) {
+              b = 0;
+              ph ^= 1u;
+            }
+          }
         }
       }
-    }
-    // Copies not consumed exist only after an expired wait: let them land
-    // (bounded) before this CTA's shared memory goes away.
-    if (lane == 0 && tl->aborted) {
-      for (int q = 0; q < NB; ++q)
-        if (issued[q] > 0) gf_wait(smem_addr(&tl->full[q]), (issued[q] - 1) & 1u, tmo, 2);
+      // Copies the consumers did not take exist only after an expired wait:
+      // let them land (bounded) before this CTA's shared memory goes away.
+      if (!ok) {
+        tl->aborted = 1;
+        for (int i = 0; i < kGfRing; ++i)
+          if (uses[i] > 0) gf_wait(smem_addr(&tl->full[i]), (uses[i] - 1) & 1u, tmo, 3);
+      }
     }
   } else {
     // ------------------------------------------------------------ consumers
@@ -352,59 +364,61 @@ __global__ void __launch_bounds__(kGfThreads, 1)
     const int32_t n = *a.kept;
     const float inv_n = n > 0 ? 1.0f / static_cast<float>(n) : 0.0f;
     const float log2n = n > 0 ? log2f(static_cast<float>(n)) : 0.0f;
-
-    // 1. rows of dropped labels: zero gradient slices and losses; count the
-    //    kept rows of this cluster.  The mask flags of kGfConsumers rows at a
-    //    time are read in parallel (one per thread) into shared memory.
-    int nk = 0;
-    for (int64_t base = cl; base < T; base += static_cast<int64_t>(kGfConsumers) * ncl) {
-      const int64_t rr = base + static_cast<int64_t>(ct) * ncl;
-      const int kf = rr < T ? a.keep[rr] : 1;
-      tl->flags[ct] = static_cast<uint8_t>(kf != 0);
-      nk += consumers_count(rr < T && kf != 0, tl);
-      for (int j = 0; j < kGfConsumers; ++j) {
-        const int64_t r = base + static_cast<int64_t>(j) * ncl;
-        if (r >= T) break;
-        if (tl->flags[j]) continue;
-        if (a.dlogits && n_valid > 0) zero_row(a.dlogits + r * a.ld_dlogits, s0, s0 + n_valid, ct);
-        if (rank == 0 && ct == 0) a.token_loss[r] = 0.0f;
+    int b = 0, q = 0;
+    uint32_t ph = 0, qph = 0;
+    bool ok = true;  // this thread's waits all completed
+    // waits for chunk b, passes it to f(x, e0, n_valid) when it arrived, and
+    // releases the buffer
+    auto take_chunk = [&](int c, auto&& f) {
+      const bool got = ok && gf_warp_wait(smem_addr(&tl->full[b]), ph, tmo, 4);
+      ok = got;
+      const int64_t e0 = c * kGfChunk;
+      const int64_t nv = max(int64_t{0}, min(kGfChunk, V - e0));
+      if (got) f(reinterpret_cast<const uint16_t*>(smem + b * kGfChunk * 2), e0, nv);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tl->empty[b]));
+      if (++b == kGfRing) {
+        b = 0;
+        ph ^= 1u;
       }
-      consumer_sync();  // flags are rewritten for the next chunk
-    }
-
-    // 2. kept rows, software-pipelined by one row
-    auto stage_of = [&](int kc) { return kc % NB; };
-    auto wait_full = [&](int kc) {
-      if (!gf_wait(smem_addr(&tl->full[stage_of(kc)]), static_cast<uint32_t>((kc / NB) & 1), tmo, 1))
-        tl->aborted = 1;
     };
-    // reduce kept row kc to this slice's entry and push it to every CTA
-    auto reduce_push = [&](int kc) {
-      wait_full(kc);
-      const int b = stage_of(kc);
-      const uint16_t* x = reinterpret_cast<const uint16_t*>(smem + b * buf_bytes);
-      const int32_t y = tl->meta_y[b];
-      const bool have = n_load > 0 && !tl->aborted;
-      float m0 = -INFINITY, s0_ = 0.0f, m1 = -INFINITY, s1 = 0.0f;
-      if (have) {
-        // whole 8-element vectors, two per iteration, then the ragged tail
-        const int64_t vfull = n_valid & ~int64_t{7};
-        for (int64_t i = 16 * ct; i < vfull; i += 16 * kGfConsumers) {
-          float xa[8];
-          unpack8(*reinterpret_cast<const uint4*>(x + i), xa);
-          online_add8(m0, s0_, xa);
-          if (i + 8 < vfull) {
-            float xb[8];
-            unpack8(*reinterpret_cast<const uint4*>(x + i + 8), xb);
-            online_add8(m1, s1, xb);
-          }
-        }
-        for (int64_t i = vfull + ct; i < n_valid; i += kGfConsumers)
-          online_add1(m1, s1, bf16_to_f32(x[i]));
+    while (true) {
+      ok = ok && gf_warp_wait(smem_addr(&tl->rq_full[q]), qph, tmo, 5);
+      const int64_t r = tl->rq_row[q];
+      const int32_t y = tl->rq_y[q];
+      const bool keep = tl->rq_keep[q] != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tl->rq_empty[q]));
+      if (++q == kGfRowQ) {
+        q = 0;
+        qph ^= 1u;
       }
-      // thread's (max, sum), then the slice's
+      if (consumers_any(!ok || r < 0)) break;
+      if (!keep) {
+        if (a.dlogits) zero_row(a.dlogits + r * a.ld_dlogits, V, ct);
+        if (ct == 0) a.token_loss[r] = 0.0f;
+        continue;
+      }
+      // 1. (max, sum of exp) of the row, and the label's logit
+      float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
+      for (int c = 0; c < nch; ++c)
+        take_chunk(c, [&](const uint16_t* x, int64_t e0, int64_t nv) {
+          const int64_t vfull = nv & ~int64_t{7};
+          for (int64_t i = 16 * ct; i < vfull; i += 16 * kGfConsumers) {
+            float xa[8];
+            unpack8(*reinterpret_cast<const uint4*>(x + i), xa);
+            online_add8(m0, s0, xa);
+            if (i + 8 < vfull) {
+              float xb[8];
+              unpack8(*reinterpret_cast<const uint4*>(x + i + 8), xb);
+              online_add8(m1, s1, xb);
+            }
+          }
+          for (int64_t i = vfull + ct; i < nv; i += kGfConsumers) online_add1(m1, s1, bf16_to_f32(x[i]));
+          if (ct == 0 && y >= e0 && y < e0 + nv) tl->zy = bf16_to_f32(x[y - e0]);
+        });
       float m = fmaxf(m0, m1);
-      float sm = (m0 > -INFINITY ? s0_ * fast_exp2((m0 - m) * kLog2e) : 0.0f) +
+      float sm = (m0 > -INFINITY ? s0 * fast_exp2((m0 - m) * kLog2e) : 0.0f) +
                  (m1 > -INFINITY ? s1 * fast_exp2((m1 - m) * kLog2e) : 0.0f);
       float wm = m;
 #pragma unroll
@@ -419,93 +433,47 @@ __global__ void __launch_bounds__(kGfThreads, 1)
       for (int o = 16; o > 0; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
       if (lane == 0) tl->red_s[cw] = ws;
       consumer_sync();
-      if (ct == 0) {
-        float S = 0.0f;
+      float S = 0.0f;
 #pragma unroll
-        for (int w = 0; w < kGfConsumerWarps; ++w) S += tl->red_s[w];
-        const bool mine = have && y >= s0 && y < s0 + n_valid;
-        const float4 entry = make_float4(M, S, mine ? bf16_to_f32(x[y - s0]) : 0.0f,
-                                         mine ? 1.0f : 0.0f);
-        const int q = kc % kInbox;
-        const uint32_t ib = smem_addr(&tl->inbox_bar[q]);
-        mbar_arrive_expect_tx(ib, static_cast<uint32_t>(16 * C));
-        const uint32_t slot = smem_addr(&tl->inbox[q][rank]);
-        for (int c = 0; c < C; ++c)
-          st_async_v4(mapa_shared(slot, static_cast<uint32_t>(c)), entry,
-                      mapa_shared(ib, static_cast<uint32_t>(c)));
-      }
-    };
-    if (nk > 0) reduce_push(0);
-    for (int kc = 0; kc < nk; ++kc) {
-      if (kc + 1 < nk) reduce_push(kc + 1);
-      const int b = stage_of(kc);
-      const int64_t r = tl->meta_row[b];
-      const int32_t y = tl->meta_y[b];
-      const uint16_t* x = reinterpret_cast<const uint16_t*>(smem + b * buf_bytes);
-      const bool have = n_load > 0 && !tl->aborted;
-      if (cw == 0) {
-        // logsumexp of the row from the C entries of its inbox slot
-        const int q = kc % kInbox;
-        // every lane waits (each then sees the pushed entries)
-        if (!gf_wait(smem_addr(&tl->inbox_bar[q]), static_cast<uint32_t>((kc / kInbox) & 1), tmo, 4))
-          tl->aborted = 1;
-        const float4 e = lane < C ? tl->inbox[q][lane] : make_float4(-INFINITY, 0.0f, 0.0f, 0.0f);
-        float M = e.x;
+      for (int w = 0; w < kGfConsumerWarps; ++w) S += tl->red_s[w];
+      const float lse = M + log2f(S) * kLn2;
+      if (ct == 0) a.token_loss[r] = lse - tl->zy;
+      // red_m, red_s and zy are rewritten only after every consumer has read
+      // them: the next row's first write follows at least one more barrier
+      // (consumers_any) that every consumer reaches after these reads.
+      if (!a.dlogits) continue;
+      // 2. gradient: p / n = 2^(z log2e - (lse log2e + log2 n)), the 1/n
+      //    folded into the exponent; the label's entry less 1/n
+      const float lb = fmaf(lse, kLog2e, log2n);
+      uint16_t* out = a.dlogits + r * a.ld_dlogits;
+      for (int c = 0; c < nch; ++c)
+        take_chunk(c, [&](const uint16_t* x, int64_t e0, int64_t nv) {
+          const int64_t yl = y - e0;  // the label's place in this chunk (may be outside)
+          const int64_t vfull = nv & ~int64_t{7};
+          for (int64_t i = 8 * ct; i < vfull; i += 8 * kGfConsumers) {
+            float g[8];
+            unpack8(*reinterpret_cast<const uint4*>(x + i), g);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        float S = e.x > -INFINITY ? e.y * fast_exp2((e.x - M) * kLog2e) : 0.0f;
-        float zy = e.w != 0.0f ? e.z : 0.0f;
+            for (int j = 0; j < 8; ++j) g[j] = fast_exp2(fmaf(g[j], kLog2e, -lb));
+            const int64_t d = yl - i;  // the label's element, if in this vector
+            if (d >= 0 && d < 8) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          S += __shfl_xor_sync(0xFFFFFFFFu, S, o);
-          zy += __shfl_xor_sync(0xFFFFFFFFu, zy, o);
-        }
-        if (lane == 0) {
-          const float lse = M + log2f(S) * kLn2;
-          tl->lse = lse;
-          if (rank == 0) a.token_loss[r] = lse - zy;
-        }
-      }
-      consumer_sync();
-      const float lse = tl->lse;
-      // gradient slice: (softmax - onehot) / n, from shared memory
-      if (a.dlogits && n_valid > 0) {
-        uint16_t* out = a.dlogits + r * a.ld_dlogits + s0;
-        // p / n = 2^(z log2e - (lse log2e + log2 n)): the 1/n folded into
-        // the exponent
-        const float lb = fmaf(lse, kLog2e, log2n);
-        const int64_t yl = y - s0;  // the label's place in this slice (may be outside)
-        const int64_t vfull = n_valid & ~int64_t{7};
-        for (int64_t i = 8 * ct; i < vfull; i += 8 * kGfConsumers) {
-          float g[8];
-          unpack8(have ? *reinterpret_cast<const uint4*>(x + i) : make_uint4(0, 0, 0, 0), g);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) g[j] = fast_exp2(fmaf(g[j], kLog2e, -lb));
-          const int64_t d = yl - i;  // the label's element, if in this vector
-          if (d >= 0 && d < 8) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (j == d) g[j] -= inv_n;
+              for (int j = 0; j < 8; ++j)
+                if (j == d) g[j] -= inv_n;
+            }
+            __stcs(reinterpret_cast<int4*>(out + e0 + i),
+                   make_int4(static_cast<int>(pack2(g[0], g[1])), static_cast<int>(pack2(g[2], g[3])),
+                             static_cast<int>(pack2(g[4], g[5])), static_cast<int>(pack2(g[6], g[7]))));
           }
-          __stcs(reinterpret_cast<int4*>(out + i),
-                 make_int4(static_cast<int>(pack2(g[0], g[1])), static_cast<int>(pack2(g[2], g[3])),
-                           static_cast<int>(pack2(g[4], g[5])), static_cast<int>(pack2(g[6], g[7]))));
-        }
-        for (int64_t i = vfull + ct; i < n_valid; i += kGfConsumers) {
-          const float z = have ? bf16_to_f32(x[i]) : 0.0f;
-          float g = fast_exp2(fmaf(z, kLog2e, -lb));
-          if (i == yl) g -= inv_n;
-          __nv_bfloat16 h = __float2bfloat16_rn(g);
-          out[i] = *reinterpret_cast<uint16_t*>(&h);
-        }
-      }
-      // this warp is done with the stage's buffer
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&tl->empty[b]));
+          for (int64_t i = vfull + ct; i < nv; i += kGfConsumers) {
+            float gs = fast_exp2(fmaf(bf16_to_f32(x[i]), kLog2e, -lb));
+            if (i == yl) gs -= inv_n;
+            __nv_bfloat16 h = __float2bfloat16_rn(gs);
+            out[e0 + i] = *reinterpret_cast<uint16_t*>(&h);
+          }
+        });
     }
   }
-  // no CTA leaves while a peer may still push into its inbox
-  cluster_sync();
 }
 
 // ------------------------------------------------------------------ mean
@@ -528,99 +496,7 @@ __global__ void __launch_bounds__(1024) goldfish_mean_kernel(GoldfishArgs a) {
 
 }  // namespace
 
-int64_t goldfish_slice(int64_t vocab, int cluster) {
-  const int64_t vpad = (vocab + 7) / 8 * 8;
-  const int64_t per = (vpad + cluster - 1) / cluster;
-  return (per + 7) / 8 * 8;
-}
-
-int goldfish_cluster(int64_t vocab) {
-  for (int c = 1; c <= 8; c *= 2)
-    if (goldfish_slice(vocab, c) * 2 <= kMaxSliceBytes) return c;
-  return 0;
-}
-
-namespace {
-
-// Ring depth and shared memory of the rows kernel for a slice.
-int ring_stages(int64_t slice) {
-  return static_cast<int>(std::min<int64_t>(kGfStages, kRingBytes / (slice * 2)));
-}
-size_t rows_smem(int64_t slice) {
-  return static_cast<size_t>(ring_stages(slice) * slice * 2) + sizeof(GfTail);
-}
-
-cudaLaunchConfig_t rows_config(int cluster, int64_t slice, int grid, cudaStream_t stream,
-                               cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kGfThreads, 1, 1);
-  cfg.dynamicSmemBytes = rows_smem(slice);
-  cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
-// The cluster size for a vocabulary: among the sizes whose slices fit a ring
-// of at least two buffers, the one that keeps the most SMs busy when the
-// GPU holds as many clusters as it can at once (a cluster must fit in one
-// GPC, so fewer large clusters may fit than SMs / C), and its cluster
-// count.  Decided once per device and vocabulary.
-struct ClusterPick {
-  int64_t vocab = -1;
-  int device = -1;
-  int cluster = 0;
-  int resident = 0;
-};
-std::mutex g_pick_mu;
-ClusterPick g_picks[16];
-
-cudaError_t pick_cluster(int64_t vocab, int sms, int* cluster, int* resident) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  std::lock_guard<std::mutex> lk(g_pick_mu);
-  for (const ClusterPick& c : g_picks)
-    if (c.vocab == vocab && c.device == dev) {
-      *cluster = c.cluster;
-      *resident = c.resident;
-      return cudaSuccess;
-    }
-  int best_c = 0, best_r = 0;
-  for (int c = 8; c >= 1; c /= 2) {
-    const int64_t slice = goldfish_slice(vocab, c);
-    if (slice * 2 > kMaxSliceBytes || ring_stages(slice) < 2) continue;
-    e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(rows_smem(slice)));
-    if (e != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = rows_config(c, slice, c * sms, nullptr, attr);
-    int r = 0;
-    if (cudaOccupancyMaxActiveClusters(&r, reinterpret_cast<const void*>(goldfish_rows_kernel),
-                                       &cfg) != cudaSuccess || r < 1) {
-      (void)cudaGetLastError();
-      r = std::max(1, sms / c);
-    }
-    if (best_c == 0 || r * c > best_r * best_c) {
-      best_c = c;
-      best_r = r;
-    }
-  }
-  if (best_c == 0) return cudaErrorInvalidValue;
-  static int next = 0;
-  g_picks[next] = ClusterPick{vocab, dev, best_c, best_r};
-  next = (next + 1) % 16;
-  *cluster = best_c;
-  *resident = best_r;
-  return cudaSuccess;
-}
-
-}  // namespace
+bool goldfish_vocab_supported(int64_t vocab) { return vocab >= 1 && vocab <= kGoldfishMaxVocab; }
 
 cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream) {
   const int64_t T = a.batch * a.seq;
@@ -628,24 +504,17 @@ cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream)
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (T > 0) {
-    int cluster = 0, resident = 0;
-    e = pick_cluster(a.vocab, sms, &cluster, &resident);
-    if (e != cudaSuccess) return e;
     RowParams p;
     p.a = a;
-    p.cluster = cluster;
-    p.slice = goldfish_slice(a.vocab, cluster);
-    p.stages = ring_stages(p.slice);
-    e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(rows_smem(p.slice)));
+    const int64_t vpad = (a.vocab + 7) / 8 * 8;
+    p.chunks = static_cast<int>((vpad + kGfChunk - 1) / kGfChunk);
+    const int smem = static_cast<int>(kGfRing * kGfChunk * 2 + sizeof(GfTail));
+    e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    // Persistent clusters: as many as the GPU holds at once, at most one per
-    // row (with more, the rest would run as a second wave).
-    const int64_t clusters = std::min<int64_t>(resident, T);
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = rows_config(cluster, p.slice, static_cast<int>(clusters * cluster),
-                                         stream, attr);
-    e = cudaLaunchKernelEx(&cfg, goldfish_rows_kernel, p);
+    // Persistent: one CTA per SM, at most one per row.
+    const int64_t ctas = std::min<int64_t>(sms, T);
+    goldfish_rows_kernel<<<static_cast<unsigned>(ctas), kGfThreads, smem, stream>>>(p);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   goldfish_mean_kernel<<<1, 1024, 0, stream>>>(a);

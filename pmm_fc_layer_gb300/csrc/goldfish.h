@@ -24,17 +24,15 @@ struct GoldfishArgs {
   uint64_t timeout_ns;
 };
 
-// Slice of a row one CTA of the cluster holds: elements per CTA (a multiple
-// of 8) for a cluster of `cluster` CTAs over a row of `vocab` elements.
-int64_t goldfish_slice(int64_t vocab, int cluster);
+// Largest vocabulary the entry point accepts (8 x 49152 tokens).
+constexpr int64_t kGoldfishMaxVocab = 8 * 49152;
 
-// Smallest cluster size in {1, 2, 4, 8} whose slice fits the per-CTA
-// shared-memory budget; 0 if none does (the vocabulary is too large).
-int goldfish_cluster(int64_t vocab);
+// Whether a vocabulary of `vocab` tokens is in [1, kGoldfishMaxVocab].
+bool goldfish_vocab_supported(int64_t vocab);
 
-// The three launches (mask and count, rows, mean) on `stream`.  The rows
-// kernel's cluster size is the feasible one that keeps the most of the
-// `sms` SMs busy (decided once per device and vocabulary).
+// The three launches (mask and count, rows, mean) on `stream`; the rows
+// kernel runs one persistent CTA on each of the `sms` SMs (fewer for fewer
+// rows).
 cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream);
 
 // Reads (and clears if set) the device error word of these kernels.

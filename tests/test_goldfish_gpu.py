@@ -2,12 +2,13 @@
 fp64 oracle (oracle/goldfish.py).
 
 * The mask and the count are integers: bit for bit.
-* Per-token cross-entropy: the kernel sums each row's exponentials in fp32,
-  at most about 80 terms in series per thread (a 32 KB slice over 256
-  threads) and then a fixed tree of at most 11 levels, so the relative
-  error of the sum is below (80 + 11) * 2^-24 < 6e-6; the exponent's own
-  rounding and exp2/log2 add a few ulps.  That bounds |CE - CE_ref| by
-  1e-5 * (1 + |logsumexp|).
+* Per-token cross-entropy: the kernel sums each row's exponentials in fp32.
+  A thread adds 8-element partial sums (4 terms, then one more add) into two
+  accumulators, at most 48 each (a 393216-element row over 512 threads);
+  then the two, a 5-level warp tree and the 16 warps' sums in series: under
+  80 roundings in series, so the relative error of the sum is below
+  91 * 2^-24 < 6e-6; the exponent's own rounding and exp2/log2 add a few
+  ulps.  That bounds |CE - CE_ref| by 1e-5 * (1 + |logsumexp|).
 * The mean adds at most one more fp32 summation of T terms (8 in series per
   thread, then a 10-level tree): 1e-5 * (1 + |loss|) plus the per-token
   bound.
@@ -102,8 +103,8 @@ def test_goldfish_vs_oracle(cuda_lib, V, k, h):
 
 @pytest.mark.parametrize("V", [128256, 300001])
 def test_goldfish_large_vocabularies(cuda_lib, V):
-    """Clusters of 8 CTAs per row (32 KB slices in a ring of four, and 75 KB
-    slices in a ring of two)."""
+    """Rows of 8 and 19 chunks of 32 KB through the six-buffer ring (the
+    last chunk of each ragged), logits and gradient rows padded."""
     ids, labels, logits = _problem(1, 48, V, 200 + V % 13)
     got = _run(cuda_lib, ids, labels, logits, 2, 13, ld_pad=8)
     _check(got, gf.goldfish_ce(logits, ids, labels, 2, 13), V, logits)
