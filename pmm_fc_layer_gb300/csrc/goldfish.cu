@@ -26,10 +26,12 @@
 //     filled by a producer warp with 1-D bulk copies: the first pass (from
 //     HBM, lines marked evict-last in L2) reduces it to (max, sum of exp)
 //     and picks the label's logit; the second pass (the same lines, still
-//     in L2, marked evict-first) writes the gradient (softmax - onehot) / n.
-//     The HBM traffic is the kept rows read once and every gradient row
-//     written once.  The producer claims a row and starts its copies while
-//     the consumer warps finish the previous one.
+//     in L2, marked evict-first) computes the gradient (softmax - onehot) / n
+//     into the chunk's buffer, and a store warp copies it out with one bulk
+//     copy per chunk (and zero-fills dropped rows the same way).  The HBM
+//     traffic is the kept rows read once and every gradient row written
+//     once.  The producer claims a row and starts its copies while the
+//     consumer warps finish the previous one.
 //  3. goldfish_mean_kernel: one CTA sums token_loss[] in a fixed order and
 //     divides by n.
 // Every wait is bounded by a wall-clock limit; on expiry the CTA records an
@@ -50,11 +52,12 @@ namespace {
 
 constexpr int kGfConsumerWarps = 16;
 constexpr int kGfConsumers = 32 * kGfConsumerWarps;
-constexpr int kGfThreads = kGfConsumers + 32;  // + the producer warp
+constexpr int kGfThreads = kGfConsumers + 64;  // + the producer and the store warp
 constexpr int kMaskThreads = 1024;
 constexpr int64_t kGfChunk = 16384;  // elements of one copy (32 KB)
 constexpr int kGfRing = 6;           // chunk buffers (192 KB)
 constexpr int kGfRowQ = 2;           // claimed rows handed to the consumers
+constexpr int kGfZeroBytes = 16384;  // zeros the store warp copies over dropped rows
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -113,6 +116,24 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+
+// 1-D bulk copy of this CTA's shared memory to global memory with an L2
+// cache policy, in the thread's current bulk group (both addresses 16-byte
+// aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes, uint64_t policy) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(
+                   reinterpret_cast<uint64_t>(dst)),
+               "r"(src), "r"(bytes), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Waits until the bulk groups of this thread have read their shared-memory
+// sources (the buffers may then be rewritten).
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Waits until the bulk groups of this thread have completed their writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // 2^x by the SFU's approximation (PTX ex2.approx.ftz.f32: relative error
 // about 2^-22; results below 2^-126 flush to zero, far below any bound the
@@ -189,7 +210,8 @@ struct RowParams {
 // Shared memory after the chunk buffers.
 struct alignas(16) GfTail {
   uint64_t full[kGfRing];
-  uint64_t empty[kGfRing];
+  uint64_t consumed[kGfRing];  // the consumer warps are done with a chunk
+  uint64_t empty[kGfRing];     // the buffer may be refilled
   uint64_t rq_full[kGfRowQ];
   uint64_t rq_empty[kGfRowQ];
   int64_t rq_row[kGfRowQ];  // claimed row, or -1: no more rows for this CTA
@@ -271,12 +293,17 @@ __device__ __forceinline__ void online_add1(float& m, float& s, float x) {
 }
 
 // Warp 0 is the producer: lane 0 claims rows (atomic add on the counter),
-// hands each to the consumers through a queue of kGfRowQ entries and, for a
-// kept row, copies its chunks in order into the ring: the whole row for the
-// first pass, then the whole row again for the second (only the first when
-// no gradient is asked for).  Warps 1..16 are the consumers.  All consumer
-// threads wait on the same barriers and take every decision that ends the
-// loop together (consumers_any), so their barrier counts always match.
+// hands each to the other warps through a queue of kGfRowQ entries and, for
+// a kept row, copies its chunks in order into the ring: the whole row for
+// the first pass, then the whole row again for the second (only the first
+// when no gradient is asked for).  Warp 1 stores: it zero-fills the
+// gradient rows of dropped labels by bulk copies from a buffer of zeros,
+// and copies each gradient chunk the consumers left in shared memory to its
+// row with one bulk copy; it frees a buffer for the producer once the
+// consumers are done with it and its bulk copy has read it.  Warps 2..17
+// are the consumers.  All consumer threads wait on the same barriers and
+// take every decision that ends the loop together (consumers_any), so their
+// barrier counts always match.
 __global__ void __launch_bounds__(kGfThreads, 1)
     goldfish_rows_kernel(const __grid_constant__ RowParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -284,24 +311,29 @@ __global__ void __launch_bounds__(kGfThreads, 1)
   const int64_t T = a.batch * a.seq;
   const int64_t V = a.vocab;
   const int64_t vpad = (V + 7) & ~int64_t{7};
+  const int64_t vfull = V & ~int64_t{7};  // elements in whole 8-element vectors
   const int nch = p.chunks;
   const int passes = a.dlogits ? 2 : 1;
-  GfTail* tl = reinterpret_cast<GfTail*>(smem + kGfRing * kGfChunk * 2);
+  const uint32_t zeros = smem_addr(smem) + static_cast<uint32_t>(kGfRing * kGfChunk * 2);
+  GfTail* tl = reinterpret_cast<GfTail*>(smem + kGfRing * kGfChunk * 2 + kGfZeroBytes);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint64_t tmo = a.timeout_ns;
   auto buf = [&](int b) { return smem_addr(smem) + static_cast<uint32_t>(b * kGfChunk * 2); };
 
+  for (int i = threadIdx.x; i < kGfZeroBytes / 16; i += blockDim.x)
+    reinterpret_cast<int4*>(smem + kGfRing * kGfChunk * 2)[i] = make_int4(0, 0, 0, 0);
+  fence_proxy_async_shared();  // the zeros, for the bulk copies that read them
   if (threadIdx.x == 0) {
     for (int b = 0; b < kGfRing; ++b) {
       mbar_init(smem_addr(&tl->full[b]), 1);
-      mbar_init(smem_addr(&tl->empty[b]), kGfConsumerWarps);
+      mbar_init(smem_addr(&tl->consumed[b]), kGfConsumerWarps);
+      mbar_init(smem_addr(&tl->empty[b]), 1);
     }
     for (int q = 0; q < kGfRowQ; ++q) {
       mbar_init(smem_addr(&tl->rq_full[q]), 1);
-      mbar_init(smem_addr(&tl->rq_empty[q]), kGfConsumerWarps);
+      mbar_init(smem_addr(&tl->rq_empty[q]), kGfConsumerWarps + 1);
     }
-    tl->aborted = 0;
     fence_mbarrier_init();
   }
   __syncthreads();
@@ -349,18 +381,72 @@ __global__ void __launch_bounds__(kGfThreads, 1)
           }
         }
       }
-      // Copies the consumers did not take exist only after an expired wait:
-      // let them land (bounded) before this CTA's shared memory goes away.
-      if (!ok) {
-        tl->aborted = 1;
+      // Copies nobody took exist only after an expired wait: let them land
+      // (bounded) before this CTA's shared memory goes away.
+      if (!ok)
         for (int i = 0; i < kGfRing; ++i)
           if (uses[i] > 0) gf_wait(smem_addr(&tl->full[i]), (uses[i] - 1) & 1u, tmo, 3);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ stores
+    const uint64_t pol = evict_first_policy();
+    int b = 0, q = 0;
+    uint32_t ph = 0, qph = 0;
+    bool ok = true;
+    while (ok) {
+      ok = gf_warp_wait(smem_addr(&tl->rq_full[q]), qph, tmo, 6);
+      const int64_t r = tl->rq_row[q];
+      const bool keep = tl->rq_keep[q] != 0;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&tl->rq_empty[q]));
+      if (++q == kGfRowQ) {
+        q = 0;
+        qph ^= 1u;
+      }
+      if (!ok || r < 0) break;
+      uint16_t* out = a.dlogits ? a.dlogits + r * a.ld_dlogits : nullptr;
+      if (!keep) {
+        if (out) {
+          if (lane == 0) {
+            for (int64_t e = 0; e < vfull; e += kGfZeroBytes / 2)
+              bulk_store(out + e, zeros,
+                         static_cast<uint32_t>(min(int64_t{kGfZeroBytes / 2}, vfull - e) * 2), pol);
+            bulk_commit();
+          }
+          for (int64_t i = vfull + lane; i < V; i += 32) out[i] = 0;
+        }
+        continue;
+      }
+      for (int pass = 0; pass < passes && ok; ++pass) {
+        for (int c = 0; c < nch; ++c) {
+          ok = gf_warp_wait(smem_addr(&tl->consumed[b]), ph, tmo, 7);
+          if (!ok) break;
+          if (lane == 0) {
+            if (pass == 1) {
+              const int64_t e0 = c * kGfChunk;
+              const int64_t nb = max(int64_t{0}, min(kGfChunk, vfull - e0));  // whole vectors
+              if (nb > 0) {
+                bulk_store(out + e0, buf(b), static_cast<uint32_t>(nb * 2), pol);
+                bulk_commit();
+                bulk_wait_read();
+              }
+            }
+            mbar_arrive(smem_addr(&tl->empty[b]));
+          }
+          __syncwarp();
+          if (++b == kGfRing) {
+            b = 0;
+            ph ^= 1u;
+          }
+        }
       }
     }
+    // the gradient's bulk copies complete before the kernel does
+    if (lane == 0) bulk_wait_all();
   } else {
     // ------------------------------------------------------------ consumers
-    const int cw = warp - 1;          // consumer warp
-    const int ct = threadIdx.x - 32;  // consumer thread
+    const int cw = warp - 2;          // consumer warp
+    const int ct = threadIdx.x - 64;  // consumer thread
     const int32_t n = *a.kept;
     const float inv_n = n > 0 ? 1.0f / static_cast<float>(n) : 0.0f;
     const float log2n = n > 0 ? log2f(static_cast<float>(n)) : 0.0f;
@@ -368,15 +454,15 @@ __global__ void __launch_bounds__(kGfThreads, 1)
     uint32_t ph = 0, qph = 0;
     bool ok = true;  // this thread's waits all completed
     // waits for chunk b, passes it to f(x, e0, n_valid) when it arrived, and
-    // releases the buffer
+    // reports the warp done with it
     auto take_chunk = [&](int c, auto&& f) {
       const bool got = ok && gf_warp_wait(smem_addr(&tl->full[b]), ph, tmo, 4);
       ok = got;
       const int64_t e0 = c * kGfChunk;
       const int64_t nv = max(int64_t{0}, min(kGfChunk, V - e0));
-      if (got) f(reinterpret_cast<const uint16_t*>(smem + b * kGfChunk * 2), e0, nv);
+      if (got) f(reinterpret_cast<uint16_t*>(smem + b * kGfChunk * 2), e0, nv);
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&tl->empty[b]));
+      if (lane == 0) mbar_arrive(smem_addr(&tl->consumed[b]));
       if (++b == kGfRing) {
         b = 0;
         ph ^= 1u;
@@ -394,8 +480,7 @@ __global__ void __launch_bounds__(kGfThreads, 1)
         qph ^= 1u;
       }
       if (consumers_any(!ok || r < 0)) break;
-      if (!keep) {
-        if (a.dlogits) zero_row(a.dlogits + r * a.ld_dlogits, V, ct);
+      if (!keep) {  // the store warp writes its zero gradient row
         if (ct == 0) a.token_loss[r] = 0.0f;
         continue;
       }
@@ -403,18 +488,18 @@ __global__ void __launch_bounds__(kGfThreads, 1)
       float m0 = -INFINITY, s0 = 0.0f, m1 = -INFINITY, s1 = 0.0f;
       for (int c = 0; c < nch; ++c)
         take_chunk(c, [&](const uint16_t* x, int64_t e0, int64_t nv) {
-          const int64_t vfull = nv & ~int64_t{7};
-          for (int64_t i = 16 * ct; i < vfull; i += 16 * kGfConsumers) {
+          const int64_t vf = nv & ~int64_t{7};
+          for (int64_t i = 16 * ct; i < vf; i += 16 * kGfConsumers) {
             float xa[8];
             unpack8(*reinterpret_cast<const uint4*>(x + i), xa);
             online_add8(m0, s0, xa);
-            if (i + 8 < vfull) {
+            if (i + 8 < vf) {
               float xb[8];
               unpack8(*reinterpret_cast<const uint4*>(x + i + 8), xb);
               online_add8(m1, s1, xb);
             }
           }
-          for (int64_t i = vfull + ct; i < nv; i += kGfConsumers) online_add1(m1, s1, bf16_to_f32(x[i]));
+          for (int64_t i = vf + ct; i < nv; i += kGfConsumers) online_add1(m1, s1, bf16_to_f32(x[i]));
           if (ct == 0 && y >= e0 && y < e0 + nv) tl->zy = bf16_to_f32(x[y - e0]);
         });
       float m = fmaxf(m0, m1);
@@ -443,14 +528,16 @@ __global__ void __launch_bounds__(kGfThreads, 1)
       // (consumers_any) that every consumer reaches after these reads.
       if (!a.dlogits) continue;
       // 2. gradient: p / n = 2^(z log2e - (lse log2e + log2 n)), the 1/n
-      //    folded into the exponent; the label's entry less 1/n
+      //    folded into the exponent; the label's entry less 1/n.  Whole
+      //    vectors go back into the chunk's buffer for the store warp's bulk
+      //    copy; the row's last (V mod 8) elements are stored here.
       const float lb = fmaf(lse, kLog2e, log2n);
       uint16_t* out = a.dlogits + r * a.ld_dlogits;
       for (int c = 0; c < nch; ++c)
-        take_chunk(c, [&](const uint16_t* x, int64_t e0, int64_t nv) {
+        take_chunk(c, [&](uint16_t* x, int64_t e0, int64_t nv) {
           const int64_t yl = y - e0;  // the label's place in this chunk (may be outside)
-          const int64_t vfull = nv & ~int64_t{7};
-          for (int64_t i = 8 * ct; i < vfull; i += 8 * kGfConsumers) {
+          const int64_t vf = nv & ~int64_t{7};
+          for (int64_t i = 8 * ct; i < vf; i += 8 * kGfConsumers) {
             float g[8];
             unpack8(*reinterpret_cast<const uint4*>(x + i), g);
 #pragma unroll
@@ -461,16 +548,16 @@ __global__ void __launch_bounds__(kGfThreads, 1)
               for (int j = 0; j < 8; ++j)
                 if (j == d) g[j] -= inv_n;
             }
-            __stcs(reinterpret_cast<int4*>(out + e0 + i),
-                   make_int4(static_cast<int>(pack2(g[0], g[1])), static_cast<int>(pack2(g[2], g[3])),
-                             static_cast<int>(pack2(g[4], g[5])), static_cast<int>(pack2(g[6], g[7]))));
+            *reinterpret_cast<uint4*>(x + i) =
+                make_uint4(pack2(g[0], g[1]), pack2(g[2], g[3]), pack2(g[4], g[5]), pack2(g[6], g[7]));
           }
-          for (int64_t i = vfull + ct; i < nv; i += kGfConsumers) {
+          for (int64_t i = vf + ct; i < nv; i += kGfConsumers) {
             float gs = fast_exp2(fmaf(bf16_to_f32(x[i]), kLog2e, -lb));
             if (i == yl) gs -= inv_n;
             __nv_bfloat16 h = __float2bfloat16_rn(gs);
             out[e0 + i] = *reinterpret_cast<uint16_t*>(&h);
           }
+          fence_proxy_async_shared();  // these writes, for the store warp's bulk copy
         });
     }
   }
@@ -508,7 +595,7 @@ cudaError_t goldfish_launch(const GoldfishArgs& a, int sms, cudaStream_t stream)
     p.a = a;
     const int64_t vpad = (a.vocab + 7) / 8 * 8;
     p.chunks = static_cast<int>((vpad + kGfChunk - 1) / kGfChunk);
-    const int smem = static_cast<int>(kGfRing * kGfChunk * 2 + sizeof(GfTail));
+    const int smem = static_cast<int>(kGfRing * kGfChunk * 2 + kGfZeroBytes + sizeof(GfTail));
     e = cudaFuncSetAttribute(goldfish_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // Persistent: one CTA per SM, at most one per row.
