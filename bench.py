@@ -96,7 +96,7 @@ TUNED_DIR = os.path.join(ROOT, "pmm_fc_layer_gb300", "tuned")
 # in profiles/).  Reported only while the kernel sources hash to the value
 # the capture was taken with and every GEMM's choice of this run is in it.
 TRAFFIC = {
-    "workload": "gpt_h6144_t8192", "kernel_sources": "7d1573a93c8d0caa",
+    "workload": "gpt_h6144_t8192", "kernel_sources": "17f9e09df4a99f33",
     "bytes": {
         ("qkv:fwd", "pair_512x256/-8/88/0"): 2033709568,
         ("qkv:fwd", "pair_512x256/16/88/0"): 2480573696,
@@ -142,12 +142,22 @@ def traffic_per_launch(workload, per, only):
     return tot / len(per)
 
 
+def code_text(src):
+    """C++ source with comments removed and whitespace collapsed: the part
+    of a file that decides what the compiler builds."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_sources_hash():
+    """Hash of the GEMM kernels' code (comments and layout ignored)."""
     import hashlib
     h = hashlib.sha256()
     for name in ("gemm_kernel.cuh", "gemm_pair_kernel.cuh", "ptx.cuh", "kernel_instances.cuh"):
-        with open(os.path.join(ROOT, "pmm_fc_layer_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "pmm_fc_layer_gb300", "csrc", name)) as f:
+            h.update(code_text(f.read()).encode())
     return h.hexdigest()[:16]
 DATA = ("synthetic, seeded: SplitMix64 + Box-Muller bf16; activations/grads N(0,1), "
         "weights N(0,0.02)")

@@ -478,9 +478,11 @@ __device__ __forceinline__ void store_zero_row(const ProblemDesc& d, int row, in
 // `remote`).  A plain bf16 tile that lies wholly inside the output is first
 // packed into registers (BN / 2 words per thread) and TMEM is released
 // before any store, so the next tile's MMAs start while the stores drain;
-// its rows are stored as 32-byte vectors.  Other tiles (partials to add,
-// fp32 output, a ragged right edge, rows not 32-byte aligned) are stored
-// chunk by chunk and release TMEM afterwards.
+// its rows are stored as 32-byte vectors.  With kTransFast a transposed
+// bf16 tile (operand roles exchanged) whose warp rows and columns all lie
+// inside a 4-byte-aligned output does the same and stores column pairs as
+// 32-bit words.  Other tiles (partials to add, fp32 output, ragged edges,
+// misaligned rows) are stored chunk by chunk and release TMEM afterwards.
 template <int BN, bool kTransFast>
 __device__ __forceinline__ void drain_accumulator(const ProblemDesc& d, uint32_t t_row, int row,
                                                   int n0, uint32_t tempty, bool arrive,

@@ -230,3 +230,14 @@ def test_traffic_reported_only_for_captured_choices(monkeypatch):
         assert bench.traffic_per_launch("gpt_h6144_t8192", flipped, None) is None
     monkeypatch.setattr(bench, "kernel_sources_hash", lambda: "0" * 16)
     assert bench.traffic_per_launch("gpt_h6144_t8192", per, None) is None
+
+
+def test_kernel_hash_follows_code_not_comments():
+    """The traffic table is tied to the kernels' code: comments and layout
+    leave the hash alone, a changed token does not."""
+    a = "int f(int x) {  // doubles x\n  return 2 * x; /* fast\n path */ }\n"
+    b = "int f(int x) {\n    return 2 * x;\n}  // another note\n"
+    c = "int f(int x) { return 3 * x; }"
+    assert bench.code_text(a) == bench.code_text(b) == "int f(int x) { return 2 * x; }"
+    assert bench.code_text(c) != bench.code_text(a)
+    assert len(bench.kernel_sources_hash()) == 16
