@@ -358,8 +358,9 @@ axonn_status_t axonn_sync_status(cudaStream_t stream, uint64_t* detail);
 void axonn_set_wait_timeout_ns(uint64_t ns);
 
 /* Test hook: 1 makes the next launches' producer withhold all operand
- * loads, so the bounded waits expire and AXONN_ERR_TIMEOUT is reported;
- * 0 restores normal operation.  Never needed in production. */
+ * loads (the GEMM kernels' tiles, the Goldfish loss's kept rows), so the
+ * bounded waits expire and AXONN_ERR_TIMEOUT is reported; 0 restores normal
+ * operation.  Never needed in production. */
 void axonn_debug_set_inject(int mode);
 
 /* Kernel configurations.  The library chooses one per call from the

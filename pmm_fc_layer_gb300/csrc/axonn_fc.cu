@@ -1602,6 +1602,7 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
   a.dlogits = static_cast<uint16_t*>(dlogits);
   a.ld_dlogits = ld_dlogits;
   a.timeout_ns = g_timeout_ns.load();
+  a.inject = g_inject.load();
   const cudaError_t e = axonn::goldfish_launch(a, dev->sms, stream);
   if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "Goldfish loss launch: %s", cudaGetErrorString(e));
   return ok();

@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kGfThreads, 1)
           qph ^= 1u;
         }
         if (!more) break;
-        if (!keep) continue;
+        if (!keep || a.inject == 1) continue;  // (the test hook withholds every copy)
         const uint16_t* src = a.logits + r * a.ld_logits;
         for (int pass = 0; pass < passes && ok; ++pass) {
           for (int c = 0; c < nch; ++c) {

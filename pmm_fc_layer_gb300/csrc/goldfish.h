@@ -22,6 +22,7 @@ struct GoldfishArgs {
   uint16_t* dlogits;   // bf16 [T x V] or null, row stride ld_dlogits
   int64_t ld_dlogits;
   uint64_t timeout_ns;
+  int32_t inject;  // 1: the rows kernel withholds every copy (a test of the bounded waits)
 };
 
 // Largest vocabulary the entry point accepts (8 x 49152 tokens).

@@ -142,6 +142,35 @@ def test_goldfish_extreme_logits(cuda_lib):
     _check(got, gf.goldfish_ce(logits, ids, labels, 0, 13), V, logits)
 
 
+def test_goldfish_bounded_wait_timeout_reports_and_recovers(cuda_lib):
+    """The rows kernel's producer withholds every copy: the consumers' waits
+    expire, every role of every CTA leaves within a few limits, the library
+    reports AXONN_ERR_TIMEOUT, and the next call is correct."""
+    fc = cuda_lib
+    V = 20000
+    ids, labels, logits = _problem(2, 200, V, 304)
+    try:
+        fc.axonn_set_wait_timeout_ns(20_000_000)
+        fc.axonn_debug_set_inject(1)
+        with pytest.raises(fc.AxonnError) as ei:
+            _run(fc, ids, labels, logits, 2, 13)
+        assert ei.value.status == fc.ERR_TIMEOUT
+    finally:
+        fc.axonn_debug_set_inject(0)
+        fc.axonn_set_wait_timeout_ns(4_000_000_000)
+    got = _run(fc, ids, labels, logits, 2, 13)
+    _check(got, gf.goldfish_ce(logits, ids, labels, 2, 13), V, logits)
+
+
+def test_goldfish_fewer_rows_than_sms(cuda_lib):
+    """One row, and a few: one CTA per row, the rest of the GPU idle."""
+    fc = cuda_lib
+    for B, S in ((1, 1), (1, 7)):
+        ids, labels, logits = _problem(B, S, 3000, 305 + S)
+        got = _run(fc, ids, labels, logits, 0, 13)
+        _check(got, gf.goldfish_ce(logits, ids, labels, 0, 13), 3000, logits)
+
+
 def test_goldfish_validation(cuda_lib):
     import torch
     fc = cuda_lib
