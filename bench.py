@@ -41,7 +41,7 @@ if ROOT not in sys.path:
 
 METRIC = "TFLOP/s per FC GEMM (fwd/dgrad/wgrad) and % of GB300 dense bf16 peak, 1 GPU"
 UNIT = "TFLOP/s"
-CPU_STRIPE_ROWS = 16      # output rows of every GEMM the CPU oracle computes per sample
+CPU_STRIPE_ROWS = 64      # output rows of every GEMM the CPU oracle computes per sample
 CPU_FULL_STEP_FLOPS = 50e9  # steps up to this size are computed whole by the CPU oracle
 L2_FLUSH_BYTES = 512 << 20
 
