@@ -220,7 +220,6 @@ struct alignas(16) GfTail {
   float red_m[kGfConsumerWarps];
   float red_s[kGfConsumerWarps];
   float zy;  // the label's logit of the row in progress
-  int aborted;
 };
 
 // Barrier among the consumer warps only (the producer warp runs ahead).
@@ -255,15 +254,6 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&x)[8]) {
   x[5] = __uint_as_float(v.z & 0xFFFF0000u);
   x[6] = __uint_as_float(v.w << 16);
   x[7] = __uint_as_float(v.w & 0xFFFF0000u);
-}
-
-// Writes zeros to elements [0, n) of a gradient row (16-byte stores for the
-// whole vectors, single elements for the tail), by the consumer threads.
-__device__ __forceinline__ void zero_row(uint16_t* row, int64_t n, int ct) {
-  const int64_t v1 = n & ~int64_t{7};
-  for (int64_t i = 8 * ct; i < v1; i += 8 * kGfConsumers)
-    __stcs(reinterpret_cast<int4*>(row + i), make_int4(0, 0, 0, 0));
-  for (int64_t i = v1 + ct; i < n; i += kGfConsumers) row[i] = 0;
 }
 
 // Adds values to one thread's running (max, sum of exp(x - max)).
