@@ -207,7 +207,7 @@ struct RowParams {
   int chunks;  // copies per row: ceil(vpad / kGfChunk), vpad = V rounded up to 8
 };
 
-// Shared memory after the chunk buffers.
+// Shared memory after the chunk buffers and the zeros.
 struct alignas(16) GfTail {
   uint64_t full[kGfRing];
   uint64_t consumed[kGfRing];  // the consumer warps are done with a chunk
@@ -222,7 +222,8 @@ struct alignas(16) GfTail {
   float zy;  // the label's logit of the row in progress
 };
 
-// Barrier among the consumer warps only (the producer warp runs ahead).
+// Barrier among the consumer warps only (the producer and store warps run
+// on their own).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kGfConsumers) : "memory");
 }
