@@ -1,5 +1,6 @@
-"""GPU parity at the full sizes of the FC workloads, in the launch
-configuration the benchmark times (the library's own kernel choice).
+"""GPU parity at the full sizes of the FC workloads, in the library's own
+kernel choice and, for the GPT block, also in the choices of the tuning
+table shipped for it, which are the launches the benchmark times.
 
 The fp64 oracle is too slow for whole products of this size, so each check
 covers the entries the oracle can compute one by one: 2 full rows, 2 full
@@ -74,6 +75,41 @@ def test_gpt_block_h6144_t8192(cuda_lib, gpt6144, layer, op):
     X, W, dY = gpt6144[layer]
     _run_and_check(cuda_lib, op, X, W, dY, T6, K, N, n_random=32768,
                    seed=zlib.crc32(f"{layer}:{op}".encode()) & 0xFFFF)
+
+
+@pytest.fixture
+def shipped_table(cuda_lib):
+    """Loads the GPT block's shipped tuning table; clears it afterwards."""
+    import json
+    import os
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                        "pmm_fc_layer_gb300", "tuned", "gpt_h6144_t8192.jsonl")
+    fc = cuda_lib
+    fc.axonn_tune_cache_clear()
+    fc.axonn_tune_cache_load(path)
+    yield {json.loads(l)["key"]: json.loads(l) for l in open(path).read().splitlines() if l.strip()}
+    fc.axonn_tune_cache_clear()
+
+
+@pytest.mark.parametrize("layer", list(LAYERS6))
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+def test_gpt_block_h6144_t8192_shipped_choices(cuda_lib, gpt6144, shipped_table, layer, op):
+    """Each GEMM runs the shipped table's configuration, rasterisation group,
+    split and operand roles (with its stream-K mode), and is checked like
+    the default choice above."""
+    fc = cuda_lib
+    sms, _ = fc.axonn_device_info()
+    K, N = LAYERS6[layer]
+    key = f"op{fc.OPS[op]}_T{T6}_K{K}_N{N}_g1x1x1_at0.0.0_f0_sm{sms}"
+    if key not in shipped_table:
+        pytest.skip(f"the shipped table is for another SM count ({sms} SMs here)")
+    X, W, dY = gpt6144[layer]
+    _run_and_check(fc, op, X, W, dY, T6, K, N, n_random=32768,
+                   seed=zlib.crc32(f"shipped {layer}:{op}".encode()) & 0xFFFF)
+    want = shipped_table[key]
+    assert fc.axonn_kernel_config_name(fc.axonn_last_choice()[0]) == want["config"]
+    assert fc.axonn_last_choice()[1:] == (want["split"], want["group_m"])
+    assert fc.axonn_last_swap() == want["swap"]
 
 
 @pytest.mark.parametrize("form", ["chained", "partials"])
