@@ -274,7 +274,10 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
  * operand roles exchanged (see axonn_set_swap) -- and times each (through a captured
  * CUDA graph of 3 calls, 20 for products under 2e10 FLOP, where the stream
  * allows it) relative to the default choice run just before and after it,
- * so clock drift under the power cap cancels.  The
+ * so clock drift under the power cap cancels.  For products of 2e11 FLOP or
+ * more, a candidate within 2 % of the fastest that loads fewer operand
+ * bytes from L2 per multiply-add is kept instead (under the power cap those
+ * bytes cost clock in a long run, which short timings do not show).  The
  * call synchronises `stream`.  It
  * records the fastest for later calls with the same op, sizes, grid, block
  * and flags on a GPU with the same SM count.  Arguments are those of the

@@ -612,6 +612,19 @@ axonn_status_t run_blocks(const OpView& v, const LaunchPlan& plan, const DeviceS
   return launch_cfg<kMaxProblems>(plan.config, v, plan, dev, stream);
 }
 
+// Operand bytes a CTA loads from L2 per multiply-add: its A rows and its
+// share of B's columns per stage, over the stage's multiply-adds.
+double operand_bytes_per_mac(const KernelConfig& c) {
+  const double rows = c.pair ? c.bm / 2 : c.bm;
+  const double cols = c.pair ? c.bn / 2 : c.bn;
+  return 2.0 * (rows + cols) / (rows * c.bn);
+}
+// Products of at least this many FLOP run long enough (about 0.1 ms and
+// more) for the power cap to set the clock; within kPowerTie of the fastest
+// timed candidate, the tuner prefers the one that moves fewer operand bytes.
+constexpr double kPowerBoundFlops = 2e11;
+constexpr double kPowerTie = 0.02;
+
 // Work units (tile slots) a configuration needs, counted in waves of the
 // units the GPU runs at once; the rounding up is the wave-quantisation loss.
 double config_cost(const std::vector<Block>& blocks, const KernelConfig& c, const DeviceState& dev) {
@@ -1329,6 +1342,30 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
       best.us = cand_us[i];
       best.choice = cands[i];
     }
+  // Products long enough for the power cap to set the clock: a candidate
+  // within kPowerTie of the fastest that moves fewer operand bytes from L2
+  // per multiply-add is taken instead.  The timing runs above are too short
+  // for the cap to act, and L2-to-SM traffic costs clock in a long step
+  // (measured: loading every A tile twice cost 3 % of SM clock).
+  if (best.us >= 0 && flops >= kPowerBoundFlops) {
+    const double limit = best_ratio * (1.0 + kPowerTie);
+    size_t pick = cands.size();
+    double pick_bytes = operand_bytes_per_mac(kConfigs[best.choice.config]);
+    for (size_t i = 0; i < cands.size(); ++i) {
+      if (cand_ratio[i] < 0 || cand_ratio[i] > limit) continue;
+      const double b = operand_bytes_per_mac(kConfigs[cands[i].config]);
+      if (b < pick_bytes * 0.99 ||
+          (pick < cands.size() && b <= pick_bytes * 1.01 && cand_ratio[i] < cand_ratio[pick])) {
+        pick = i;
+        pick_bytes = b;
+      }
+    }
+    if (pick < cands.size()) {
+      best_ratio = cand_ratio[pick];
+      best.us = cand_us[pick];
+      best.choice = cands[pick];
+    }
+  }
   // Exchanged operand roles (C^T = B^T . A^T): the two best candidates are
   // timed again with the roles swapped, each between reference runs like
   // the others, and a swapped one is kept where it scores better.
