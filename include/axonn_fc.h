@@ -268,7 +268,8 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
  * arXiv 2502.08145).  Runs this call once per candidate -- kernel
  * configuration x rasterisation group {8, 16 tile rows; 8, 16 tile columns,
  * written -8, -16}, every configuration for products that leave SMs idle
- * (with reduction splits {2, 4, 8} of the 128x128 configuration, each piece
+ * (with reduction splits {2, 4, 8} of the 128x128 and 128x64
+ * configurations, each piece
  * at least 128 deep), the 128x256 and 256-row configurations otherwise,
  * and the two best of them again with the
  * operand roles exchanged (see axonn_set_swap) -- and times each (through a captured
@@ -297,7 +298,8 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
  *   {"key": "...", "config": "<name>", "split": S, "group_m": G,
  *    "streamk": 0 | 1 | 2, "swap": 0 | 1, "us": t}
  * (S a whole number 1..8, run as the largest power of two not above it
- * or the product's stage count, and only on the 128x128 configuration;
+ * or the product's stage count, and only on the 128x128 and 128x64
+ * configurations;
  * G a whole number in -64..-1 or 1..64, tile rows
  * per rasterisation group, negative for tile columns; streamk: off, on for
  * a partial round at most a quarter full, on wherever it applies; a line
@@ -377,8 +379,13 @@ void axonn_debug_set_inject(int mode);
  *                        per B slice), 3 stages, single-buffered TMEM
  *   4  1cta_128x192      one CTA per 128x192 output tile, 5 stages
  *   5  1cta_256x192      one CTA per 256x192 output tile, 4 stages
+ *   6  pair_512x256      a CTA pair per 512x256 output tile (each CTA two
+ *                        M=128 halves of 256 columns), 4 stages, 12 warps
+ *   7  1cta_128x64       one CTA per 128x64 output tile, 8 stages (for
+ *                        products with too few larger tiles)
  * (the N=192 tiles trade a little operand reuse for fewer idle SMs in the
- * last wave on shapes such as 8192 x 6144) 
+ * last wave on shapes such as 8192 x 6144; configurations 0 and 7 also run
+ * the reduction split inside a cluster)
  * axonn_set_kernel_config(c) forces configuration c for all later calls in
  * the process (-1 restores automatic choice); AXONN_ERR_INVALID_ARG if c is
  * out of range.  axonn_last_kernel_config() is the configuration the last

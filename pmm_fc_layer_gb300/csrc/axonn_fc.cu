@@ -77,9 +77,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 struct DeviceState {
   int sms = 0;
   int max_pairs = 0;  // CTA pairs (clusters of 2) resident at once
-  // Clusters of the reduction-split kernel resident at once, by pieces:
-  // [1] 2 pieces, [2] 4, [3] 8.
-  int split_clusters[4] = {0, 0, 0, 0};
+  // Clusters of the reduction-split kernels resident at once, by tile
+  // ([0] 128 x 128, [1] 128 x 64) and pieces ([1] 2, [2] 4, [3] 8).
+  int split_clusters[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
   bool attrs_set = false;
 };
 
@@ -135,14 +135,16 @@ axonn_status_t device_state(DeviceState** out) {
     e = axonn::split_kernel_init();
     if (e != cudaSuccess)
       return fail(AXONN_ERR_CUDA, "split kernel attributes: %s", cudaGetErrorString(e));
-    for (int lg = 1; lg <= 3; ++lg) {
-      int n = 0;
-      if (axonn::split_clusters_resident(d.sms, 1 << lg, &n) != cudaSuccess || n <= 0) {
-        (void)cudaGetLastError();
-        n = 0;  // this split is not offered on the device
+    for (int t = 0; t < 2; ++t)
+      for (int lg = 1; lg <= 3; ++lg) {
+        int n = 0;
+        if (axonn::split_clusters_resident(d.sms, 1 << lg, t == 0 ? 128 : 64, &n) != cudaSuccess ||
+            n <= 0) {
+          (void)cudaGetLastError();
+          n = 0;  // this split is not offered on the device
+        }
+        d.split_clusters[t][lg] = n;
       }
-      d.split_clusters[lg] = n;
-    }
     d.attrs_set = true;
   }
   *out = &d;
@@ -565,6 +567,13 @@ axonn_status_t configure_streamk(GemmParams<MAXP>& P, const KernelConfig& c, int
   return AXONN_OK;
 }
 
+// The reduction split runs on configurations 0 (128 x 128 tiles) and 7
+// (128 x 64): the kernels that hold a split tile's staging rows and inbox
+// beside their operand rings.  Index of the configuration's split kernel.
+bool split_config(int c) { return c == 0 || c == 7; }
+int split_index(int c) { return c == 7 ? 1 : 0; }
+int split_lg(int split) { return split == 2 ? 1 : (split == 4 ? 2 : 3); }
+
 // One launch of configuration `config` over the plan's blocks: the
 // persistent grid is one unit (CTA, or CTA pair) per resident slot, or one
 // per tile when there are fewer tiles.
@@ -581,14 +590,15 @@ axonn_status_t launch_cfg(int config, const OpView& v, const LaunchPlan& plan,
     // cluster at a time, as many clusters as are resident at once.
     t_last_sk_tiles = 0;
     if constexpr (P1 == 1) {
-      const int lg = plan.split == 2 ? 1 : (plan.split == 4 ? 2 : 3);
-      const int resident = dev.split_clusters[lg];
-      if (config != 0 || P.num_problems != 1 || resident <= 0 || (plan.split & (plan.split - 1)) ||
+      if (!split_config(config) || P.num_problems != 1 || (plan.split & (plan.split - 1)) ||
           plan.split > 8)
         return fail(AXONN_ERR_UNSUPPORTED, "reduction split of %d pieces not available here", plan.split);
+      const int resident = dev.split_clusters[split_index(config)][split_lg(plan.split)];
+      if (resident <= 0)
+        return fail(AXONN_ERR_UNSUPPORTED, "reduction split of %d pieces not available here", plan.split);
       const int clusters = P.total_tiles < resident ? P.total_tiles : resident;
-      const cudaError_t e =
-          axonn::split_kernel_launch(P, plan.split, clusters, g_pdl.load() != 0, stream);
+      const cudaError_t e = axonn::split_kernel_launch(P, plan.split, clusters, kConfigs[config].bn,
+                                                       g_pdl.load() != 0, stream);
       if (e != cudaSuccess) return fail(AXONN_ERR_CUDA, "split GEMM launch: %s", cudaGetErrorString(e));
       return AXONN_OK;
     } else {
@@ -663,10 +673,6 @@ bool underfilled(int64_t M, int64_t N, const DeviceState& dev) {
 bool split_eligible(int64_t M, int64_t N, int64_t R, const DeviceState& dev) {
   return underfilled(M, N, dev) && R >= 4 * kSplitMinR;
 }
-
-// The reduction split runs on configuration 0 (128 x 128 tiles) only: the
-// kernel that holds a split tile's inbox beside its operand ring.
-bool split_config(int c) { return c == 0; }
 
 // The split actually run for a request of `want` pieces over nk reduction
 // steps: a power of two (the tile's 128 rows are dealt out in equal bands),
@@ -906,7 +912,7 @@ axonn_status_t fc_op(int op, const void* P, const void* Q, void* C, int64_t ldp,
     const Block& b0 = plan.blocks[0];
     const bool able = !vgrid && plan.blocks.size() == 1 && split_config(ch.config);
     ch.split = able ? split_pieces(ch.split, (b0.R + 63) / 64) : 1;
-    if (ch.split > 1 && dev->split_clusters[ch.split == 2 ? 1 : (ch.split == 4 ? 2 : 3)] <= 0)
+    if (ch.split > 1 && dev->split_clusters[split_index(ch.config)][split_lg(ch.split)] <= 0)
       ch.split = 1;
   }
   // Exchanged operand roles: C^T[N x M] = B^T . A^T, the same operands read
@@ -1244,7 +1250,8 @@ axonn_status_t axonn_fc_tune(int op, const void* P, const void* Q, void* C, int6
   if (!(flags & AXONN_VGRID) && splittable)
     for (int sp = 2; sp <= kMaxSplit; sp *= 2)
       if (red.len() / sp >= kSplitMinR)
-        for (int gm : {16, -16}) cands.push_back(TuneChoice{0, sp, gm});
+        for (int c : {0, 7})
+          for (int gm : {16, -16}) cands.push_back(TuneChoice{c, sp, gm});
 
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (cudaEventCreate(&e0) != cudaSuccess || cudaEventCreate(&e1) != cudaSuccess) {

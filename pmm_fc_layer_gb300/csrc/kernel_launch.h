@@ -39,13 +39,14 @@ cudaError_t kernels_take_status(unsigned long long* word, cudaStream_t stream);
 // Clusters of 2 of the pair kernels that can be resident at once.
 cudaError_t pair_clusters_resident(int sms, int* clusters);
 
-// The reduction-split kernel (128 x 128 tiles, one problem; see
-// fc_gemm_tcgen05_kernel's kSplit): its shared-memory limit, how many of
-// its clusters of `pieces` CTAs (2, 4 or 8) can be resident at once, and a
-// launch of `clusters` such clusters.
+// The reduction-split kernels (one problem; see fc_gemm_tcgen05_kernel's
+// kSplit), with 128 x 128 tiles (bn = 128) or 128 x 64 tiles (bn = 64):
+// their shared-memory limits, how many of their clusters of `pieces` CTAs
+// (2, 4 or 8) can be resident at once, and a launch of `clusters` such
+// clusters.
 cudaError_t split_kernel_init();
-cudaError_t split_clusters_resident(int sms, int pieces, int* clusters);
-cudaError_t split_kernel_launch(const GemmParams<1>& P, int pieces, int clusters, bool pdl,
+cudaError_t split_clusters_resident(int sms, int pieces, int bn, int* clusters);
+cudaError_t split_kernel_launch(const GemmParams<1>& P, int pieces, int clusters, int bn, bool pdl,
                                 cudaStream_t stream);
 
 }  // namespace axonn

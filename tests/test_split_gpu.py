@@ -1,6 +1,7 @@
 """GPU parity of the reduction split: a tile's reduction cut into S pieces
 (S = 2, 4, 8) computed by the S CTAs of one thread-block cluster and added
-in fixed order inside it, each CTA finishing a band of 128/S rows.  Bit for
+in fixed order inside it, each CTA finishing a band of 128/S rows, on
+128 x 128 tiles (configuration 0) and 128 x 64 tiles (configuration 7).  Bit for
 bit on integer inputs for every split, storage layout, output mode, ragged
 shape, block of the grid and with the operand roles exchanged; several
 tiles per cluster (the inbox reused); within the bound on random inputs.
@@ -26,13 +27,14 @@ def force_split(cuda_lib, tmp_path):
     split into `split` pieces; clears the table afterwards."""
     fc = cuda_lib
 
-    def force(op, T, K, N, flags, split, group_m=16, grid=(1, 1, 1), coords=(0, 0, 0), swap=0):
+    def force(op, T, K, N, flags, split, group_m=16, grid=(1, 1, 1), coords=(0, 0, 0), swap=0,
+              config="1cta_128x128"):
         sms, _ = fc.axonn_device_info()
         g = "x".join(str(v) for v in grid)
         at = ".".join(str(v) for v in coords)
         key = f"op{fc.OPS[op]}_T{T}_K{K}_N{N}_g{g}_at{at}_f{flags:x}_sm{sms}"
         path = tmp_path / "split.jsonl"
-        path.write_text(json.dumps({"key": key, "config": "1cta_128x128", "split": split,
+        path.write_text(json.dumps({"key": key, "config": config, "split": split,
                                     "group_m": group_m, "streamk": 1, "swap": swap,
                                     "us": 1.0}) + "\n")
         fc.axonn_tune_cache_load(str(path))
@@ -168,7 +170,51 @@ def test_split_single_layer_random(cuda_lib, force_split, op, split):
     assert_within_bound(host_f64(out), C, S, f"split {op}")
 
 
-def test_split_only_on_the_128x128_configuration(cuda_lib, force_split):
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("op", ["fwd", "dgrad", "wgrad"])
+@pytest.mark.parametrize("p_t,q_t", [(False, False), (True, True)])
+def test_split_128x64_integer_exact(cuda_lib, force_split, split, op, p_t, q_t):
+    """The same split on 128 x 64 tiles: bit for bit, ragged in every
+    dimension."""
+    fc = cuda_lib
+    T, K, N = 300, 1000, 520
+    if op == "wgrad":
+        T, K, N = 1000, 300, 520
+    pn, qn = operand_names(op)
+    P = make_operand(pn, T, K, N, p_t, seed=721, kind="int")
+    Q = make_operand(qn, T, K, N, q_t, seed=721, kind="int")
+    flags = (fc.A_T if p_t else 0) | (fc.B_T if q_t else 0)
+    force_split(op, T, K, N, flags, split, config="1cta_128x64")
+    out = run_gpu(fc, op, P, Q, p_t, q_t, T, K, N, workspace=False)
+    assert fc.axonn_last_choice()[:2] == (7, split)
+    C, _ = oracle.fc(op, P, Q, p_t, q_t)
+    bad = np.argwhere(host_bits(out) != oracle.bf16_rne(C))
+    assert bad.size == 0, f"{len(bad)} mismatches, first at {bad[:5].tolist()}"
+
+
+@pytest.mark.parametrize("split", [2, 8])
+def test_split_128x64_many_tiles_and_single_layer(cuda_lib, force_split, split):
+    """128 x 64 tiles: more tiles than resident clusters (the inbox reused),
+    and the single layer's data gradient within the bound."""
+    fc = cuda_lib
+    T, K, N = 2048, 1024, 2040
+    X = make_operand("X", T, K, N, False, seed=723, kind="int")
+    W = make_operand("W", T, K, N, False, seed=723, kind="int")
+    force_split("fwd", T, K, N, 0, split, config="1cta_128x64")
+    out = run_gpu(fc, "fwd", X, W, False, False, T, K, N, workspace=False)
+    assert fc.axonn_last_choice()[:2] == (7, split)
+    assert np.array_equal(host_bits(out), oracle.bf16_rne(oracle.fc_fwd(X, W)[0]))
+    T, K, N = 256, 512, 2048
+    dY = make_operand("dY", T, K, N, False, seed=1001)
+    Wr = make_operand("W", T, K, N, False, seed=1001)
+    force_split("dgrad", T, K, N, 0, split, config="1cta_128x64")
+    out = run_gpu(fc, "dgrad", dY, Wr, False, False, T, K, N, workspace=False)
+    assert fc.axonn_last_choice()[:2] == (7, split)
+    C, S = oracle.fc("dgrad", dY, Wr)
+    assert_within_bound(host_f64(out), C, S, "split dgrad on 128 x 64 tiles")
+
+
+def test_split_not_on_other_configurations(cuda_lib, force_split):
     fc = cuda_lib
     T, K, N = 256, 2048, 512
     dY = make_operand("dY", T, K, N, False, seed=707, kind="int")

@@ -59,8 +59,8 @@ def test_small_layer_splits_reduction(clean_cache, op):
 
 def test_every_split_and_config_exact(clean_cache, tmp_path):
     """Drive each (config, split, group) through a loaded tuning entry.  The
-    reduction split runs on configuration 0 (128 x 128 tiles); the others
-    run such an entry unsplit."""
+    reduction split runs on configurations 0 and 7 (128 x 128 and 128 x 64
+    tiles); the others run such an entry unsplit."""
     fc = clean_cache
     T, K, N = 300, 1000, 520
     P = make_operand("X", T, K, N, False, seed=103, kind="int")
@@ -76,7 +76,7 @@ def test_every_split_and_config_exact(clean_cache, tmp_path):
                                             "split": split, "group_m": gm, "us": 1.0}) + "\n")
                 fc.axonn_tune_cache_load(str(path))
                 out, choice, _ = _call(fc, "fwd", P, Q, T, K, N)
-                assert choice == (cfg, split if cfg == 0 else 1, gm)
+                assert choice == (cfg, split if cfg in (0, 7) else 1, gm)
                 bad = np.argwhere(host_bits(out) != want)
                 assert bad.size == 0, (cfg, split, gm, bad[:3].tolist())
 
