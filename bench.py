@@ -1142,6 +1142,9 @@ def run_ours(args):
                     if args.order_free else "; grid partials summed in fixed order"
                     if grid != (1, 1, 1) else "")),
             "per_gemm": per,
+            "per_gemm_note": ("each GEMM's rate from replays of that GEMM alone, after the timed "
+                              "steps; the SM clock under the power cap differs from the step's "
+                              "and is not sampled per GEMM"),
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1),
                          "peak": peaks["burst"], "unit": "TFLOP/s",
                          "frac": round(achieved / peaks["burst"], 4),
