@@ -263,9 +263,9 @@ axonn_status_t axonn_goldfish_ce(const void* logits, int64_t ld_logits, const in
                                  cudaStream_t stream);
 
 /*
- * Per-shape tuning -- the GB300 counterpart of the pages' "automated BLAS
- * kernel tuning" (TL;DR of the sciencestack.ai page; "The reading", review of
- * arXiv 2502.08145).  Runs this call once per candidate -- kernel
+ * Per-shape tuning -- the GB300 counterpart of the automatic tuning of BLAS
+ * kernels that the pages credit (TL;DR of the sciencestack.ai page; "The
+ * reading", review of arXiv 2502.08145).  Runs this call once per candidate -- kernel
  * configuration x rasterisation group {8, 16 tile rows; 8, 16 tile columns,
  * written -8, -16}, every configuration for products that leave SMs idle
  * (with reduction splits {2, 4, 8} of the 128x128 and 128x64
@@ -369,7 +369,7 @@ void axonn_set_wait_timeout_ns(uint64_t ns);
 void axonn_debug_set_inject(int mode);
 
 /* Kernel configurations.  The library chooses one per call from the
- * problem's tile counts (the pages' "automated BLAS kernel tuning": review of
+ * problem's tile counts (the pages' automatic BLAS kernel tuning: review of
  * arXiv 2502.08145, "The reading"); these calls expose the choice.
  *   0  1cta_128x128      one CTA per 128x128 output tile, 64-deep stages
  *   1  1cta_128x256      one CTA per 128x256 output tile, 64-deep stages
@@ -420,8 +420,8 @@ axonn_status_t axonn_set_streamk(int mode);
  * in the second's, and the epilogue writes each tile back transposed, so
  * the caller's output is the same matrix.  The tuner times the swap for the
  * two best configurations of each call, the row-major BLAS counterpart of
- * choosing among NN, NT and TN operand orders (the pages' "automated BLAS
- * kernel tuning": TL;DR of the sciencestack.ai page; review of arXiv
+ * choosing among NN, NT and TN operand orders (the pages' automatic BLAS
+ * kernel tuning: TL;DR of the sciencestack.ai page; review of arXiv
  * 2502.08145, "The reading").  It does not apply with AXONN_VGRID_PARTIALS.
  * Results may differ from the unswapped call in the
  * last bit (another tile order of the same fp32 sums).  Host-only;
