@@ -241,3 +241,27 @@ def test_kernel_hash_follows_code_not_comments():
     assert bench.code_text(a) == bench.code_text(b) == "int f(int x) { return 2 * x; }"
     assert bench.code_text(c) != bench.code_text(a)
     assert len(bench.kernel_sources_hash()) == 16
+
+
+def test_shipped_table_choices_have_captured_traffic():
+    """The default line runs the tuning table shipped for its workload; each
+    of its choices has captured DRAM bytes in the traffic table, so the
+    line reports roofline.traffic (a retuned table needs a new capture)."""
+    import json
+    path = os.path.join(bench.TUNED_DIR, f"{bench.DEFAULT_WORKLOAD}.jsonl")
+    entries = [json.loads(l) for l in open(path).read().splitlines() if l.strip()]
+    assert len(entries) == 12
+    names = {0: "fwd", 1: "dgrad", 2: "wgrad"}
+    layers = {(T, K, N): name for name, T, K, N in bench.WORKLOADS[bench.DEFAULT_WORKLOAD]["layers"]}
+    for e in entries:
+        key = e["key"]
+        op = int(key.split("_")[0][2:])
+        T, K, N = (int(key.split("_")[i][1:]) for i in (1, 2, 3))
+        gemm = f"{layers[(T, K, N)]}:{names[op]}"
+        # the stream-K tiles of a choice are fixed by its mode and the shape;
+        # every capture of this GEMM in this configuration, group and roles
+        # is listed with the tiles it ran
+        prefix = f"{e['config']}/{e['group_m']}/"
+        suffix = f"/{e['swap']}"
+        assert any(g == gemm and c.startswith(prefix) and c.endswith(suffix)
+                   for (g, c) in bench.TRAFFIC["bytes"]), (gemm, e)
